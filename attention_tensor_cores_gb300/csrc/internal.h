@@ -1,0 +1,70 @@
+// Host-side helpers shared by the library's translation units: error reporting, the device
+// status word, bounded-wait limit, TMA tensor-map encoding, and the launch functions each
+// kernel file exports to the C-ABI layer (api.cu).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+#include <string>
+
+#include "../../include/fmha.h"
+
+namespace fmha {
+
+// ---- errors ------------------------------------------------------------------------------
+int set_error(int code, const std::string& msg);  // records msg for fmha_last_error(), returns code
+int cuda_error(cudaError_t e, const char* what);  // FMHA_ERR_CUDA with the CUDA message
+#define FMHA_CHECK_CUDA(expr)                                      \
+    do {                                                           \
+        cudaError_t e__ = (expr);                                  \
+        if (e__ != cudaSuccess) return ::fmha::cuda_error(e__, #expr); \
+    } while (0)
+#define FMHA_CHECK_LAUNCH(what)                                                 \
+    do {                                                                        \
+        cudaError_t e__ = cudaGetLastError();                                   \
+        if (e__ != cudaSuccess) return ::fmha::cuda_error(e__, what);           \
+    } while (0)
+
+// ---- device status word and wait limit -------------------------------------------------------
+int* device_status_ptr();   // device address of the library's status word (current device)
+long long wait_limit();     // cycles
+int num_sms();              // SMs of the current device
+
+// ---- TMA ---------------------------------------------------------------------------------------
+// Encodes a tiled map over a BF16 tensor with up to 3 dims (dim 0 innermost), 128-byte swizzle,
+// out-of-bounds elements filled with zero.  dims/box in elements, strides in bytes (dims 1..).
+int make_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                   const uint64_t* strides_bytes, const uint32_t* box);
+
+// ---- launchers (each validates nothing: api.cu has done it) ----------------------------------
+int launch_qk_gemm(const void* q, const void* k, float* s, int Sq, int Skv, int D, cudaStream_t st);
+int launch_selftest(int which, const void* in, void* out, size_t out_bytes, int param, cudaStream_t st);
+
+struct AttnArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    void* out;          // final output (BF16 / F32) or NULL when the output is NVFP4
+    float* lse;         // may be NULL
+    int B, Hq, Hkv, Sq, Skv, D;
+    float scale;
+    const int32_t* seqlens;  // device, may be NULL
+    int out_kind;            // FMHA_OUT_*
+    float* out_f32;          // FP32 O destination (NVFP4 path), else NULL
+    float* amax_slot;        // NVFP4 path: |O| max accumulator (uint bits), else NULL
+};
+
+// Decode / small-group path (query rows per key/value head <= 16): swap-AB kernels.
+size_t decode_workspace_bytes(const AttnArgs& a, int splits_mode);
+int launch_decode(const AttnArgs& a, int num_splits, void* ws, size_t ws_bytes, cudaStream_t st);
+
+// Row-tile path (128 query rows per tile): prefill and wide-head decode.
+size_t prefill_workspace_bytes(const AttnArgs& a);
+int launch_prefill(const AttnArgs& a, void* ws, size_t ws_bytes, cudaStream_t st);
+
+// NVFP4
+int launch_nvfp4(const float* x, uint8_t* codes, uint8_t* scales, float* tensor_scale, unsigned* amax_bits,
+                 int64_t n, bool amax_ready, cudaStream_t st);
+
+}  // namespace fmha

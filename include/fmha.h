@@ -1,0 +1,143 @@
+/*
+ * fmha.h - C ABI of the GB300 (sm_103a) fused attention library, libfmha.so.
+ *
+ * Computes O = softmax(scale * Q K^T) V over BF16 Q/K/V, with an online (running max / sum)
+ * softmax and O rescale across key/value tiles, a split-KV decode path with a combine step,
+ * and optional NVFP4 quantisation of O.  Sources:
+ *   - "NVFP4-1.1_RAW_CUDA_CPP_APPROACH.md" (nvfp4-megamoe-kernel), kernel plan items 1-7:
+ *     TMA loads of Q/K/V, tcgen05 MMA with a Tensor Memory accumulator, in-kernel softmax with
+ *     O rescale, multi-KV-tile support, FP4 quantisation for NVFP4;
+ *   - "CURRENT_ISSUE.md" @4b129c1, QK verify kernel: tensors laid out (B, H, S, D) contiguous;
+ *   - "CURRENT_ISSUE.md" @57d67e6, "The 4x Bug": the raw S = Q K^T check (fmha_qk_gemm).
+ *
+ * Conventions shared by every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the library never allocates
+ *     or frees device memory, never synchronises (except fmha_check_status) and launches only
+ *     on `stream`.  Inputs are read-only; outputs must not alias inputs.
+ *   - Layouts are contiguous, row-major: Q/O [B][Hq][Sq][D], K/V [B][Hkv][Skv][D], LSE [B][Hq][Sq].
+ *   - Grouped-query attention: query head hq reads key/value head hq / (Hq / Hkv).
+ *   - LSE is the natural logarithm of sum_j exp(scale * q.k_j) (scale included), FP32.
+ *   - A key set of size 0 (seqlens_k[b] == 0) gives O = 0 and LSE = -inf.
+ *   - Pointers must be 16-byte aligned.  D must be 64, 128 or 512 (16 is also accepted by
+ *     fmha_qk_gemm).
+ *   - Return value: FMHA_OK or an fmha_status code; nothing aborts or throws.  A failed call
+ *     leaves a message for fmha_error_string(code) / fmha_last_error() of the calling thread.
+ *   - Asynchronous device-side failures (a bounded wait inside a kernel that timed out) are
+ *     reported by fmha_check_status().
+ */
+#ifndef FMHA_H_
+#define FMHA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t without pulling in the CUDA headers; NULL = the legacy default stream. */
+typedef struct CUstream_st* fmha_stream_t;
+
+typedef enum {
+    FMHA_OK = 0,
+    FMHA_ERR_INVALID = 1,     /* bad argument: NULL pointer, Hq % Hkv != 0, unsupported D, misalignment */
+    FMHA_ERR_UNSUPPORTED = 2, /* valid request that this library does not implement */
+    FMHA_ERR_WORKSPACE = 3,   /* workspace missing or smaller than fmha_workspace_size() */
+    FMHA_ERR_CUDA = 4,        /* a CUDA runtime/driver call or kernel launch failed */
+    FMHA_ERR_TIMEOUT = 5      /* a kernel's bounded wait expired (see fmha_check_status) */
+} fmha_status;
+
+typedef enum {
+    FMHA_OUT_BF16 = 0,  /* out: BF16 [B,Hq,Sq,D] */
+    FMHA_OUT_F32 = 1,   /* out: FP32 [B,Hq,Sq,D] */
+    FMHA_OUT_NVFP4 = 2  /* out: packed E2M1 codes [B,Hq,Sq,D/2] (element 2i in bits 3:0),
+                           plus out_scales / out_tensor_scale below */
+} fmha_out_kind;
+
+typedef struct {
+    int out_kind;             /* fmha_out_kind; default FMHA_OUT_BF16 */
+    const int32_t* seqlens_k; /* device int32[B], 0 <= seqlens_k[b] <= Skv: keys at or beyond
+                                 seqlens_k[b] are never read (ragged batches); NULL = all Skv */
+    int num_splits;           /* 0 = automatic split-KV; 1 = no split (each (b, kv-head) handled
+                                 by one CTA, no workspace needed for BF16/F32 output) */
+    void* workspace;          /* device scratch of at least fmha_workspace_size() bytes (256-B
+                                 aligned); contents on entry do not matter */
+    size_t workspace_bytes;
+    uint8_t* out_scales;      /* NVFP4: E4M3 block scales [B,Hq,Sq,D/16] */
+    float* out_tensor_scale;  /* NVFP4: device float[1], the per-tensor scale s_g */
+    float* out_f32;           /* optional, NVFP4 only: the FP32 O that was quantised */
+} fmha_opts;
+
+/*
+ * Attention forward with default options (BF16 output, dense keys, no workspace).
+ *   q: BF16 [B,Hq,Sq,D]; k, v: BF16 [B,Hkv,Skv,D]; out: BF16 [B,Hq,Sq,D];
+ *   lse: FP32 [B,Hq,Sq] or NULL; scale: multiplies Q K^T before the softmax.
+ * Same as fmha_fwd_ex(..., opts = NULL).
+ */
+int fmha_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq, int Hkv,
+             int Sq, int Skv, int D, float scale, fmha_stream_t stream);
+
+/*
+ * Attention forward with options (output kind, ragged key lengths, split-KV, NVFP4).
+ * opts == NULL means all defaults.  Split-KV and NVFP4 output need opts->workspace.
+ */
+int fmha_fwd_ex(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq, int Hkv,
+                int Sq, int Skv, int D, float scale, fmha_stream_t stream, const fmha_opts* opts);
+
+/* Bytes of workspace fmha_fwd_ex needs for this problem and these options (0 if none). */
+size_t fmha_workspace_size(int B, int Hq, int Hkv, int Sq, int Skv, int D, const fmha_opts* opts);
+
+/*
+ * NVFP4 quantisation of an FP32 tensor x[n], n % 16 == 0 (the NVFP4 step of the pages' kernel
+ * plan, "FP4 quantization for NVFP4-1.1"):
+ *   s_g = fp32(amax / (6 * 448)); per block of 16: sc = E4M3(amax_block / (6 s_g)) (round to
+ *   nearest even, saturating at 448); code_i = E2M1(x_i / (sc * s_g)) (nearest even, saturating
+ *   at 6, sign copied).  amax == 0 gives all-zero codes and scales.
+ *   q: uint8[n/2] codes, element 2i in bits 3:0 and 2i+1 in bits 7:4.
+ *   scales: nvfp4_scales_bytes(n) bytes: E4M3 scales [n/16], then at byte offset
+ *   align16(n/16) the FP32 s_g, then 12 bytes the call uses as scratch.
+ */
+int nvfp4_quantize(const float* x, uint8_t* q, uint8_t* scales, int64_t n, fmha_stream_t stream);
+
+/* Size in bytes of the `scales` buffer nvfp4_quantize needs for n values. */
+size_t nvfp4_scales_bytes(int64_t n);
+
+/*
+ * Test hook: raw S = Q K^T in FP32, no scale ("CURRENT_ISSUE.md" @57d67e6, "The 4x Bug":
+ * the single tcgen05 MMA product checked against a scalar dot product).
+ *   q: BF16 [Sq,D], k: BF16 [Skv,D], s: FP32 [Sq,Skv]; D in {16, 64, 128, 512}.
+ */
+int fmha_qk_gemm(const void* q, const void* k, float* s, int Sq, int Skv, int D, fmha_stream_t stream);
+
+/*
+ * Test hook: layout self-checks of the building blocks.  Each writes its results to `out`
+ * (device, `out_bytes` bytes, see the test-suite for the layouts) from inputs in `in`:
+ *   which = 1: Tensor Memory round trip (tcgen05.st then tcgen05.ld, 32x32b shape);
+ *   which = 2: O^T = V^T P^T with V^T an MN-major shared-memory operand (decode PV form);
+ *   which = 3: O = P V with P in Tensor Memory and V MN-major in shared memory (TS form).
+ */
+int fmha_selftest(int which, const void* in, void* out, size_t out_bytes, int param, fmha_stream_t stream);
+
+/*
+ * Waits for `stream`, then returns FMHA_ERR_TIMEOUT if any kernel of this library timed out
+ * in a bounded wait since the last call (and clears that state), FMHA_ERR_CUDA if the stream
+ * reports an error, else FMHA_OK.
+ */
+int fmha_check_status(fmha_stream_t stream);
+
+/* Bounded-wait limit in SM clock cycles for later launches (0 = default, about 2 s). */
+void fmha_set_wait_limit(long long cycles);
+
+/* Static text for a status code. */
+const char* fmha_error_string(int code);
+
+/* Message of the last failing call on this thread ("" if none). */
+const char* fmha_last_error(void);
+
+/* Number of SMs of the current device as the library sees it (0 on failure). */
+int fmha_num_sms(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FMHA_H_ */
