@@ -81,6 +81,8 @@ def load(path: str | None = None):
             "fmha_error_string": ([I], ctypes.c_char_p),
             "fmha_last_error": ([], ctypes.c_char_p),
             "fmha_num_sms": ([], I),
+            "fmha_launch_count": ([], ctypes.c_longlong),
+            "fmha_time_next_call": ([V, V], None),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name, None)
@@ -195,3 +197,12 @@ def fmha_set_wait_limit(cycles: int):
 
 def fmha_num_sms() -> int:
     return int(load().fmha_num_sms())
+
+
+def fmha_launch_count() -> int:
+    return int(load().fmha_launch_count())
+
+
+def fmha_time_next_call(start_event, stop_event):
+    """torch.cuda.Event pair (enable_timing=True, already recorded once so the handle exists)."""
+    load().fmha_time_next_call(ctypes.c_void_p(start_event.cuda_event), ctypes.c_void_p(stop_event.cuda_event))

@@ -70,6 +70,24 @@ int num_sms()
     return n;
 }
 
+// ---- launch accounting / timing hook --------------------------------------------------------------
+static std::atomic<long long> g_launches{0};
+static thread_local cudaEvent_t g_ev_begin = nullptr;
+static thread_local cudaEvent_t g_ev_end = nullptr;
+
+void count_launch(int n) { g_launches.fetch_add(n); }
+
+void timing_mark_begin(cudaStream_t st)
+{
+    if (g_ev_begin) cudaEventRecord(g_ev_begin, st);
+}
+
+void timing_mark_end(cudaStream_t st)
+{
+    if (g_ev_end) cudaEventRecord(g_ev_end, st);
+    g_ev_begin = g_ev_end = nullptr;
+}
+
 // ---- TMA tensor maps -------------------------------------------------------------------------------
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 {
@@ -143,6 +161,14 @@ void fmha_set_wait_limit(long long cycles) { g_wait_limit.store(cycles > 0 ? cyc
 
 int fmha_num_sms(void) { return num_sms(); }
 
+long long fmha_launch_count(void) { return g_launches.load(); }
+
+void fmha_time_next_call(void* start_event, void* stop_event)
+{
+    g_ev_begin = static_cast<cudaEvent_t>(start_event);
+    g_ev_end = static_cast<cudaEvent_t>(stop_event);
+}
+
 int fmha_check_status(fmha_stream_t stream)
 {
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -178,6 +204,148 @@ int fmha_selftest(int which, const void* in, void* out, size_t out_bytes, int pa
     if (!aligned16(in) || !aligned16(out)) return set_error(FMHA_ERR_INVALID, "fmha_selftest: misaligned");
     if (!device_status_ptr()) return set_error(FMHA_ERR_CUDA, "no CUDA device");
     return launch_selftest(which, in, out, out_bytes, param, reinterpret_cast<cudaStream_t>(stream));
+}
+
+// ---- attention ---------------------------------------------------------------------------------------
+static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+static bool use_decode_path(int Hq, int Hkv, int Sq) { return static_cast<long long>(Hq / Hkv) * Sq <= 16; }
+
+// Workspace: [path scratch][NVFP4 amax word].  The path scratch of the decode path holds the
+// tile prefix, the split partials and (NVFP4 without out_f32) the FP32 staging of O.
+static size_t workspace_bytes(const AttnArgs& a, int num_splits)
+{
+    size_t w = use_decode_path(a.Hq, a.Hkv, a.Sq) ? decode_workspace_bytes(a, num_splits) : prefill_workspace_bytes(a);
+    w = align256(w);
+    if (a.out_kind == FMHA_OUT_NVFP4) w += 256;
+    return w;
+}
+
+static int validate(const void* q, const void* k, const void* v, const void* out, int B, int Hq, int Hkv, int Sq,
+                    int Skv, int D, const fmha_opts* o)
+{
+    if (!q || !k || !v || !out) return set_error(FMHA_ERR_INVALID, "NULL q/k/v/out");
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Sq < 0 || Skv <= 0)
+        return set_error(FMHA_ERR_INVALID, "need B >= 0, Hq > 0, Hkv > 0, Sq >= 0, Skv >= 1");
+    if (Hq % Hkv != 0) return set_error(FMHA_ERR_INVALID, "Hq must be a multiple of Hkv");
+    if (D != 64 && D != 128 && D != 512) return set_error(FMHA_ERR_INVALID, "D must be 64, 128 or 512");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+        return set_error(FMHA_ERR_INVALID, "q/k/v/out must be 16-byte aligned");
+    if (static_cast<long long>(B) * Hkv * Skv >= (1LL << 31) || static_cast<long long>(B) * Hq * Sq >= (1LL << 31))
+        return set_error(FMHA_ERR_UNSUPPORTED, "more than 2^31 rows");
+    if (o) {
+        if (o->out_kind < FMHA_OUT_BF16 || o->out_kind > FMHA_OUT_NVFP4) return set_error(FMHA_ERR_INVALID, "bad out_kind");
+        if (o->num_splits < 0) return set_error(FMHA_ERR_INVALID, "num_splits must be >= 0");
+        if (o->out_kind == FMHA_OUT_NVFP4) {
+            if (!o->out_scales || !o->out_tensor_scale)
+                return set_error(FMHA_ERR_INVALID, "NVFP4 output needs out_scales and out_tensor_scale");
+            if ((o->out_f32 && !aligned16(o->out_f32)))
+                return set_error(FMHA_ERR_INVALID, "out_f32 must be 16-byte aligned");
+        }
+        if (o->seqlens_k && (reinterpret_cast<uintptr_t>(o->seqlens_k) & 3))
+            return set_error(FMHA_ERR_INVALID, "seqlens_k must be 4-byte aligned");
+        if (o->workspace && (reinterpret_cast<uintptr_t>(o->workspace) & 255))
+            return set_error(FMHA_ERR_INVALID, "workspace must be 256-byte aligned");
+    }
+    return FMHA_OK;
+}
+
+static AttnArgs make_args(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq, int Hkv,
+                          int Sq, int Skv, int D, float scale, const fmha_opts* o)
+{
+    AttnArgs a{};
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.out = out;
+    a.lse = lse;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.Sq = Sq;
+    a.Skv = Skv;
+    a.D = D;
+    a.scale = scale;
+    a.seqlens = o ? o->seqlens_k : nullptr;
+    a.out_kind = o ? o->out_kind : FMHA_OUT_BF16;
+    a.out_f32 = (o && o->out_kind == FMHA_OUT_NVFP4) ? o->out_f32 : nullptr;
+    return a;
+}
+
+size_t fmha_workspace_size(int B, int Hq, int Hkv, int Sq, int Skv, int D, const fmha_opts* opts)
+{
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Sq < 0 || Skv <= 0 || Hq % Hkv) return 0;
+    AttnArgs a = make_args(nullptr, nullptr, nullptr, nullptr, nullptr, B, Hq, Hkv, Sq, Skv, D, 1.f, opts);
+    return workspace_bytes(a, opts ? opts->num_splits : 1);
+}
+
+int fmha_fwd_ex(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq, int Hkv, int Sq,
+                int Skv, int D, float scale, fmha_stream_t stream, const fmha_opts* opts)
+{
+    int rc = validate(q, k, v, out, B, Hq, Hkv, Sq, Skv, D, opts);
+    if (rc) return rc;
+    if (lse && (reinterpret_cast<uintptr_t>(lse) & 3)) return set_error(FMHA_ERR_INVALID, "lse must be 4-byte aligned");
+    if (!device_status_ptr()) return set_error(FMHA_ERR_CUDA, "no CUDA device");
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    AttnArgs a = make_args(q, k, v, out, lse, B, Hq, Hkv, Sq, Skv, D, scale, opts);
+    void* ws = opts ? opts->workspace : nullptr;
+    // automatic split-KV when the caller supplied a workspace, whole units otherwise
+    const int num_splits = (opts && (opts->num_splits != 0 || ws)) ? opts->num_splits : 1;
+    const size_t ws_bytes = opts ? opts->workspace_bytes : 0;
+    const size_t need = workspace_bytes(a, num_splits);
+    if (need > 0 && (!ws || ws_bytes < need))
+        return set_error(FMHA_ERR_WORKSPACE, "workspace missing or smaller than fmha_workspace_size()");
+    if (static_cast<long long>(B) * Hq * Sq == 0) return FMHA_OK;
+    const bool nvfp4 = a.out_kind == FMHA_OUT_NVFP4;
+    const size_t path_bytes = nvfp4 ? need - 256 : need;
+    unsigned* amax = nvfp4 ? reinterpret_cast<unsigned*>(static_cast<uint8_t*>(ws) + path_bytes) : nullptr;
+    if (nvfp4) {
+        a.amax_slot = reinterpret_cast<float*>(amax);
+        FMHA_CHECK_CUDA(cudaMemsetAsync(amax, 0, sizeof(unsigned), st));
+    }
+    if (use_decode_path(Hq, Hkv, Sq))
+        rc = launch_decode(a, num_splits, ws, path_bytes, st);
+    else
+        rc = launch_prefill(a, ws, path_bytes, st);
+    if (rc) return rc;
+    if (nvfp4) {
+        // the FP32 O the quantiser reads: caller's out_f32, else the staging area of the workspace
+        const float* src = a.out_f32;
+        if (!src) {
+            const size_t n = static_cast<size_t>(B) * Hq * Sq * D;
+            src = reinterpret_cast<const float*>(static_cast<uint8_t*>(ws) + path_bytes - align256(n * 4));
+        }
+        rc = launch_nvfp4(src, static_cast<uint8_t*>(out), opts->out_scales, opts->out_tensor_scale, amax,
+                          static_cast<int64_t>(B) * Hq * Sq * D, true, st);
+    }
+    return rc;
+}
+
+int fmha_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq, int Hkv, int Sq, int Skv,
+             int D, float scale, fmha_stream_t stream)
+{
+    return fmha_fwd_ex(q, k, v, out, lse, B, Hq, Hkv, Sq, Skv, D, scale, stream, nullptr);
+}
+
+// ---- standalone NVFP4 ------------------------------------------------------------------------------------
+static size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
+
+size_t nvfp4_scales_bytes(int64_t n)
+{
+    if (n < 0) return 0;
+    return align16(static_cast<size_t>(n / 16)) + 16;
+}
+
+int nvfp4_quantize(const float* x, uint8_t* q, uint8_t* scales, int64_t n, fmha_stream_t stream)
+{
+    if (!x || !q || !scales) return set_error(FMHA_ERR_INVALID, "nvfp4_quantize: NULL pointer");
+    if (n < 0 || n % 16 != 0) return set_error(FMHA_ERR_INVALID, "nvfp4_quantize: n must be a non-negative multiple of 16");
+    if (!aligned16(x) || (reinterpret_cast<uintptr_t>(q) & 7) || (reinterpret_cast<uintptr_t>(scales) & 15))
+        return set_error(FMHA_ERR_INVALID, "nvfp4_quantize: x and scales 16-byte, q 8-byte aligned");
+    if (!device_status_ptr()) return set_error(FMHA_ERR_CUDA, "no CUDA device");
+    uint8_t* tail = scales + align16(static_cast<size_t>(n / 16));
+    return launch_nvfp4(x, q, scales, reinterpret_cast<float*>(tail), reinterpret_cast<unsigned*>(tail + 4), n, false,
+                        reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

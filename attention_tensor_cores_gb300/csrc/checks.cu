@@ -302,6 +302,7 @@ int launch_qk_gemm(const void* q, const void* k, float* s, int Sq, int Skv, int 
     dim3 grid((Skv + 127) / 128, (Sq + 127) / 128);
     qk_gemm_kernel<<<grid, kQkThreads, smem, st>>>(qmap, kmap, s, Sq, Skv, D, device_status_ptr(), wait_limit());
     FMHA_CHECK_LAUNCH("qk_gemm_kernel");
+    count_launch();
     return FMHA_OK;
 }
 

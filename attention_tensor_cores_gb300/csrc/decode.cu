@@ -1,0 +1,733 @@
+// Decode attention (few query rows per key/value head): split-KV over a persistent grid, plus
+// the combine of the partial results.
+//
+// Follows the kernel plan of "NVFP4-1.1_RAW_CUDA_CPP_APPROACH.md" (nvfp4-megamoe-kernel): TMA
+// loads of Q/K/V, the QK product on tcgen05 with the accumulator in Tensor Memory, softmax warps
+// reading S back with tcgen05.ld, the running max / sum with O rescale over several KV tiles
+// ("in-kernel softmax with O rescale", "multi-KV-tile support"), then the PV product.  The
+// GB300 design around it is this file's own:
+//
+//  * Swap-AB.  With G <= 16 query rows per key/value head (G = (Hq/Hkv) * Sq), the products are
+//    taken transposed so that the 128 keys of a tile fill the MMA's M dimension:
+//      S^T[kv][q] = K[kv][:] . Q[q][:]      (A = K tile, K-major; B = Q rows, K-major; N = 16)
+//      O^T[d][q]  = V^T[d][kv] . P^T[kv][q]  (A = V tile read MN-major; B = P, K-major; N = 16)
+//    Thread t of the softmax warpgroup owns TMEM lane t: key t of the tile for S, feature d = t
+//    for O.  Reductions over keys are warp shuffles plus a 4-warp shared-memory step.
+//  * The per-tile PV product goes to a fresh TMEM buffer (no accumulate) and the softmax threads
+//    fold it into register accumulators with the rescale factor: acc = alpha * acc + O_tile.
+//    O is never read-modify-written in TMEM, so there is no ordering hazard between the rescale
+//    and the next MMA.
+//  * Work split ("stream-K" over keys): the key tiles of all units (b, kv-head) are laid end to
+//    end and CTA c of P takes tiles [c*T/P, (c+1)*T/P).  Each maximal run inside one unit is a
+//    work item; an item that covers a whole unit writes the final O and LSE, otherwise it writes
+//    a normalised partial (O_i, lse_i) to slot u + c of the workspace and the combine kernel
+//    merges them: lse = log sum_i exp(lse_i), O = sum_i exp(lse_i - lse) O_i.  Ragged batches
+//    balance by construction.  With num_splits == 1 each CTA takes whole units instead.
+//  * Roles: warps 0-3 softmax/epilogue, warp 4 TMA producer, warp 5 MMA issuer.  Every wait is
+//    bounded; a timeout flips the CTA into a drain mode (no new TMA/MMA, loops run out) and sets
+//    the device status word.
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace fmha {
+namespace {
+
+constexpr int kTileKV = 128;    // keys per tile = MMA M
+constexpr int kN = 16;          // query rows per unit, padded (MMA N)
+constexpr int kThreads = 192;   // 4 softmax warps + producer + MMA
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+template <int D>
+struct DecodeCfg {
+    static constexpr int kAtoms = D / 64;                  // 64-column swizzle atoms per row
+    static constexpr int kStages = (D == 64) ? 4 : 3;      // K and V ring depth
+    static constexpr int kQBytes = kAtoms * kN * 128;      // one Q buffer
+    static constexpr int kKVBytes = kAtoms * kTileKV * 128;
+    static constexpr int kPBytes = 2 * kN * 128;           // P^T: 16 rows x 128 keys
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffK = kOffQ + 2 * kQBytes;
+    static constexpr int kOffV = kOffK + kStages * kKVBytes;
+    static constexpr int kOffP = kOffV + kStages * kKVBytes;
+    static constexpr int kSmemBytes = kOffP + 2 * kPBytes + 1024;   // + alignment slack
+    static constexpr uint32_t kTmemCols = 64;              // S[2] x 16, O[2] x 16
+};
+
+struct DecodeParams {
+    int U;              // units = B * Hkv
+    int Hkv;
+    int G;              // real query rows per unit
+    int Skv;
+    int D;
+    float c;            // scale * log2(e)
+    const int32_t* seqlens;
+    const int32_t* prefix;   // [U+1] tile prefix (ragged split mode), else NULL
+    int tiles_uniform;       // tiles per unit when prefix == NULL
+    int split;               // 1 = stream-K partition, 0 = whole units per CTA
+    // outputs
+    void* out;               // BF16 or F32 [U*G][D] (NULL when writing FP32 staging only)
+    int out_f32;             // 1: `out` is FP32
+    float* lse;              // [U*G] or NULL
+    float* o_stage;          // FP32 [U*G][D] copy for NVFP4, else NULL
+    unsigned* amax_bits;     // NVFP4: running max |O| (FP32 bits), else NULL
+    float* part_o;           // [slots][16][D]
+    float* part_lse;         // [slots][16]
+    int* status;
+    long long limit;
+};
+
+// ---- work items ----------------------------------------------------------------------------------
+struct Item {
+    int u, t0, t1;   // unit and its tile range [t0, t1)
+    int n;           // valid keys of the unit
+    bool whole;      // covers every tile of the unit
+    int slot;        // partial slot (u + cta)
+};
+
+struct Sched {
+    const DecodeParams* p;
+    long long g, g1;    // split mode: current / end global tile
+    int u;              // whole-unit mode: next unit
+    int cta, nctas;
+
+    __device__ int unit_tiles(int u) const
+    {
+        if (p->prefix) return p->prefix[u + 1] - p->prefix[u];
+        if (p->seqlens) return (p->seqlens[u / p->Hkv] + kTileKV - 1) / kTileKV;
+        return p->tiles_uniform;
+    }
+    __device__ long long unit_start(int u) const
+    {
+        return p->prefix ? static_cast<long long>(p->prefix[u]) : static_cast<long long>(u) * p->tiles_uniform;
+    }
+    __device__ int unit_keys(int u) const { return p->seqlens ? p->seqlens[u / p->Hkv] : p->Skv; }
+
+    __device__ void init(const DecodeParams* pp, int c, int n)
+    {
+        p = pp;
+        cta = c;
+        nctas = n;
+        if (p->split) {
+            const long long T = p->prefix ? p->prefix[p->U] : static_cast<long long>(p->U) * p->tiles_uniform;
+            g = (static_cast<long long>(c) * T) / n;
+            g1 = (static_cast<long long>(c + 1) * T) / n;
+        } else {
+            u = c;
+        }
+    }
+
+    __device__ bool next(Item& it)
+    {
+        if (p->split) {
+            if (g >= g1) return false;
+            int uu;
+            if (p->prefix) {   // last unit whose start <= g (prefix is non-decreasing)
+                int lo = 0, hi = p->U - 1;
+                while (lo < hi) {
+                    const int mid = (lo + hi + 1) >> 1;
+                    if (p->prefix[mid] <= g) lo = mid; else hi = mid - 1;
+                }
+                uu = lo;
+                while (uu + 1 < p->U && p->prefix[uu + 1] <= g) ++uu;   // skip empty units
+            } else {
+                uu = static_cast<int>(g / p->tiles_uniform);
+            }
+            const long long s = unit_start(uu);
+            const int nt = unit_tiles(uu);
+            it.u = uu;
+            it.t0 = static_cast<int>(g - s);
+            it.t1 = static_cast<int>(min(static_cast<long long>(nt), g1 - s));
+            it.n = unit_keys(uu);
+            it.whole = (it.t0 == 0 && it.t1 == nt);
+            it.slot = uu + cta;
+            g = s + it.t1;
+            return true;
+        }
+        if (u >= p->U) return false;
+        it.u = u;
+        it.t0 = 0;
+        it.t1 = unit_tiles(u);
+        it.n = unit_keys(u);
+        it.whole = true;
+        it.slot = 0;
+        u += nctas;
+        return true;
+    }
+};
+
+// Byte offset of element (row r, column k) of a K-major operand made of 128-byte-swizzled
+// atoms of 64 columns, `atom_bytes` apart.
+__device__ __forceinline__ uint32_t sw128_offset(int r, int k, uint32_t atom_bytes)
+{
+    const int a = k >> 6, kk = k & 63;
+    return a * atom_bytes + r * 128 + ((((kk >> 3) ^ (r & 7)) & 7) << 4) + ((kk & 7) << 1);
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int n)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// Bounded wait that ignores the abort flag: used at teardown so nothing is still in flight.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, long long limit)
+{
+    const uint32_t a = smem_u32(bar);
+    const long long t0 = clock64();
+    while (!mbar_try_wait(a, parity)) {
+        if (clock64() - t0 > limit) return;
+    }
+}
+
+struct Ring {
+    uint32_t idx = 0, phase = 0;
+    int n;
+    __device__ explicit Ring(int stages) : n(stages) {}
+    __device__ void advance()
+    {
+        if (++idx == static_cast<uint32_t>(n)) {
+            idx = 0;
+            phase ^= 1;
+        }
+    }
+};
+
+__device__ __forceinline__ float warp_max(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+                  const __grid_constant__ CUtensorMap vmap, const __grid_constant__ DecodeParams p)
+{
+    using C = DecodeCfg<D>;
+    constexpr int S = C::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+    __shared__ uint64_t q_full[2], q_empty[2], k_full[S], k_empty[S], v_full[S], v_empty[S];
+    __shared__ uint64_t s_full[2], s_empty[2], p_full[2], p_empty[2], o_full[2], o_empty[2], mma_done;
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_flag;
+    __shared__ float red_max[2][4][kN];
+    __shared__ float red_sum[4][kN];
+
+    const int warp = threadIdx.x / 32;
+    const WaitCtl wc{&abort_flag, p.status, p.limit};
+
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&q_full[i], 1);
+            mbar_init(&q_empty[i], 1);
+            mbar_init(&s_full[i], 1);
+            mbar_init(&s_empty[i], 128);
+            mbar_init(&p_full[i], 128);
+            mbar_init(&p_empty[i], 1);
+            mbar_init(&o_full[i], 1);
+            mbar_init(&o_empty[i], 128);
+        }
+        for (int i = 0; i < S; ++i) {
+            mbar_init(&k_full[i], 1);
+            mbar_init(&k_empty[i], 1);
+            mbar_init(&v_full[i], 1);
+            mbar_init(&v_empty[i], 1);
+        }
+        mbar_init(&mma_done, 1);
+        fence_barrier_init();
+    }
+    if (warp == 5) {
+        tmem_alloc(&tmem_slot, C::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;   // S buffers at columns 0/16, O buffers at 32/48
+
+    Sched sched;
+    sched.init(&p, blockIdx.x, gridDim.x);
+    Item it;
+
+    if (warp == 4) {
+        // ------------------------------------------------ TMA producer
+        if (lane_id() == 0) {
+            tma_prefetch_desc(&qmap);
+            tma_prefetch_desc(&kmap);
+            tma_prefetch_desc(&vmap);
+            const uint64_t pol = policy_evict_first();
+            Ring qr(2), kr(S), vr(S);
+            uint32_t kcnt[S], vcnt[S], qcnt[2] = {0, 0};
+            for (int i = 0; i < S; ++i) kcnt[i] = vcnt[i] = 0;
+            while (sched.next(it)) {
+                if (it.t1 <= it.t0) continue;
+                mbar_wait(&q_empty[qr.idx], qr.phase ^ 1, wc);
+                if (!aborted(wc)) {
+                    uint8_t* dst = smem + C::kOffQ + qr.idx * C::kQBytes;
+                    mbar_arrive_expect_tx(&q_full[qr.idx], C::kQBytes);
+                    for (int a = 0; a < C::kAtoms; ++a)
+                        tma_load_3d(dst + a * (kN * 128), &qmap, &q_full[qr.idx], a * 64, 0, it.u);
+                    ++qcnt[qr.idx];
+                }
+                qr.advance();
+                for (int t = it.t0; t < it.t1; ++t) {
+                    mbar_wait(&k_empty[kr.idx], kr.phase ^ 1, wc);
+                    if (!aborted(wc)) {
+                        uint8_t* dst = smem + C::kOffK + kr.idx * C::kKVBytes;
+                        mbar_arrive_expect_tx(&k_full[kr.idx], C::kKVBytes);
+                        for (int a = 0; a < C::kAtoms; ++a)
+                            tma_load_3d_hint(dst + a * (kTileKV * 128), &kmap, &k_full[kr.idx], a * 64, t * kTileKV,
+                                             it.u, pol);
+                        ++kcnt[kr.idx];
+                    }
+                    kr.advance();
+                    mbar_wait(&v_empty[vr.idx], vr.phase ^ 1, wc);
+                    if (!aborted(wc)) {
+                        uint8_t* dst = smem + C::kOffV + vr.idx * C::kKVBytes;
+                        mbar_arrive_expect_tx(&v_full[vr.idx], C::kKVBytes);
+                        for (int a = 0; a < C::kAtoms; ++a)
+                            tma_load_3d_hint(dst + a * (kTileKV * 128), &vmap, &v_full[vr.idx], a * 64, t * kTileKV,
+                                             it.u, pol);
+                        ++vcnt[vr.idx];
+                    }
+                    vr.advance();
+                }
+            }
+            // nothing may still be landing in shared memory when the CTA exits
+            for (int i = 0; i < S; ++i) {
+                if (kcnt[i]) drain_wait(&k_full[i], (kcnt[i] - 1) & 1, p.limit);
+                if (vcnt[i]) drain_wait(&v_full[i], (vcnt[i] - 1) & 1, p.limit);
+            }
+            for (int i = 0; i < 2; ++i)
+                if (qcnt[i]) drain_wait(&q_full[i], (qcnt[i] - 1) & 1, p.limit);
+        }
+    } else if (warp == 5) {
+        // ------------------------------------------------ MMA issuer
+        if (lane_id() == 0) {
+            constexpr uint32_t idesc_qk = idesc_bf16_f32(128, kN, false, false);
+            constexpr uint32_t idesc_pv = idesc_bf16_f32(128, kN, true, false);
+            constexpr uint32_t lbo_v = (D >= 128) ? 16384u : 0u;   // D = 64: M rows 64..127 repeat 0..63
+            Ring qr(2), kr(S), vr(S), sr(2), pr(2), orr(2);
+            auto pv = [&]() {
+                mbar_wait(&p_full[pr.idx], pr.phase, wc);
+                mbar_wait(&v_full[vr.idx], vr.phase, wc);
+                mbar_wait(&o_empty[orr.idx], orr.phase ^ 1, wc);
+                tc_fence_after();
+                if (!aborted(wc)) {
+                    const uint32_t sV = smem_u32(smem + C::kOffV + vr.idx * C::kKVBytes);
+                    const uint32_t sP = smem_u32(smem + C::kOffP + pr.idx * C::kPBytes);
+                    const uint32_t dO = tmem + 32 + orr.idx * 16;
+#pragma unroll
+                    for (int ks = 0; ks < kTileKV / 16; ++ks) {
+                        const uint64_t da = sdesc_sw128(sV + ks * 2048, lbo_v, 1024);
+                        const uint64_t db = sdesc_sw128(sP + (ks >> 2) * (kN * 128) + (ks & 3) * 32, 16, 1024);
+                        mma_ss(dO, da, db, idesc_pv, ks > 0 ? 1u : 0u);
+                    }
+                    mma_commit(&o_full[orr.idx]);
+                    mma_commit(&v_empty[vr.idx]);
+                    mma_commit(&p_empty[pr.idx]);
+                }
+                pr.advance();
+                vr.advance();
+                orr.advance();
+            };
+            while (sched.next(it)) {
+                if (it.t1 <= it.t0) continue;
+                mbar_wait(&q_full[qr.idx], qr.phase, wc);
+                const uint32_t sQ = smem_u32(smem + C::kOffQ + qr.idx * C::kQBytes);
+                for (int t = it.t0; t < it.t1; ++t) {
+                    mbar_wait(&k_full[kr.idx], kr.phase, wc);
+                    mbar_wait(&s_empty[sr.idx], sr.phase ^ 1, wc);
+                    tc_fence_after();
+                    if (!aborted(wc)) {
+                        const uint32_t sK = smem_u32(smem + C::kOffK + kr.idx * C::kKVBytes);
+                        const uint32_t dS = tmem + sr.idx * 16;
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint64_t da = sdesc_sw128(sK + (kk >> 2) * (kTileKV * 128) + (kk & 3) * 32, 16, 1024);
+                            const uint64_t db = sdesc_sw128(sQ + (kk >> 2) * (kN * 128) + (kk & 3) * 32, 16, 1024);
+                            mma_ss(dS, da, db, idesc_qk, kk > 0 ? 1u : 0u);
+                        }
+                        mma_commit(&s_full[sr.idx]);
+                        mma_commit(&k_empty[kr.idx]);
+                    }
+                    kr.advance();
+                    sr.advance();
+                    if (t > it.t0) pv();   // PV of the previous tile overlaps this tile's softmax
+                }
+                pv();
+                if (!aborted(wc)) mma_commit(&q_empty[qr.idx]);
+                qr.advance();
+            }
+            mma_commit(&mma_done);
+            drain_wait(&mma_done, 0, p.limit);
+        }
+    } else {
+        // ------------------------------------------------ softmax / correction / epilogue (128 threads)
+        const int tid = threadIdx.x;
+        const int lane = static_cast<int>(lane_id());
+        const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+        const int G = p.G;
+        Ring sr(2), pr(2), orr(2), vr(S);
+        uint32_t tile_ctr = 0;
+        while (sched.next(it)) {
+            float m[kN], l[kN], acc[kN], alpha_prev[kN];
+#pragma unroll
+            for (int q = 0; q < kN; ++q) {
+                m[q] = -INFINITY;
+                l[q] = 0.f;
+                acc[q] = 0.f;
+                alpha_prev[q] = 0.f;
+            }
+            auto consume = [&](const float (&al)[kN]) {
+                mbar_wait(&o_full[orr.idx], orr.phase, wc);
+                tc_fence_after();
+                uint32_t ov[16];
+                tmem_ld16(tmem + lane_base + 32 + orr.idx * 16, ov);
+                tmem_ld_wait();
+                tc_fence_before();
+                mbar_arrive(&o_empty[orr.idx]);
+                orr.advance();
+#pragma unroll
+                for (int q = 0; q < kN; ++q) acc[q] = fmaf(acc[q], al[q], __uint_as_float(ov[q]));
+            };
+            for (int t = it.t0; t < it.t1; ++t) {
+                mbar_wait(&s_full[sr.idx], sr.phase, wc);
+                tc_fence_after();
+                uint32_t sv[16];
+                tmem_ld16(tmem + lane_base + sr.idx * 16, sv);
+                tmem_ld_wait();
+                tc_fence_before();
+                mbar_arrive(&s_empty[sr.idx]);
+                sr.advance();
+
+                const bool valid = t * kTileKV + tid < it.n;
+                float x[kN];
+#pragma unroll
+                for (int q = 0; q < kN; ++q) x[q] = valid ? __uint_as_float(sv[q]) * p.c : -INFINITY;
+                float(*rb)[kN] = red_max[tile_ctr & 1];
+#pragma unroll
+                for (int q = 0; q < kN; ++q)
+                    if (q < G) {
+                        const float mx = warp_max(x[q]);
+                        if (lane == 0) rb[warp][q] = mx;
+                    }
+                named_bar_sync(1, 128);
+                ++tile_ctr;
+                float alpha[kN], pv[kN];
+#pragma unroll
+                for (int q = 0; q < kN; ++q) {
+                    if (q < G) {
+                        const float mt = fmaxf(fmaxf(rb[0][q], rb[1][q]), fmaxf(rb[2][q], rb[3][q]));
+                        const float mn = fmaxf(m[q], mt);
+                        alpha[q] = ex2_approx(m[q] - mn);
+                        m[q] = mn;
+                        pv[q] = ex2_approx(x[q] - mn);
+                        l[q] = fmaf(l[q], alpha[q], pv[q]);
+                    } else {
+                        alpha[q] = 0.f;
+                        pv[q] = 0.f;
+                    }
+                }
+                // Keys at or beyond n in a partial tile: their V rows may hold anything (NaN in
+                // padded memory) and P = 0 does not cancel NaN in the MMA, so zero those rows.
+                // Whole 128-byte rows are zeroed, which the swizzle only permutes within.
+                if ((t + 1) * kTileKV > it.n) {
+                    mbar_wait(&v_full[vr.idx], vr.phase, wc);
+                    if (!valid) {
+                        uint8_t* rowp = smem + C::kOffV + vr.idx * C::kKVBytes + tid * 128;
+#pragma unroll
+                        for (int a = 0; a < C::kAtoms; ++a)
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                reinterpret_cast<uint4*>(rowp + a * (kTileKV * 128))[i] = make_uint4(0, 0, 0, 0);
+                    }
+                }
+                vr.advance();
+                mbar_wait(&p_empty[pr.idx], pr.phase ^ 1, wc);
+                uint8_t* sP = smem + C::kOffP + pr.idx * C::kPBytes;
+#pragma unroll
+                for (int q = 0; q < kN; ++q)
+                    *reinterpret_cast<uint16_t*>(sP + sw128_offset(q, tid, kN * 128)) = float_to_bf16_bits(pv[q]);
+                fence_proxy_async_smem();
+                mbar_arrive(&p_full[pr.idx]);
+                pr.advance();
+                if (t > it.t0) consume(alpha_prev);
+#pragma unroll
+                for (int q = 0; q < kN; ++q) alpha_prev[q] = alpha[q];
+            }
+            if (it.t1 > it.t0) consume(alpha_prev);
+
+            // ---- epilogue: L = sum over the 128 key lanes, O = acc / L, lse = ln2 * (m + log2 L)
+            float L[kN];
+            if (it.t1 > it.t0) {
+#pragma unroll
+                for (int q = 0; q < kN; ++q)
+                    if (q < G) {
+                        const float s = warp_sum(l[q]);
+                        if (lane == 0) red_sum[warp][q] = s;
+                    }
+                named_bar_sync(1, 128);
+#pragma unroll
+                for (int q = 0; q < kN; ++q) L[q] = (q < G) ? (red_sum[0][q] + red_sum[1][q]) + (red_sum[2][q] + red_sum[3][q]) : 1.f;
+            } else {
+#pragma unroll
+                for (int q = 0; q < kN; ++q) L[q] = 0.f;
+            }
+            if (aborted(wc)) continue;
+            const bool empty = it.t1 <= it.t0;
+            float local_amax = 0.f;
+            if (tid < D) {
+#pragma unroll
+                for (int q = 0; q < kN; ++q) {
+                    if (q >= G) break;
+                    const float o = empty ? 0.f : acc[q] / L[q];
+                    const float lse_v = empty ? -INFINITY : (m[q] + __log2f(L[q])) * kLn2;
+                    const size_t row = static_cast<size_t>(it.u) * G + q;
+                    if (it.whole) {
+                        if (p.o_stage) {
+                            p.o_stage[row * D + tid] = o;
+                            local_amax = fmaxf(local_amax, fabsf(o));
+                        }
+                        if (p.out) {
+                            if (p.out_f32)
+                                static_cast<float*>(p.out)[row * D + tid] = o;
+                            else
+                                static_cast<uint16_t*>(p.out)[row * D + tid] = float_to_bf16_bits(o);
+                        }
+                        if (tid == 0 && p.lse) p.lse[row] = lse_v;
+                    } else {
+                        p.part_o[(static_cast<size_t>(it.slot) * kN + q) * D + tid] = o;
+                        if (tid == 0) p.part_lse[static_cast<size_t>(it.slot) * kN + q] = lse_v;
+                    }
+                }
+            }
+            if (p.amax_bits && it.whole) {
+                const float wm = warp_max(local_amax);
+                if (lane == 0 && wm > 0.f) atomicMax(p.amax_bits, __float_as_uint(wm));
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) tmem_dealloc(tmem, C::kTmemCols);
+}
+
+// Exclusive prefix of per-unit tile counts (ragged keys), one block.
+__global__ void __launch_bounds__(1024) tile_prefix_kernel(const int32_t* seqlens, int Hkv, int U, int32_t* prefix)
+{
+    __shared__ int part[1024];
+    const int per = (U + 1023) / 1024;
+    const int b0 = threadIdx.x * per;
+    int s = 0;
+    for (int u = b0; u < min(U, b0 + per); ++u) s += (seqlens[u / Hkv] + kTileKV - 1) / kTileKV;
+    part[threadIdx.x] = s;
+    __syncthreads();
+    for (int off = 1; off < 1024; off <<= 1) {
+        const int v = threadIdx.x >= off ? part[threadIdx.x - off] : 0;
+        __syncthreads();
+        part[threadIdx.x] += v;
+        __syncthreads();
+    }
+    int run = threadIdx.x ? part[threadIdx.x - 1] : 0;
+    for (int u = b0; u < min(U, b0 + per); ++u) {
+        prefix[u] = run;
+        run += (seqlens[u / Hkv] + kTileKV - 1) / kTileKV;
+    }
+    if (threadIdx.x == 1023) prefix[U] = part[1023];
+}
+
+// Merges the partial results of units whose tiles were split over several CTAs, and writes the
+// result of units without keys (O = 0, LSE = -inf).  One block of D threads per query row.
+__global__ void combine_kernel(const __grid_constant__ DecodeParams p, int nctas)
+{
+    const int row = blockIdx.x;
+    const int u = row / p.G;
+    const int q = row % p.G;
+    const int d = threadIdx.x;
+    const int D = p.D;
+    int tiles;
+    long long Tu, T;
+    if (p.prefix) {
+        tiles = p.prefix[u + 1] - p.prefix[u];
+        Tu = p.prefix[u];
+        T = p.prefix[p.U];
+    } else {
+        tiles = p.tiles_uniform;
+        Tu = static_cast<long long>(u) * tiles;
+        T = static_cast<long long>(p.U) * tiles;
+    }
+    float o = 0.f, lse_v = -INFINITY;
+    if (tiles > 0) {
+        const long long P = nctas;
+        const int c0 = static_cast<int>(min((((Tu + 1) * P) - 1) / T, P - 1));
+        const int c1 = static_cast<int>(min((((Tu + tiles) * P) - 1) / T, P - 1));
+        if (c0 == c1) return;   // one CTA held the whole unit and wrote it
+        // CTAs with an empty tile range (possible when T < P) hold no partial
+        auto has_work = [&](int c) { return (c * T) / P != ((c + 1) * T) / P; };
+        float mx = -INFINITY;
+        for (int c = c0; c <= c1; ++c)
+            if (has_work(c)) mx = fmaxf(mx, p.part_lse[static_cast<size_t>(u + c) * kN + q]);
+        float sum = 0.f;
+        for (int c = c0; c <= c1; ++c)
+            if (has_work(c)) sum += __expf(p.part_lse[static_cast<size_t>(u + c) * kN + q] - mx);
+        lse_v = mx + __logf(sum);
+        for (int c = c0; c <= c1; ++c) {
+            if (!has_work(c)) continue;
+            const size_t sl = static_cast<size_t>(u + c) * kN + q;
+            o = fmaf(__expf(p.part_lse[sl] - lse_v), p.part_o[sl * D + d], o);
+        }
+    }
+    const size_t r = static_cast<size_t>(row);
+    if (p.o_stage) p.o_stage[r * D + d] = o;
+    if (p.out) {
+        if (p.out_f32)
+            static_cast<float*>(p.out)[r * D + d] = o;
+        else
+            static_cast<uint16_t*>(p.out)[r * D + d] = float_to_bf16_bits(o);
+    }
+    if (d == 0 && p.lse) p.lse[r] = lse_v;
+    if (p.amax_bits) {
+        const float wm = warp_max(fabsf(o));
+        if ((threadIdx.x & 31) == 0 && wm > 0.f) atomicMax(p.amax_bits, __float_as_uint(wm));
+    }
+}
+
+}  // namespace
+
+// ---- host side ------------------------------------------------------------------------------------
+namespace {
+
+struct DecodeWs {
+    size_t prefix_off, lse_off, o_off, stage_off, total;
+};
+
+DecodeWs decode_ws_layout(const AttnArgs& a, bool split, int nsm)
+{
+    auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
+    const size_t U = static_cast<size_t>(a.B) * a.Hkv;
+    const size_t slots = split ? U + nsm : 0;
+    DecodeWs w{};
+    size_t off = 0;
+    w.prefix_off = off;
+    off += (split && a.seqlens) ? al((U + 1) * 4) : 0;
+    w.lse_off = off;
+    off += al(slots * kN * 4);
+    w.o_off = off;
+    off += al(slots * kN * a.D * 4);
+    w.stage_off = off;
+    const bool stage = (a.out_kind == FMHA_OUT_NVFP4) && !a.out_f32;
+    off += stage ? al(static_cast<size_t>(a.B) * a.Hq * a.Sq * a.D * 4) : 0;
+    w.total = off;
+    return w;
+}
+
+template <int D>
+int run_decode(const AttnArgs& a, bool split, void* ws, cudaStream_t st)
+{
+    using C = DecodeCfg<D>;
+    const int nsm = num_sms();
+    if (nsm <= 0) return set_error(FMHA_ERR_CUDA, "cannot query the SM count");
+    const int U = a.B * a.Hkv;
+    const int G = (a.Hq / a.Hkv) * a.Sq;
+    const DecodeWs w = decode_ws_layout(a, split, nsm);
+    uint8_t* base = static_cast<uint8_t*>(ws);
+
+    CUtensorMap qmap, kmap, vmap;
+    {
+        const uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(G), static_cast<uint64_t>(U)};
+        const uint64_t strides[2] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(G) * D * 2};
+        const uint32_t box[3] = {64, static_cast<uint32_t>(kN), 1};
+        int rc = make_tmap_bf16(&qmap, a.q, 3, dims, strides, box);
+        if (rc) return rc;
+    }
+    {
+        const uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(a.Skv), static_cast<uint64_t>(U)};
+        const uint64_t strides[2] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(a.Skv) * D * 2};
+        const uint32_t box[3] = {64, static_cast<uint32_t>(kTileKV), 1};
+        int rc = make_tmap_bf16(&kmap, a.k, 3, dims, strides, box);
+        if (rc) return rc;
+        rc = make_tmap_bf16(&vmap, a.v, 3, dims, strides, box);
+        if (rc) return rc;
+    }
+
+    DecodeParams p{};
+    p.U = U;
+    p.Hkv = a.Hkv;
+    p.G = G;
+    p.Skv = a.Skv;
+    p.D = D;
+    p.c = a.scale * kLog2e;
+    p.seqlens = a.seqlens;
+    p.tiles_uniform = (a.Skv + kTileKV - 1) / kTileKV;
+    p.split = split ? 1 : 0;
+    p.prefix = (split && a.seqlens) ? reinterpret_cast<const int32_t*>(base + w.prefix_off) : nullptr;
+    const bool nvfp4 = a.out_kind == FMHA_OUT_NVFP4;
+    p.out = nvfp4 ? nullptr : a.out;
+    p.out_f32 = a.out_kind == FMHA_OUT_F32 ? 1 : 0;
+    p.lse = a.lse;
+    p.o_stage = nvfp4 ? (a.out_f32 ? a.out_f32 : reinterpret_cast<float*>(base + w.stage_off)) : nullptr;
+    p.amax_bits = nvfp4 ? reinterpret_cast<unsigned*>(a.amax_slot) : nullptr;
+    p.part_lse = split ? reinterpret_cast<float*>(base + w.lse_off) : nullptr;
+    p.part_o = split ? reinterpret_cast<float*>(base + w.o_off) : nullptr;
+    p.status = device_status_ptr();
+    p.limit = wait_limit();
+
+    if (p.prefix) {
+        tile_prefix_kernel<<<1, 1024, 0, st>>>(a.seqlens, a.Hkv, U, const_cast<int32_t*>(p.prefix));
+        FMHA_CHECK_LAUNCH("tile_prefix_kernel");
+        count_launch();
+    }
+    FMHA_CHECK_CUDA(cudaFuncSetAttribute(decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes));
+    const int grid = split ? nsm : (U < nsm ? U : nsm);
+    if (grid > 0) {
+        timing_mark_begin(st);
+        decode_kernel<D><<<grid, kThreads, C::kSmemBytes, st>>>(qmap, kmap, vmap, p);
+        timing_mark_end(st);
+        FMHA_CHECK_LAUNCH("decode_kernel");
+        count_launch();
+    }
+    if (split && U * G > 0) {
+        combine_kernel<<<U * G, D, 0, st>>>(p, grid);
+        FMHA_CHECK_LAUNCH("combine_kernel");
+        count_launch();
+    }
+    return FMHA_OK;
+}
+
+}  // namespace
+
+size_t decode_workspace_bytes(const AttnArgs& a, int num_splits)
+{
+    const int nsm = num_sms() > 0 ? num_sms() : 256;   // sized for the largest plausible SM count
+    const bool split = num_splits != 1;
+    return decode_ws_layout(a, split, nsm).total;
+}
+
+int launch_decode(const AttnArgs& a, int num_splits, void* ws, size_t ws_bytes, cudaStream_t st)
+{
+    const bool split = num_splits != 1 && ws != nullptr;
+    const int nsm = num_sms();
+    const DecodeWs w = decode_ws_layout(a, split, nsm);
+    if (w.total > 0 && (!ws || ws_bytes < w.total)) return set_error(FMHA_ERR_WORKSPACE, "decode: workspace too small");
+    switch (a.D) {
+        case 64: return run_decode<64>(a, split, ws, st);
+        case 128: return run_decode<128>(a, split, ws, st);
+        default: return set_error(FMHA_ERR_UNSUPPORTED, "decode path: D must be 64 or 128");
+    }
+}
+
+}  // namespace fmha

@@ -31,6 +31,11 @@ int* device_status_ptr();   // device address of the library's status word (curr
 long long wait_limit();     // cycles
 int num_sms();              // SMs of the current device
 
+// ---- launch accounting and the dominant-kernel timing hook ---------------------------------------
+void count_launch(int n = 1);                 // kernels this library launched (process-wide)
+void timing_mark_begin(cudaStream_t st);      // records the pending start event (one-shot), if any
+void timing_mark_end(cudaStream_t st);        // records the pending stop event and clears the hook
+
 // ---- TMA ---------------------------------------------------------------------------------------
 // Encodes a tiled map over a BF16 tensor with up to 3 dims (dim 0 innermost), 128-byte swizzle,
 // out-of-bounds elements filled with zero.  dims/box in elements, strides in bytes (dims 1..).

@@ -1,0 +1,450 @@
+#!/usr/bin/env python
+"""Benchmark of the fused attention library on one GB300 (or N replicas under torchrun).
+
+Headline line: decode, B8 Hq=Hkv=32 Sq1 Skv4096 D128, BF16 in / BF16 O + FP32 LSE, split-KV.
+`value` = algorithmic K/V bytes per step / device time per step (GB/s), inputs resident in HBM;
+every step's K/V (512 MiB) is larger than L2, so no flush is needed between steps.
+Also reported: the decode kernel's roofline fraction (timed alone through the library's timing
+hook), an end-to-end figure through the C ABI with pinned host buffers, the CPU oracle baseline,
+clock samples taken during the timed region, and the other specified workloads (single head,
+prefill, wide-head decode, ragged GQA decode with NVFP4 output) under "workloads".
+
+--impl reference times the CPU FP64 oracle on the same workload instead (bounded samples).
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode KV GB/s and prefill TFLOP/s per GB300; fraction of HBM / tensor roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu capture of the
+# named kernel, with the sha256 of its source file at capture time; reported only while the
+# source is unchanged.
+TRAFFIC = {}
+
+
+# ------------------------------------------------------------------------------------------------
+# clocks during the timed region (NVML through ctypes; read-only)
+# ------------------------------------------------------------------------------------------------
+class ClockSampler:
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown", 0x2: "applications_clocks"}
+
+    def __init__(self, device_index: int = 0, period_s: float = 0.002):
+        self.ok = False
+        self.samples = []
+        self.period = period_s
+        try:
+            self.nvml = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nvml.nvmlInit_v2() != 0:
+                return
+            self.dev = ctypes.c_void_p()
+            bus = None
+            try:
+                import torch
+                pr = torch.cuda.get_device_properties(device_index)
+                bus = f"{pr.pci_domain_id:08x}:{pr.pci_bus_id:02x}:{pr.pci_device_id:02x}.0".encode()
+            except Exception:
+                pass
+            rc = self.nvml.nvmlDeviceGetHandleByPciBusId_v2(bus, ctypes.byref(self.dev)) if bus else 1
+            if rc != 0 and self.nvml.nvmlDeviceGetHandleByIndex_v2(device_index, ctypes.byref(self.dev)) != 0:
+                return
+            mx = ctypes.c_uint()
+            self.nvml.nvmlDeviceGetMaxClockInfo(self.dev, 1, ctypes.byref(mx))
+            self.max_mhz = mx.value
+            self.ok = True
+        except OSError:
+            pass
+
+    def _run(self):
+        clk = ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            self.nvml.nvmlDeviceGetClockInfo(self.dev, 1, ctypes.byref(clk))
+            if self.nvml.nvmlDeviceGetCurrentClocksEventReasons(self.dev, ctypes.byref(rs)) != 0:
+                self.nvml.nvmlDeviceGetCurrentClocksThrottleReasons(self.dev, ctypes.byref(rs))
+            self.samples.append((clk.value, rs.value))
+            time.sleep(self.period)
+
+    def start(self):
+        if not self.ok:
+            return
+        self._stop = threading.Event()
+        self._t = threading.Thread(target=self._run, daemon=True)
+        self._t.start()
+
+    def stop(self):
+        if not self.ok:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvml unavailable"], "samples": 0}
+        self._stop.set()
+        self._t.join()
+        mhz = [s[0] for s in self.samples]
+        bits = 0
+        for s in self.samples:
+            bits |= s[1]
+        reasons = [n for b, n in self.REASONS.items() if bits & b]
+        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(mhz)}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def source_sha(name: str) -> str:
+    p = os.path.join(ROOT, "attention_tensor_cores_gb300", "csrc", name)
+    return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
+
+
+def traffic_for(kernel: str, src: str, launches_per_step: int = 1):
+    t = TRAFFIC.get(kernel)
+    if not t or t.get("source_sha") != source_sha(src):
+        return None
+    return t["bytes"]
+
+
+# ------------------------------------------------------------------------------------------------
+# one workload on the GPU
+# ------------------------------------------------------------------------------------------------
+class Case:
+    """Device inputs/outputs of one workload and the library call that processes them."""
+
+    def __init__(self, F, w, num_splits=0, pad_fill=None):
+        import torch
+        self.F, self.w = F, w
+        self.q, self.k, self.v, self.sl = w.make("cuda", pad_fill=pad_fill)
+        B, Hq, Sq, D = self.q.shape
+        self.n_out = B * Hq * Sq * D
+        kind = {"bf16": F.FMHA_OUT_BF16, "f32": F.FMHA_OUT_F32, "nvfp4": F.FMHA_OUT_NVFP4}[w.out_kind]
+        self.scales = self.ts = None
+        if w.out_kind == "nvfp4":
+            self.out = torch.empty(self.n_out // 2, dtype=torch.uint8, device="cuda")
+            self.scales = torch.empty(self.n_out // 16, dtype=torch.uint8, device="cuda")
+            self.ts = torch.empty(1, dtype=torch.float32, device="cuda")
+        else:
+            dt = torch.bfloat16 if w.out_kind == "bf16" else torch.float32
+            self.out = torch.empty(B, Hq, Sq, D, dtype=dt, device="cuda")
+        self.lse = torch.empty(B, Hq, Sq, dtype=torch.float32, device="cuda")
+        opts = F.make_opts(kind, self.sl, num_splits, None, self.scales, self.ts, None)
+        wsb = F.fmha_workspace_size(B, Hq, w.Hkv, Sq, w.Skv, D, opts)
+        self.ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device="cuda") if wsb else None
+        self.opts = F.make_opts(kind, self.sl, num_splits, self.ws, self.scales, self.ts, None)
+
+    def call(self, q=None, k=None, v=None):
+        self.F.fmha_fwd_ex(self.q if q is None else q, self.k if k is None else k, self.v if v is None else v,
+                           self.out, self.lse, self.w.scale, self.opts)
+
+    def algorithmic_bytes(self) -> int:
+        """K/V rows actually read, plus Q, O and LSE."""
+        w = self.w
+        o_bytes = {"bf16": 2, "f32": 4, "nvfp4": 0.5 + 1 / 16}[w.out_kind] * self.n_out
+        return int(w.kv_bytes() + self.q.numel() * 2 + o_bytes + self.lse.numel() * 4)
+
+
+def time_case(F, case, steps, warmup, sampler=None, dist=None):
+    import torch
+    for _ in range(warmup):
+        case.call()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in kev:            # creates the event handles the library records
+        a.record()
+        b.record()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    l0 = F.fmha_launch_count()
+    if sampler:
+        sampler.start()
+    for i in range(steps):
+        ev[i][0].record()
+        F.fmha_time_next_call(kev[i][0], kev[i][1])
+        case.call()
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    if dist is not None:
+        dist.barrier()
+    launches = F.fmha_launch_count() - l0
+    assert F.fmha_check_status() == 0, "device status word set during the benchmark"
+    return {
+        "region_ms": ev[0][0].elapsed_time(ev[-1][1]),
+        "step_ms": [a.elapsed_time(b) for a, b in ev],
+        "kernel_ms": [a.elapsed_time(b) for a, b in kev],
+        "launches": launches,
+        "clocks": clocks,
+    }
+
+
+def time_e2e(F, case, steps, warmup):
+    """Same call with pinned host inputs: H2D copies + attention + D2H of O and LSE per step."""
+    import torch
+    qh = case.q.cpu().pin_memory()
+    kh = case.k.cpu().pin_memory()
+    vh = case.v.cpu().pin_memory()
+    outh = torch.empty(case.out.shape, dtype=case.out.dtype, pin_memory=True)
+    lseh = torch.empty(case.lse.shape, dtype=case.lse.dtype, pin_memory=True)
+    qd, kd, vd = torch.empty_like(case.q), torch.empty_like(case.k), torch.empty_like(case.v)
+
+    def step():
+        qd.copy_(qh, non_blocking=True)
+        kd.copy_(kh, non_blocking=True)
+        vd.copy_(vh, non_blocking=True)
+        case.call(qd, kd, vd)
+        outh.copy_(case.out, non_blocking=True)
+        lseh.copy_(case.lse, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        step()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    h2d = (qh.numel() + kh.numel() + vh.numel()) * 2
+    d2h = outh.numel() * outh.element_size() + lseh.numel() * 4
+    del qh, kh, vh, qd, kd, vd
+    return ms, h2d, d2h
+
+
+# ------------------------------------------------------------------------------------------------
+# CPU oracle baseline
+# ------------------------------------------------------------------------------------------------
+def oracle_sample(w, rows_per_step: int, step: int):
+    """Inputs for a bounded sample of `w`: `rows_per_step` consecutive query rows (whole heads),
+    regenerated on the CPU.  Returns (callable, algorithmic K/V bytes, FLOPs, description)."""
+    import numpy as np
+    import oracle
+    total = w.B * w.Hq * w.Sq
+    r0 = (step * rows_per_step) % total
+    rows = np.arange(r0, min(total, r0 + rows_per_step), dtype=np.int64)
+    sl = w.seqlens()
+    g = w.Hq // w.Hkv
+    groups = {}
+    for r in rows:
+        b = int(r // (w.Hq * w.Sq))
+        hq = int((r // w.Sq) % w.Hq)
+        groups.setdefault((b, hq // g), []).append(int(r))
+    jobs = []
+    kv_bytes = flops = 0
+    for (b, kvh), rr in groups.items():
+        n = w.Skv if sl is None else int(sl[b])
+        kk, vv = w.kv_head_np(b, kvh, n)
+        qq = w.q_rows_np(rr)
+        jobs.append((qq.reshape(1, 1, len(rr), w.D), kk.reshape(1, 1, n, w.D), vv.reshape(1, 1, n, w.D)))
+        kv_bytes += 2 * n * w.D * 2 * len(rr) / (g * w.Sq)   # each K/V head counted once per group
+        flops += 4 * n * w.D * len(rr)
+
+    def run():
+        for qq, kk, vv in jobs:
+            oracle.attention(qq, kk, vv, w.scale)
+
+    return run, kv_bytes, flops, f"{len(rows)} query rows from row {r0}"
+
+
+def cpu_baseline(w, metric_unit: str, budget_s: float = 8.0, rows_per_step: int = 64):
+    import oracle
+    run, kvb, fl, desc = oracle_sample(w, rows_per_step, 0)
+    run()   # builds/loads the library, touches memory
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        run()
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or reps >= 50:
+            break
+    per = el / reps
+    val = (kvb / per / 1e9) if metric_unit == "GB/s" else (fl / per / 1e12)
+    return {"value": val, "unit": metric_unit, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{desc} of {w.name}, {reps} repetitions, {per * 1e3:.1f} ms each"}
+
+
+# ------------------------------------------------------------------------------------------------
+# arms
+# ------------------------------------------------------------------------------------------------
+def _max_over_ranks(x: float, dist):
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _workload_entry(F, w, idx, steps, warmup, peaks):
+    """Timing + roofline of one extra workload (rank 0 only)."""
+    import torch
+    case = Case(F, w, num_splits=0)
+    r = time_case(F, case, steps, warmup)
+    step_ms = r["region_ms"] / steps
+    kern_ms = statistics.mean(r["kernel_ms"])
+    e = {"workload": w.name, "ms_per_step": step_ms, "kernel_ms": kern_ms, "gpu_launches_per_step": r["launches"] / steps}
+    if idx == 2:   # prefill: tensor-bound
+        tf = w.flops() / (step_ms / 1e3) / 1e12
+        ach = w.flops() / (kern_ms / 1e3) / 1e12
+        e.update({"value": tf, "unit": "TFLOP/s",
+                  "roofline": {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                               "frac": ach / peaks["bf16_tflops"], "traffic": None}})
+    elif idx == 0:
+        e.update({"value": step_ms * 1e3, "unit": "us", "note": "latency-bound, fits in L2: no roofline claim"})
+    else:
+        gbs = w.kv_bytes() / (step_ms / 1e3) / 1e9
+        ach = case.algorithmic_bytes() / (kern_ms / 1e3) / 1e9
+        e.update({"value": gbs, "unit": "GB/s", "kv_bytes": w.kv_bytes(), "flops": w.flops(),
+                  "tflops": w.flops() / (step_ms / 1e3) / 1e12,
+                  "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                               "frac": ach / peaks["hbm_gbs"], "traffic": None}})
+    del case
+    torch.cuda.empty_cache()
+    return e
+
+
+def run_ours(args, rank, world, local):
+    import torch
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as td
+        td.init_process_group("nccl", device_id=torch.device("cuda", local))
+        dist = td
+    import __graft_entry__ as ge
+    if rank == 0:
+        ge.build()
+    if dist is not None:
+        dist.barrier()
+        if rank != 0:
+            ge.build()
+    import attention_tensor_cores_gb300 as F
+    from attention_tensor_cores_gb300 import inputs
+    F.load()
+    peaks, peaks_src = load_peaks()
+    wl = inputs.workloads()
+    w = wl[1]
+    head = Case(F, w, num_splits=0)
+    sampler = ClockSampler(local)
+    r = time_case(F, head, args.steps, args.warmup, sampler, dist)
+    region_ms = _max_over_ranks(r["region_ms"], dist)
+    step_ms = region_ms / args.steps
+    value = world * args.steps * w.kv_bytes() / (region_ms / 1e3) / 1e9
+    kern_ms = statistics.mean(r["kernel_ms"])
+    achieved = head.algorithmic_bytes() / (kern_ms / 1e3) / 1e9
+    roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": achieved / peaks["hbm_gbs"], "traffic": traffic_for("decode_kernel<128>", "decode.cu"),
+            "kernel": "decode_kernel<128>", "kernel_ms": kern_ms, "algorithmic_bytes": head.algorithmic_bytes(),
+            "peak_source": f"{peaks_src} HBM copy bandwidth (burst)"}
+    e2e_ms, h2d, d2h = time_e2e(F, head, args.steps, min(args.warmup, 3))
+    e2e_ms = _max_over_ranks(e2e_ms, dist)
+    e2e = {"value": world * w.kv_bytes() / (e2e_ms / 1e3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+    del head
+    torch.cuda.empty_cache()
+    extra = {}
+    if rank == 0 and not args.only_headline:
+        for idx in (0, 2, 3, 4):
+            try:
+                extra[f"c{idx + 1}"] = _workload_entry(F, wl[idx], idx, min(args.steps, 10), args.warmup, peaks)
+            except F.FmhaError as ex:
+                extra[f"c{idx + 1}"] = {"workload": wl[idx].name, "unsupported": str(ex)}
+    cpu = cpu_baseline(w, "GB/s") if (rank == 0 and world == 1) else None
+    if dist is not None:
+        dist.barrier()
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name + ", + FP32 LSE", "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Sq": w.Sq,
+                   "Skv": w.Skv, "D": w.D, "kv_bytes_per_step": w.kv_bytes(),
+                   "l2": "inputs larger than L2 (512 MiB of K/V per step, L2 126.5 MiB): no flush",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": r["launches"],
+        "clocks": r["clocks"], "workloads": extra,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_reference(args, rank, world):
+    """The CPU FP64 oracle on the headline workload, bounded samples (whole heads) per step."""
+    if rank != 0:
+        return
+    import oracle
+    from attention_tensor_cores_gb300 import inputs
+    oracle.build()
+    w = inputs.workloads()[1]
+    rows_per_step = 32
+    cache = {}
+
+    def sample(i):
+        key = i % 8
+        if key not in cache:
+            cache[key] = oracle_sample(w, rows_per_step, key)
+        return cache[key]
+
+    for i in range(args.warmup):
+        sample(i)[0]()
+    times, kvb = [], 0.0
+    for i in range(args.steps):
+        run, b, _, _ = sample(args.warmup + i)
+        t0 = time.perf_counter()
+        run()
+        times.append(time.perf_counter() - t0)
+        kvb += b
+    tot = sum(times)
+    val = kvb / tot / 1e9
+    desc = f"{rows_per_step} query rows (one batch entry, all heads) of {w.name} per step"
+    line = {
+        "metric": METRIC, "value": val, "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": tot / args.steps * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic", "impl": "reference",
+        "config": {"workload": w.name + ", + FP32 LSE", "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Sq": w.Sq, "Skv": w.Skv,
+                   "D": w.D, "parallelism": "host cores (OpenMP)"},
+        "cpu_baseline": {"value": val, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle", "sample": desc},
+        "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--only-headline", action="store_true", help="skip the other workloads")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

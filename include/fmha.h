@@ -128,6 +128,17 @@ int fmha_check_status(fmha_stream_t stream);
 /* Bounded-wait limit in SM clock cycles for later launches (0 = default, about 2 s). */
 void fmha_set_wait_limit(long long cycles);
 
+/* Number of kernels this library has launched in this process (all devices, all threads). */
+long long fmha_launch_count(void);
+
+/*
+ * Timing hook, one-shot and per calling thread: the next attention / quantisation call records
+ * `start_event` on its stream immediately before launching its dominant kernel (the attention
+ * kernel; the quantiser for nvfp4_quantize) and `stop_event` right after it.  Both are
+ * cudaEvent_t handles owned by the caller; NULL, NULL clears the hook.
+ */
+void fmha_time_next_call(void* start_event, void* stop_event);
+
 /* Static text for a status code. */
 const char* fmha_error_string(int code);
 

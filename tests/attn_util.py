@@ -1,0 +1,108 @@
+"""Helpers for the GPU parity tests: run the library through the C ABI and compare with the
+FP64 oracle (full tensors for small cases, sampled rows for the full-size workloads)."""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+import oracle
+from attention_tensor_cores_gb300 import inputs
+
+# Tolerances: O max |err| <= 2e-2 and mean |err| <= 2e-3; LSE |err| <= 1e-3 * max(1, |lse|).
+O_MAX = 2e-2
+O_MEAN = 2e-3
+LSE_REL = 1e-3
+
+
+def run_attention(F, q, k, v, scale, out_kind="bf16", seqlens=None, num_splits=None, want_f32=False):
+    """Calls fmha_fwd (no options) or fmha_fwd_ex; returns dict of host numpy results."""
+    B, Hq, Sq, D = q.shape
+    Hkv, Skv = k.shape[1], k.shape[2]
+    lse = torch.full((B, Hq, Sq), float("nan"), dtype=torch.float32, device="cuda")
+    res = {}
+    if out_kind == "bf16" and seqlens is None and num_splits is None:
+        out = torch.full((B, Hq, Sq, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+        F.fmha_fwd(q, k, v, out, lse, scale)
+        torch.cuda.synchronize()
+        res["o"] = out.float().cpu().numpy().reshape(-1, D)
+    else:
+        kind = {"bf16": F.FMHA_OUT_BF16, "f32": F.FMHA_OUT_F32, "nvfp4": F.FMHA_OUT_NVFP4}[out_kind]
+        n = B * Hq * Sq * D
+        if out_kind == "nvfp4":
+            out = torch.zeros(n // 2, dtype=torch.uint8, device="cuda")
+            scales = torch.zeros(n // 16, dtype=torch.uint8, device="cuda")
+            ts = torch.zeros(1, dtype=torch.float32, device="cuda")
+            f32 = torch.full((n,), float("nan"), dtype=torch.float32, device="cuda") if want_f32 else None
+        else:
+            dt = torch.bfloat16 if out_kind == "bf16" else torch.float32
+            out = torch.full((B, Hq, Sq, D), float("nan"), dtype=dt, device="cuda")
+            scales = ts = f32 = None
+        ns = 0 if num_splits is None else num_splits
+        opts = F.make_opts(kind, seqlens, ns, None, scales, ts, f32)
+        wsb = F.fmha_workspace_size(B, Hq, Hkv, Sq, Skv, D, opts)
+        ws = torch.empty(max(wsb, 1), dtype=torch.uint8, device="cuda") if wsb else None
+        opts = F.make_opts(kind, seqlens, ns, ws, scales, ts, f32)
+        F.fmha_fwd_ex(q, k, v, out, lse, scale, opts)
+        torch.cuda.synchronize()
+        if out_kind == "nvfp4":
+            res["codes"] = out.cpu().numpy()
+            res["scales"] = scales.cpu().numpy()
+            res["tensor_scale"] = float(ts.cpu()[0])
+            if want_f32:
+                res["o"] = f32.cpu().numpy().reshape(-1, D)
+        else:
+            res["o"] = out.float().cpu().numpy().reshape(-1, D)
+    res["lse"] = lse.cpu().numpy().reshape(-1)
+    assert F.fmha_check_status() == 0, "device status word set (bounded wait expired)"
+    return res
+
+
+def check_o_lse(o, lse, o_ref, lse_ref, what=""):
+    assert o.shape == o_ref.shape, (o.shape, o_ref.shape)
+    err = np.abs(o.astype(np.float64) - o_ref)
+    assert np.all(np.isfinite(o)), f"{what}: non-finite O"
+    assert err.max() <= O_MAX, f"{what}: max|dO| = {err.max():.3e}"
+    assert err.mean() <= O_MEAN, f"{what}: mean|dO| = {err.mean():.3e}"
+    if lse is not None:
+        fin = np.isfinite(lse_ref)
+        assert np.array_equal(np.isfinite(lse), fin) and np.all(lse[~fin] == lse_ref[~fin]), f"{what}: LSE inf pattern"
+        lerr = np.abs(lse[fin].astype(np.float64) - lse_ref[fin])
+        assert np.all(lerr <= LSE_REL * np.maximum(1.0, np.abs(lse_ref[fin]))), f"{what}: max|dLSE| = {lerr.max():.3e}"
+    return float(err.max()), float(err.mean())
+
+
+def oracle_rows(w: inputs.Workload, rows):
+    """FP64 oracle for flat query rows of workload `w`, from regenerated slices only."""
+    sl = w.seqlens()
+    g = w.Hq // w.Hkv
+    o = np.zeros((len(rows), w.D))
+    lse = np.zeros(len(rows))
+    qs = w.q_rows_np(rows)
+    cache = {}
+    for i, r in enumerate(rows):
+        b = r // (w.Hq * w.Sq)
+        hq = (r // w.Sq) % w.Hq
+        kvh = hq // g
+        n = w.Skv if sl is None else int(sl[b])
+        key = (b, kvh)
+        if key not in cache:
+            cache = {key: w.kv_head_np(b, kvh, n)}
+        kk, vv = cache[key]
+        if n == 0:
+            o[i] = 0.0
+            lse[i] = -math.inf
+            continue
+        oi, li = oracle.attention(qs[i].reshape(1, 1, 1, w.D), kk.reshape(1, 1, n, w.D), vv.reshape(1, 1, n, w.D), w.scale)
+        o[i] = oi[0]
+        lse[i] = li[0]
+    return o, lse
+
+
+def sample_rows(w: inputs.Workload, count: int, seed: int = 0):
+    """Sorted sample of flat query rows covering first/last rows and a seeded random spread."""
+    total = w.B * w.Hq * w.Sq
+    rng = np.random.default_rng(seed)
+    rows = set([0, total - 1]) | set(rng.choice(total, size=min(count, total), replace=False).tolist())
+    return np.array(sorted(rows), dtype=np.int64)
