@@ -83,6 +83,7 @@ def load(path: str | None = None):
             "fmha_num_sms": ([], I),
             "fmha_launch_count": ([], ctypes.c_longlong),
             "fmha_time_next_call": ([V, V], None),
+            "fmha_fwd_decode_noalloc": ([V, V, V, V, V, I, I, I, I, I, I, F, V, V], I),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name, None)
@@ -206,3 +207,13 @@ def fmha_launch_count() -> int:
 def fmha_time_next_call(start_event, stop_event):
     """torch.cuda.Event pair (enable_timing=True, already recorded once so the handle exists)."""
     load().fmha_time_next_call(ctypes.c_void_p(start_event.cuda_event), ctypes.c_void_p(stop_event.cuda_event))
+
+
+def fmha_fwd_decode_noalloc(q, k, v, out, lse, scale: float, seqlens_k=None, stream=None):
+    """Split-KV decode whose scratch is the library's fixed device array (nothing is allocated)."""
+    _need_cuda(q, k, v, out, lse, seqlens_k)
+    B, Hq, Sq, D = q.shape
+    Hkv, Skv = k.shape[1], k.shape[2]
+    rc = load().fmha_fwd_decode_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Sq, Skv, D,
+                                        float(scale), _ptr(seqlens_k), _stream(stream))
+    _check(rc, "fmha_fwd_decode_noalloc")

@@ -28,6 +28,9 @@
 //    the device status word.
 #include <cuda_runtime.h>
 
+#include <atomic>
+#include <cstdio>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -731,3 +734,95 @@ int launch_decode(const AttnArgs& a, int num_splits, void* ws, size_t ws_bytes, 
 }
 
 }  // namespace fmha
+
+// ================================================================================================
+// Split-KV decode without any device allocation by the caller or the library.
+//
+// Some callers cannot provide the workspace that fmha_fwd_ex's split-KV path needs: plug-ins and
+// foreign-language bindings that are handed only tensor pointers and have no allocator to ask,
+// and latency-critical loops that must not call cudaMalloc (it can synchronise the device and
+// its latency is unbounded).  For them the split partials and the tile prefix live in the fixed
+// array below, which every GPU that loads this library holds until the process exits.
+//
+// The array is shared by every call on a device and keeps the contents of the last call.  No
+// part of it needs to start at zero: each byte a call reads (tile prefix, partial O and LSE) is
+// written earlier in the same call.  Calls that overlap on the GPU (different streams, or
+// different host threads, without ordering between them) race on it.
+// ================================================================================================
+static __device__ __align__(256) unsigned char g_fmha_decode_scratch[FMHA_NOALLOC_SCRATCH_BYTES];
+
+namespace fmha {
+namespace {
+
+constexpr int kMaxScratchDevices = 64;
+std::atomic<void*> g_decode_scratch_addr[kMaxScratchDevices];
+
+// Device address of the scratch array on the current device, looked up once per device (with
+// that device current) and cached.
+int decode_scratch_address(void** out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_error(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxScratchDevices) return set_error(FMHA_ERR_UNSUPPORTED, "device index out of range");
+    void* p = g_decode_scratch_addr[dev].load();
+    if (!p) {
+        e = cudaGetSymbolAddress(&p, g_fmha_decode_scratch);
+        if (e != cudaSuccess) return cuda_error(e, "cudaGetSymbolAddress(decode scratch)");
+        g_decode_scratch_addr[dev].store(p);
+    }
+    *out = p;
+    return FMHA_OK;
+}
+
+}  // namespace
+}  // namespace fmha
+
+extern "C" int fmha_fwd_decode_noalloc(const void* q, const void* k, const void* v, void* out, float* lse, int B,
+                                       int Hq, int Hkv, int Sq, int Skv, int D, float scale,
+                                       const int32_t* seqlens_k, fmha_stream_t stream)
+{
+    using namespace fmha;
+    if (!q || !k || !v || !out) return set_error(FMHA_ERR_INVALID, "fmha_fwd_decode_noalloc: NULL q/k/v/out");
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Sq < 0 || Skv <= 0 || Hq % Hkv != 0)
+        return set_error(FMHA_ERR_INVALID, "fmha_fwd_decode_noalloc: need B >= 0, Sq >= 0, Skv >= 1, Hq % Hkv == 0");
+    if (D != 64 && D != 128) return set_error(FMHA_ERR_INVALID, "fmha_fwd_decode_noalloc: D must be 64 or 128");
+    if (static_cast<long long>(Hq / Hkv) * Sq > 16)
+        return set_error(FMHA_ERR_INVALID, "fmha_fwd_decode_noalloc: at most 16 query rows per key/value head");
+    auto mis = [](const void* p, uintptr_t m) { return (reinterpret_cast<uintptr_t>(p) & m) != 0; };
+    if (mis(q, 15) || mis(k, 15) || mis(v, 15) || mis(out, 15) || mis(lse, 3) || mis(seqlens_k, 3))
+        return set_error(FMHA_ERR_INVALID, "fmha_fwd_decode_noalloc: q/k/v/out 16-byte, lse/seqlens 4-byte aligned");
+    if (static_cast<long long>(B) * Hkv * Skv >= (1LL << 31))
+        return set_error(FMHA_ERR_UNSUPPORTED, "fmha_fwd_decode_noalloc: more than 2^31 key rows");
+    if (static_cast<long long>(B) * Hq * Sq == 0) return FMHA_OK;
+    if (!device_status_ptr()) return set_error(FMHA_ERR_CUDA, "no CUDA device");
+
+    AttnArgs a{};
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.out = out;
+    a.lse = lse;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.Sq = Sq;
+    a.Skv = Skv;
+    a.D = D;
+    a.scale = scale;
+    a.seqlens = seqlens_k;
+    a.out_kind = FMHA_OUT_BF16;
+    const size_t need = decode_workspace_bytes(a, 0);
+    if (need > FMHA_NOALLOC_SCRATCH_BYTES) {
+        char msg[200];
+        snprintf(msg, sizeof msg,
+                 "fmha_fwd_decode_noalloc: this problem needs %zu bytes of split-KV scratch, the static area holds %zu "
+                 "(B*Hkv and the SM count set the size)",
+                 need, static_cast<size_t>(FMHA_NOALLOC_SCRATCH_BYTES));
+        return set_error(FMHA_ERR_WORKSPACE, msg);
+    }
+    void* scratch = nullptr;
+    int rc = decode_scratch_address(&scratch);
+    if (rc) return rc;
+    return launch_decode(a, 0, scratch, FMHA_NOALLOC_SCRATCH_BYTES, reinterpret_cast<cudaStream_t>(stream));
+}

@@ -128,6 +128,25 @@ int fmha_check_status(fmha_stream_t stream);
 /* Bounded-wait limit in SM clock cycles for later launches (0 = default, about 2 s). */
 void fmha_set_wait_limit(long long cycles);
 
+/*
+ * Split-KV decode that allocates nothing.  The pages have no counterpart: it serves callers that
+ * cannot hand the library a workspace, such as plug-ins and foreign-language bindings that see
+ * only tensor pointers and have no allocator to ask, or latency-critical loops that must not call
+ * cudaMalloc (it can synchronise the device and its latency is unbounded).
+ *   Same arguments and results as fmha_fwd (BF16 out, optional LSE) plus seqlens_k (device
+ *   int32[B] or NULL, as in fmha_opts); at most 16 query rows per key/value head, D = 64 or 128.
+ *   The split-KV scratch (partials and tile prefix) is a fixed array of FMHA_NOALLOC_SCRATCH_BYTES
+ *   inside the library, held by every GPU that loads it until the process exits; a problem that
+ *   needs more returns FMHA_ERR_WORKSPACE with the size in fmha_last_error().  The library calls
+ *   no allocation routine.  The first call on a device looks up that device's address of the
+ *   array (make it before any stream capture).  All calls on a device share the array: calls that
+ *   overlap on the GPU race and must be ordered by the caller.
+ */
+#define FMHA_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u)
+int fmha_fwd_decode_noalloc(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq,
+                            int Hkv, int Sq, int Skv, int D, float scale, const int32_t* seqlens_k,
+                            fmha_stream_t stream);
+
 /* Number of kernels this library has launched in this process (all devices, all threads). */
 long long fmha_launch_count(void);
 
