@@ -33,7 +33,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu capture of the
 # named kernel, with the sha256 of its source file at capture time; reported only while the
 # source is unchanged.
-TRAFFIC = {}
+TRAFFIC = {
+    # decode B8 H32 Sq1 Skv4096 D128: read 537,045,760 + written 2,796,800 bytes (profiles/decode_kernel_decode-B8-H32-Skv4096-D128.md)
+    "decode_kernel<128>": {"bytes": 539842560, "source_sha": "19cdb3b4f432a765"},
+}
 
 
 # ------------------------------------------------------------------------------------------------
@@ -434,7 +437,23 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--only-headline", action="store_true", help="skip the other workloads")
+    ap.add_argument("--profile", choices=["c1", "c2", "c3", "c4", "c5"], default=None,
+                    help="run one workload's call --repeat times, untimed (for a profiler)")
+    ap.add_argument("--repeat", type=int, default=5)
     args = ap.parse_args()
+    if args.profile:
+        import torch
+        import __graft_entry__ as ge
+        ge.build()
+        import attention_tensor_cores_gb300 as F
+        from attention_tensor_cores_gb300 import inputs
+        case = Case(F, inputs.workloads()[int(args.profile[1]) - 1], num_splits=0)
+        for _ in range(args.repeat):
+            case.call()
+        torch.cuda.synchronize()
+        assert F.fmha_check_status() == 0
+        print(f"profile run of {case.w.name}: {args.repeat} calls ok")
+        return
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     world = int(os.environ.get("WORLD_SIZE", "1"))
