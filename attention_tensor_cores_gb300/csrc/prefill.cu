@@ -1,9 +1,514 @@
-// Row-tile attention (placeholder until the kernel lands).
+// Row-tile attention: 128 query rows per MMA tile, for problems with more than 16 query rows per
+// key/value head (prefill, large GQA groups).
+//
+// Follows the kernel plan of "NVFP4-1.1_RAW_CUDA_CPP_APPROACH.md" (nvfp4-megamoe-kernel): TMA for
+// Q/K/V, tcgen05 MMA into a Tensor Memory accumulator, softmax warps reading S with tcgen05.ld and
+// writing P back to Tensor Memory for the PV product ("SS" QK, "TS" PV with A = P in TMEM), the
+// in-kernel softmax with O rescale over several KV tiles.  The GB300 design:
+//
+//  * A persistent CTA owns a PAIR of 128-row query tiles of one (b, kv-head) unit and streams
+//    that unit's K/V tiles (128 keys) through TMA rings.  Two softmax warpgroups (one per query
+//    tile) ping-pong: while one computes exponentials the tensor core runs the other's MMAs.
+//  * Tensor Memory (512 columns) for D = 64: S0, S1 (128 each), P0, P1 (64 each, BF16 pairs),
+//    O0, O1 (64 each).  For D = 128 P is written over the first half of its S buffer.
+//  * Rows are one per thread (thread t of a warpgroup owns TMEM lane t), so row max / sum need
+//    no cross-thread reduction.
+//  * Lazy rescale: the running max m used for P only moves when a tile's max exceeds it by more
+//    than 2^8 (log2 units), so O in TMEM is rescaled (ld/mul/st) only a few times per row; P
+//    stays <= 256, and the final O / l and LSE use the same m, so the result is exact.
+//  * One MMA thread polls the readiness of every pending QK / PV (non-blocking mbarrier tests)
+//    and issues whichever can go, so a slow softmax of one tile never blocks the other's MMAs.
+//  * Every wait is bounded (clock64 limit); a timeout sets the device status word and the CTA
+//    drains without issuing more copies or MMAs.
+#include <cuda_runtime.h>
+
 #include "internal.h"
+#include "ptx.cuh"
+
 namespace fmha {
-size_t prefill_workspace_bytes(const AttnArgs&) { return 0; }
-int launch_prefill(const AttnArgs&, void*, size_t, cudaStream_t)
+namespace {
+
+constexpr int kTM = 128;          // query rows per tile (MMA M)
+constexpr int kTN = 128;          // keys per tile
+constexpr int kPThreads = 320;    // 2 softmax warpgroups + TMA warp + MMA warp
+constexpr float kLog2eP = 1.4426950408889634f;
+constexpr float kLn2P = 0.6931471805599453f;
+constexpr float kRescaleLog2 = 8.0f;
+
+template <int D>
+struct PrefillCfg {
+    static constexpr int kAtoms = D / 64;
+    static constexpr int kQStages = (D == 64) ? 2 : 1;
+    static constexpr int kStages = (D == 64) ? 4 : 2;
+    static constexpr int kQTileBytes = kAtoms * kTM * 128;
+    static constexpr int kQBytes = 2 * kQTileBytes;
+    static constexpr int kKVBytes = kAtoms * kTN * 128;
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffK = kOffQ + kQStages * kQBytes;
+    static constexpr int kOffV = kOffK + kStages * kKVBytes;
+    static constexpr int kSmemBytes = kOffV + kStages * kKVBytes + 1024;
+    static constexpr bool kAliasP = (D != 64);
+    static constexpr uint32_t kColP = kAliasP ? 0u : 256u;     // P_q at kColP + q * kPStride
+    static constexpr uint32_t kPStride = kAliasP ? 128u : 64u;
+    static constexpr uint32_t kColO = kAliasP ? 256u : 384u;   // O_q at kColO + q * D
+};
+
+struct PrefillParams {
+    int U;          // units = B * Hkv
+    int Hkv;
+    int R;          // query rows per unit = (Hq / Hkv) * Sq
+    int Skv;
+    int pairs;      // ceil(R / 256)
+    float c;        // scale * log2(e)
+    const int32_t* seqlens;
+    void* out;
+    int out_f32;
+    float* lse;
+    float* o_stage;
+    unsigned* amax_bits;
+    int* status;
+    long long limit;
+};
+
+__device__ __forceinline__ int unit_keys(const PrefillParams& p, int u)
 {
-    return set_error(FMHA_ERR_UNSUPPORTED, "row-tile path (more than 16 query rows per key/value head) not built yet");
+    return p.seqlens ? p.seqlens[u / p.Hkv] : p.Skv;
 }
+
+__device__ __forceinline__ void drain_wait_p(uint64_t* bar, uint32_t parity, long long limit)
+{
+    const uint32_t a = smem_u32(bar);
+    const long long t0 = clock64();
+    while (!mbar_try_wait(a, parity)) {
+        if (clock64() - t0 > limit) return;
+    }
+}
+
+struct PRing {
+    uint32_t idx = 0, phase = 0;
+    int n;
+    __device__ explicit PRing(int stages) : n(stages) {}
+    __device__ void advance()
+    {
+        if (++idx == static_cast<uint32_t>(n)) {
+            idx = 0;
+            phase ^= 1;
+        }
+    }
+};
+
+template <int D>
+__global__ void __launch_bounds__(kPThreads, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+                   const __grid_constant__ CUtensorMap vmap, const __grid_constant__ PrefillParams p)
+{
+    using C = PrefillCfg<D>;
+    constexpr int S = C::kStages;
+    constexpr int QS = C::kQStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+    __shared__ uint64_t q_full[QS], q_empty[QS], k_full[S], k_empty[S], v_full[S], v_empty[S];
+    __shared__ uint64_t s_full[2], s_free[2], p_full[2], o_done[2], mma_done;
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_flag;
+
+    const int warp = threadIdx.x / 32;
+    const WaitCtl wc{&abort_flag, p.status, p.limit};
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        for (int i = 0; i < QS; ++i) {
+            mbar_init(&q_full[i], 1);
+            mbar_init(&q_empty[i], 1);
+        }
+        for (int i = 0; i < S; ++i) {
+            mbar_init(&k_full[i], 1);
+            mbar_init(&k_empty[i], 1);
+            mbar_init(&v_full[i], 1);
+            mbar_init(&v_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&s_full[i], 1);
+            mbar_init(&s_free[i], 128);
+            mbar_init(&p_full[i], 128);
+            mbar_init(&o_done[i], 1);
+        }
+        mbar_init(&mma_done, 1);
+        fence_barrier_init();
+    }
+    if (warp == 9) {
+        tmem_alloc(&tmem_slot, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+    const int n_items = p.U * p.pairs;
+
+    if (warp == 8) {
+        // ------------------------------------------------ TMA producer
+        if (lane_id() == 0) {
+            tma_prefetch_desc(&qmap);
+            tma_prefetch_desc(&kmap);
+            tma_prefetch_desc(&vmap);
+            PRing qr(QS), kr(S), vr(S);
+            uint32_t kcnt[S], vcnt[S], qcnt[QS];
+            for (int i = 0; i < S; ++i) kcnt[i] = vcnt[i] = 0;
+            for (int i = 0; i < QS; ++i) qcnt[i] = 0;
+            for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+                const int u = item / p.pairs;
+                const int r0 = (item % p.pairs) * 2 * kTM;
+                const int T = (unit_keys(p, u) + kTN - 1) / kTN;
+                if (T == 0) continue;
+                mbar_wait(&q_empty[qr.idx], qr.phase ^ 1, wc);
+                if (!aborted(wc)) {
+                    uint8_t* dst = smem + C::kOffQ + qr.idx * C::kQBytes;
+                    mbar_arrive_expect_tx(&q_full[qr.idx], C::kQBytes);
+                    for (int q = 0; q < 2; ++q)
+                        for (int a = 0; a < C::kAtoms; ++a)
+                            tma_load_3d(dst + q * C::kQTileBytes + a * (kTM * 128), &qmap, &q_full[qr.idx], a * 64,
+                                        r0 + q * kTM, u);
+                    ++qcnt[qr.idx];
+                }
+                qr.advance();
+                for (int t = 0; t < T; ++t) {
+                    mbar_wait(&k_empty[kr.idx], kr.phase ^ 1, wc);
+                    if (!aborted(wc)) {
+                        uint8_t* dst = smem + C::kOffK + kr.idx * C::kKVBytes;
+                        mbar_arrive_expect_tx(&k_full[kr.idx], C::kKVBytes);
+                        for (int a = 0; a < C::kAtoms; ++a)
+                            tma_load_3d(dst + a * (kTN * 128), &kmap, &k_full[kr.idx], a * 64, t * kTN, u);
+                        ++kcnt[kr.idx];
+                    }
+                    kr.advance();
+                    mbar_wait(&v_empty[vr.idx], vr.phase ^ 1, wc);
+                    if (!aborted(wc)) {
+                        uint8_t* dst = smem + C::kOffV + vr.idx * C::kKVBytes;
+                        mbar_arrive_expect_tx(&v_full[vr.idx], C::kKVBytes);
+                        for (int a = 0; a < C::kAtoms; ++a)
+                            tma_load_3d(dst + a * (kTN * 128), &vmap, &v_full[vr.idx], a * 64, t * kTN, u);
+                        ++vcnt[vr.idx];
+                    }
+                    vr.advance();
+                }
+            }
+            for (int i = 0; i < S; ++i) {
+                if (kcnt[i]) drain_wait_p(&k_full[i], (kcnt[i] - 1) & 1, p.limit);
+                if (vcnt[i]) drain_wait_p(&v_full[i], (vcnt[i] - 1) & 1, p.limit);
+            }
+            for (int i = 0; i < QS; ++i)
+                if (qcnt[i]) drain_wait_p(&q_full[i], (qcnt[i] - 1) & 1, p.limit);
+        }
+    } else if (warp == 9) {
+        // ------------------------------------------------ MMA issuer (polls, issues whatever is ready)
+        if (lane_id() == 0) {
+            constexpr uint32_t idesc_qk = idesc_bf16_f32(kTM, kTN, false, false);
+            constexpr uint32_t idesc_pv = idesc_bf16_f32(kTM, D, false, true);
+            PRing qr(QS);
+            uint32_t gtile = 0;          // global K/V tile counter (ring position of tile 0 of an item)
+            uint32_t nqk[2] = {0, 0};    // QKs issued per query tile over the kernel's life
+            uint32_t npv[2] = {0, 0};    // PVs issued per query tile
+            for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+                const int u = item / p.pairs;
+                const int T = (unit_keys(p, u) + kTN - 1) / kTN;
+                if (T == 0) continue;
+                mbar_wait(&q_full[qr.idx], qr.phase, wc);
+                tc_fence_after();
+                const uint32_t sQ = smem_u32(smem + C::kOffQ + qr.idx * C::kQBytes);
+                int jq[2] = {0, 0}, jp[2] = {0, 0};
+                long long t_idle = clock64();
+                while ((jp[0] < T || jp[1] < T) && !aborted(wc)) {
+                    bool did = false;
+#pragma unroll
+                    for (int q = 0; q < 2; ++q) {
+                        if (jq[q] < T) {
+                            const uint32_t g = gtile + jq[q];
+                            bool ok = mbar_test(&k_full[g % S], (g / S) & 1);
+                            if (ok && nqk[q] > 0) ok = mbar_test(&s_free[q], (nqk[q] - 1) & 1);
+                            // P aliases S: the previous PV must have been issued and have finished reading P
+                            if (ok && C::kAliasP && nqk[q] > 0)
+                                ok = npv[q] == nqk[q] && mbar_test(&o_done[q], (npv[q] - 1) & 1);
+                            if (ok) {
+                                tc_fence_after();
+                                const uint32_t sK = smem_u32(smem + C::kOffK + (g % S) * C::kKVBytes);
+                                const uint32_t sQq = sQ + q * C::kQTileBytes;
+                                const uint32_t dS = tmem + q * 128;
+#pragma unroll
+                                for (int kk = 0; kk < D / 16; ++kk) {
+                                    const uint64_t da = sdesc_sw128(sQq + (kk >> 2) * (kTM * 128) + (kk & 3) * 32, 16, 1024);
+                                    const uint64_t db = sdesc_sw128(sK + (kk >> 2) * (kTN * 128) + (kk & 3) * 32, 16, 1024);
+                                    mma_ss(dS, da, db, idesc_qk, kk > 0 ? 1u : 0u);
+                                }
+                                mma_commit(&s_full[q]);
+                                ++nqk[q];
+                                ++jq[q];
+                                if (jq[q] <= jq[q ^ 1]) mma_commit(&k_empty[g % S]);   // both tiles read K_g
+                                did = true;
+                            }
+                        }
+                        if (jp[q] < jq[q]) {
+                            const uint32_t g = gtile + jp[q];
+                            bool ok = mbar_test(&p_full[q], npv[q] & 1);
+                            if (ok) ok = mbar_test(&v_full[g % S], (g / S) & 1);
+                            if (ok) {
+                                tc_fence_after();
+                                const uint32_t sV = smem_u32(smem + C::kOffV + (g % S) * C::kKVBytes);
+                                const uint32_t dO = tmem + C::kColO + q * D;
+                                const uint32_t aP = tmem + C::kColP + q * C::kPStride;
+#pragma unroll
+                                for (int ks = 0; ks < kTN / 16; ++ks) {
+                                    const uint64_t db = sdesc_sw128(sV + ks * 2048, kTN * 128, 1024);
+                                    mma_ts(dO, aP + ks * 8, db, idesc_pv, (jp[q] > 0 || ks > 0) ? 1u : 0u);
+                                }
+                                mma_commit(&o_done[q]);
+                                ++npv[q];
+                                ++jp[q];
+                                if (jp[q] <= jp[q ^ 1]) mma_commit(&v_empty[g % S]);   // both tiles read V_g
+                                did = true;
+                            }
+                        }
+                    }
+                    if (did) {
+                        t_idle = clock64();
+                    } else if (clock64() - t_idle > p.limit) {
+                        abort_flag = 1;
+                        atomicExch(p.status, kDevTimeout);
+                    }
+                }
+                if (!aborted(wc)) mma_commit(&q_empty[qr.idx]);
+                qr.advance();
+                gtile += T;
+            }
+            mma_commit(&mma_done);
+            drain_wait_p(&mma_done, 0, p.limit);
+        }
+    } else {
+        // ------------------------------------------------ softmax / rescale / epilogue, one row per thread
+        const int q = warp / 4;
+        const int wl = warp % 4;
+        const uint32_t lane_base = static_cast<uint32_t>(wl * 32) << 16;
+        const int row_in_tile = wl * 32 + static_cast<int>(lane_id());
+        const uint32_t tS = tmem + lane_base + q * 128;
+        const uint32_t tP = tmem + lane_base + C::kColP + q * C::kPStride;
+        const uint32_t tO = tmem + lane_base + C::kColO + q * D;
+        uint32_t gt = 0;   // tiles processed by this warpgroup over the kernel's life (= K/V ring position)
+        for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+            const int u = item / p.pairs;
+            const int row = (item % p.pairs) * 2 * kTM + q * kTM + row_in_tile;
+            const int n = unit_keys(p, u);
+            const int T = (n + kTN - 1) / kTN;
+            float m_run = -INFINITY, l = 0.f;
+            for (int j = 0; j < T; ++j, ++gt) {
+                mbar_wait(&s_full[q], gt & 1, wc);
+                tc_fence_after();
+                float s[kTN];
+                uint32_t* su = reinterpret_cast<uint32_t*>(s);
+#pragma unroll
+                for (int c4 = 0; c4 < kTN / 32; ++c4) tmem_ld32p(tS + c4 * 32, su + c4 * 32);
+                tmem_ld_wait();
+                tc_fence_before();
+                mbar_arrive(&s_free[q]);
+                if ((j + 1) * kTN > n) {
+#pragma unroll
+                    for (int i = 0; i < kTN; ++i)
+                        if (j * kTN + i >= n) s[i] = -INFINITY;
+                }
+                float mx[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) mx[k] = s[k];
+#pragma unroll
+                for (int i = 8; i < kTN; ++i) mx[i & 7] = fmaxf(mx[i & 7], s[i]);
+                const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                       fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * p.c;
+                const bool rescale = mt > m_run + kRescaleLog2;
+                float alpha = 1.f;
+                if (rescale) {
+                    alpha = ex2_approx(m_run - mt);
+                    m_run = mt;
+                }
+                const float neg_m = -m_run;
+                uint32_t pk[kTN / 2];
+                float ls[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) ls[k] = 0.f;
+#pragma unroll
+                for (int i = 0; i < kTN; i += 2) {
+                    const float p0 = ex2_approx(fmaf(s[i], p.c, neg_m));
+                    const float p1 = ex2_approx(fmaf(s[i + 1], p.c, neg_m));
+                    ls[(i >> 1) & 7] += p0 + p1;
+                    pk[i >> 1] = pack_bf16x2(p0, p1);
+                }
+                l = fmaf(l, alpha, ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7])));
+                // PV of the previous tile must be done: its P buffer is reused and O must be stable.
+                if (j > 0) mbar_wait(&o_done[q], (gt - 1) & 1, wc);
+                tc_fence_after();
+                // tcgen05.ld/st are warp-collective (.sync.aligned): rescale if any lane of the warp
+                // needs it (alpha = 1 for the others), never under a per-lane branch.
+                if (__any_sync(0xffffffffu, rescale) && j > 0) {
+#pragma unroll
+                    for (int c4 = 0; c4 < D / 32; ++c4) {
+                        uint32_t o[32];
+                        tmem_ld32p(tO + c4 * 32, o);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                        tmem_st32(tO + c4 * 32, o);
+                    }
+                }
+                // Keys at or beyond n of a ragged unit may be anything in memory (NaN in padding) and
+                // P = 0 does not cancel NaN in the MMA: zero those V rows of a partial tile.  Both
+                // warpgroups write the same zeros; each makes them visible before its own p_full.
+                if (p.seqlens && (j + 1) * kTN > n) {
+                    mbar_wait(&v_full[gt % S], (gt / S) & 1, wc);
+                    for (int r = n - j * kTN + row_in_tile; r < kTN; r += kTM) {
+                        uint8_t* rowp = smem + C::kOffV + (gt % S) * C::kKVBytes + r * 128;
+#pragma unroll
+                        for (int a = 0; a < C::kAtoms; ++a)
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                reinterpret_cast<uint4*>(rowp + a * (kTN * 128))[i] = make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
+                }
+                __syncwarp();
+                tmem_st32(tP, pk);
+                tmem_st32(tP + 32, pk + 32);
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(&p_full[q]);
+            }
+            // ---- epilogue: O / l, LSE
+            if (T > 0) {
+                mbar_wait(&o_done[q], (gt - 1) & 1, wc);
+                tc_fence_after();
+            }
+            // The TMEM loads below are warp-collective: every lane executes them; only the stores
+            // are predicated on the row existing.
+            const bool store = row < p.R && !aborted(wc);
+            const size_t orow = static_cast<size_t>(u) * p.R + (row < p.R ? row : 0);
+            const float inv_l = T > 0 ? 1.f / l : 0.f;
+            float amax = 0.f;
+            __syncwarp();
+#pragma unroll
+            for (int c4 = 0; c4 < D / 32; ++c4) {
+                uint32_t o[32];
+                if (T > 0) {
+                    tmem_ld32p(tO + c4 * 32, o);
+                    tmem_ld_wait();
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = 0u;
+                }
+                float v[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(o[i]) * inv_l;
+                if (store) {
+                    if (p.o_stage) {
+                        float4* dst = reinterpret_cast<float4*>(p.o_stage + orow * D + c4 * 32);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+                    }
+                    if (p.out) {
+                        if (p.out_f32) {
+                            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow * D + c4 * 32);
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                        } else {
+                            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + orow * D + c4 * 32);
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                dst[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                                                    pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+                        }
+                    }
+                }
+            }
+            if (store && p.lse) p.lse[orow] = T > 0 ? (m_run + __log2f(l)) * kLn2P : -INFINITY;
+            if (store && p.amax_bits && amax > 0.f) atomicMax(p.amax_bits, __float_as_uint(amax));
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 9) tmem_dealloc(tmem, 512);
+}
+
+// ---- host side ------------------------------------------------------------------------------------
+template <int D>
+int run_prefill(const AttnArgs& a, void* ws, cudaStream_t st)
+{
+    using C = PrefillCfg<D>;
+    const int nsm = num_sms();
+    if (nsm <= 0) return set_error(FMHA_ERR_CUDA, "cannot query the SM count");
+    const int U = a.B * a.Hkv;
+    const int R = (a.Hq / a.Hkv) * a.Sq;
+    CUtensorMap qmap, kmap, vmap;
+    {
+        const uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(R), static_cast<uint64_t>(U)};
+        const uint64_t strides[2] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(R) * D * 2};
+        const uint32_t box[3] = {64, static_cast<uint32_t>(kTM), 1};
+        int rc = make_tmap_bf16(&qmap, a.q, 3, dims, strides, box);
+        if (rc) return rc;
+    }
+    {
+        const uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(a.Skv), static_cast<uint64_t>(U)};
+        const uint64_t strides[2] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(a.Skv) * D * 2};
+        const uint32_t box[3] = {64, static_cast<uint32_t>(kTN), 1};
+        int rc = make_tmap_bf16(&kmap, a.k, 3, dims, strides, box);
+        if (rc) return rc;
+        rc = make_tmap_bf16(&vmap, a.v, 3, dims, strides, box);
+        if (rc) return rc;
+    }
+    PrefillParams p{};
+    p.U = U;
+    p.Hkv = a.Hkv;
+    p.R = R;
+    p.Skv = a.Skv;
+    p.pairs = (R + 2 * kTM - 1) / (2 * kTM);
+    p.c = a.scale * kLog2eP;
+    p.seqlens = a.seqlens;
+    const bool nvfp4 = a.out_kind == FMHA_OUT_NVFP4;
+    p.out = nvfp4 ? nullptr : a.out;
+    p.out_f32 = a.out_kind == FMHA_OUT_F32 ? 1 : 0;
+    p.lse = a.lse;
+    p.o_stage = nvfp4 ? (a.out_f32 ? a.out_f32 : static_cast<float*>(ws)) : nullptr;
+    p.amax_bits = nvfp4 ? reinterpret_cast<unsigned*>(a.amax_slot) : nullptr;
+    p.status = device_status_ptr();
+    p.limit = wait_limit();
+    const long long items = static_cast<long long>(U) * p.pairs;
+    const int grid = static_cast<int>(items < nsm ? items : nsm);
+    FMHA_CHECK_CUDA(cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes));
+    if (grid > 0) {
+        timing_mark_begin(st);
+        prefill_kernel<D><<<grid, kPThreads, C::kSmemBytes, st>>>(qmap, kmap, vmap, p);
+        timing_mark_end(st);
+        FMHA_CHECK_LAUNCH("prefill_kernel");
+        count_launch();
+    }
+    return FMHA_OK;
+}
+
+}  // namespace
+
+size_t prefill_workspace_bytes(const AttnArgs& a)
+{
+    // NVFP4 output without a caller-provided FP32 buffer: FP32 staging of O at offset 0
+    if (a.out_kind == FMHA_OUT_NVFP4 && !a.out_f32)
+        return (static_cast<size_t>(a.B) * a.Hq * a.Sq * a.D * 4 + 255) & ~size_t(255);
+    return 0;
+}
+
+int launch_prefill(const AttnArgs& a, void* ws, size_t ws_bytes, cudaStream_t st)
+{
+    if (ws_bytes < prefill_workspace_bytes(a)) return set_error(FMHA_ERR_WORKSPACE, "row-tile path: workspace too small");
+    switch (a.D) {
+        case 64: return run_prefill<64>(a, ws, st);
+        case 128: return run_prefill<128>(a, ws, st);
+        default: return set_error(FMHA_ERR_UNSUPPORTED, "row-tile path: D must be 64 or 128 (D = 512 not built yet)");
+    }
+}
+
 }  // namespace fmha
