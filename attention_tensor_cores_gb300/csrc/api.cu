@@ -215,7 +215,8 @@ static bool use_decode_path(int Hq, int Hkv, int Sq) { return static_cast<long l
 // tile prefix, the split partials and (NVFP4 without out_f32) the FP32 staging of O.
 static size_t workspace_bytes(const AttnArgs& a, int num_splits)
 {
-    size_t w = use_decode_path(a.Hq, a.Hkv, a.Sq) ? decode_workspace_bytes(a, num_splits) : prefill_workspace_bytes(a);
+    size_t w = a.D == 512 ? wide_workspace_bytes(a)
+               : use_decode_path(a.Hq, a.Hkv, a.Sq) ? decode_workspace_bytes(a, num_splits) : prefill_workspace_bytes(a);
     w = align256(w);
     if (a.out_kind == FMHA_OUT_NVFP4) w += 256;
     return w;
@@ -303,7 +304,9 @@ int fmha_fwd_ex(const void* q, const void* k, const void* v, void* out, float* l
         a.amax_slot = reinterpret_cast<float*>(amax);
         FMHA_CHECK_CUDA(cudaMemsetAsync(amax, 0, sizeof(unsigned), st));
     }
-    if (use_decode_path(Hq, Hkv, Sq))
+    if (D == 512)
+        rc = launch_wide(a, ws, path_bytes, st);
+    else if (use_decode_path(Hq, Hkv, Sq))
         rc = launch_decode(a, num_splits, ws, path_bytes, st);
     else
         rc = launch_prefill(a, ws, path_bytes, st);

@@ -68,6 +68,10 @@ int launch_decode(const AttnArgs& a, int num_splits, void* ws, size_t ws_bytes, 
 size_t prefill_workspace_bytes(const AttnArgs& a);
 int launch_prefill(const AttnArgs& a, void* ws, size_t ws_bytes, cudaStream_t st);
 
+// Wide-head path (D = 512): CTA pairs split the value columns, stream-K over 32-key tiles.
+size_t wide_workspace_bytes(const AttnArgs& a);
+int launch_wide(const AttnArgs& a, void* ws, size_t ws_bytes, cudaStream_t st);
+
 // NVFP4
 int launch_nvfp4(const float* x, uint8_t* codes, uint8_t* scales, float* tensor_scale, unsigned* amax_bits,
                  int64_t n, bool amax_ready, cudaStream_t st);

@@ -1,0 +1,615 @@
+// Wide-head attention (D = 512 for K and V), e.g. 128 query heads sharing one key/value head.
+//
+// Same computation as the other paths ("NVFP4-1.1_RAW_CUDA_CPP_APPROACH.md", nvfp4-megamoe-kernel,
+// kernel plan: TMA loads, tcgen05 QK and PV with Tensor Memory accumulators, in-kernel softmax with O
+// rescale, multi-KV-tile, and the pages' goal of head dims up to 512).  What D = 512 changes on
+// GB300: an FP32 O tile of 128 rows x 512 columns is all 512 Tensor Memory columns, and the 128 x 512
+// BF16 Q tile alone is 128 KB of shared memory.  The design:
+//
+//  * CTA pairs split the value dimension: CTA h of a pair accumulates O[:, 256h : 256h + 256] (256
+//    TMEM columns).  Both CTAs of the pair compute the full S = Q K^T (M = 128 query rows, N = 32
+//    keys, K = 512), so each holds all of Q (128 KB) and each 32-key K tile (32 KB), plus its half of
+//    the V tile (16 KB); two K/V stages fit in the remaining shared memory.  The pair's K tiles are
+//    the same addresses, read once from HBM and once more from L2.
+//  * Stream-K over keys: the 32-key tiles of all units (b, kv-head, 128-row block) are laid end to
+//    end and pair p of P takes [p*T/P, (p+1)*T/P); a run that covers a whole unit writes O and LSE,
+//    otherwise a normalised partial goes to slot unit + p and the combine kernel merges them.
+//  * Roles: warps 0-3 softmax (one query row per thread, lazy rescale as in the row-tile kernel),
+//    warp 4 TMA producer, warp 5 MMA issuer.  S and P are double-buffered in TMEM so the QK of the
+//    next tile overlaps the softmax of this one.  All waits are bounded.
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace fmha {
+namespace {
+
+constexpr int kWD = 512;            // head dim of Q/K/V
+constexpr int kWHalf = 256;         // value columns per CTA
+constexpr int kWRows = 128;         // query rows per unit (MMA M)
+constexpr int kWKeys = 32;          // keys per tile (QK N, PV K)
+constexpr int kWStages = 2;
+constexpr int kWThreads = 192;
+constexpr float kLog2eW = 1.4426950408889634f;
+constexpr float kLn2W = 0.6931471805599453f;
+constexpr float kRescaleW = 8.0f;
+
+constexpr int kWQBytes = 8 * kWRows * 128;          // 8 atoms of 128 rows x 128 B = 128 KB
+constexpr int kWKBytes = 8 * kWKeys * 128;          // 8 atoms of 32 rows x 128 B = 32 KB
+constexpr int kWVBytes = 4 * kWKeys * 128;          // 4 atoms (this CTA's 256 columns) = 16 KB
+constexpr int kWOffQ = 0;
+constexpr int kWOffK = kWOffQ + kWQBytes;
+constexpr int kWOffV = kWOffK + kWStages * kWKBytes;
+constexpr int kWSmem = kWOffV + kWStages * kWVBytes + 1024;
+// TMEM columns: S[2] at 0/32, P[2] at 64/80 (16 columns = 32 BF16 keys), O half at 256..511.
+constexpr uint32_t kWColS = 0, kWColP = 64, kWColO = 256;
+
+struct WideParams {
+    int U;          // units = B * Hkv * row_tiles
+    int row_tiles;  // ceil(R / 128)
+    int Hkv;
+    int R;          // query rows per (b, kv-head) = (Hq / Hkv) * Sq
+    int Skv;
+    float c;
+    const int32_t* seqlens;
+    const int32_t* prefix;   // [U+1] tile prefix (ragged), else NULL
+    int tiles_uniform;
+    void* out;
+    int out_f32;
+    float* lse;
+    float* o_stage;
+    unsigned* amax_bits;
+    float* part_o;      // [slots][128][512]
+    float* part_lse;    // [slots][128]
+    int* status;
+    long long limit;
+};
+
+struct WItem {
+    int u, t0, t1, n;
+    bool whole;
+    int slot;
+};
+
+// Unit u -> (b*Hkv + kvh, 128-row block).
+__device__ __forceinline__ int wunit_head(const WideParams& p, int u) { return u / p.row_tiles; }
+__device__ __forceinline__ int wunit_keys(const WideParams& p, int u)
+{
+    return p.seqlens ? p.seqlens[wunit_head(p, u) / p.Hkv] : p.Skv;
+}
+__device__ __forceinline__ int wunit_tiles(const WideParams& p, int u)
+{
+    if (p.prefix) return p.prefix[u + 1] - p.prefix[u];
+    return (wunit_keys(p, u) + kWKeys - 1) / kWKeys;
+}
+__device__ __forceinline__ long long wunit_start(const WideParams& p, int u)
+{
+    return p.prefix ? static_cast<long long>(p.prefix[u]) : static_cast<long long>(u) * p.tiles_uniform;
+}
+
+struct WSched {
+    const WideParams* p;
+    long long g, g1;
+    int pair;
+    __device__ void init(const WideParams* pp, int pr, int npairs)
+    {
+        p = pp;
+        pair = pr;
+        const long long T = p->prefix ? p->prefix[p->U] : static_cast<long long>(p->U) * p->tiles_uniform;
+        g = (static_cast<long long>(pr) * T) / npairs;
+        g1 = (static_cast<long long>(pr + 1) * T) / npairs;
+    }
+    __device__ bool next(WItem& it)
+    {
+        if (g >= g1) return false;
+        int uu;
+        if (p->prefix) {
+            int lo = 0, hi = p->U - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (p->prefix[mid] <= g) lo = mid; else hi = mid - 1;
+            }
+            uu = lo;
+        } else {
+            uu = static_cast<int>(g / p->tiles_uniform);
+        }
+        const long long s = wunit_start(*p, uu);
+        const int nt = wunit_tiles(*p, uu);
+        it.u = uu;
+        it.t0 = static_cast<int>(g - s);
+        it.t1 = static_cast<int>(min(static_cast<long long>(nt), g1 - s));
+        it.n = wunit_keys(*p, uu);
+        it.whole = (it.t0 == 0 && it.t1 == nt);
+        it.slot = uu + pair;
+        g = s + it.t1;
+        return true;
+    }
+};
+
+__device__ __forceinline__ void wdrain(uint64_t* bar, uint32_t parity, long long limit)
+{
+    const uint32_t a = smem_u32(bar);
+    const long long t0 = clock64();
+    while (!mbar_try_wait(a, parity)) {
+        if (clock64() - t0 > limit) return;
+    }
+}
+
+struct WRing {
+    uint32_t idx = 0, phase = 0;
+    int n;
+    __device__ explicit WRing(int stages) : n(stages) {}
+    __device__ void advance()
+    {
+        if (++idx == static_cast<uint32_t>(n)) {
+            idx = 0;
+            phase ^= 1;
+        }
+    }
+};
+
+__global__ void __launch_bounds__(kWThreads, 1)
+    wide_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+                const __grid_constant__ CUtensorMap vmap, const __grid_constant__ WideParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ uint64_t q_full, q_empty, k_full[kWStages], k_empty[kWStages], v_full[kWStages], v_empty[kWStages];
+    __shared__ uint64_t s_full[2], s_empty[2], p_full, o_done, mma_done;
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_flag;
+
+    const int warp = threadIdx.x / 32;
+    const int half = blockIdx.x & 1;
+    const WaitCtl wc{&abort_flag, p.status, p.limit};
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        mbar_init(&q_full, 1);
+        mbar_init(&q_empty, 1);
+        for (int i = 0; i < kWStages; ++i) {
+            mbar_init(&k_full[i], 1);
+            mbar_init(&k_empty[i], 1);
+            mbar_init(&v_full[i], 1);
+            mbar_init(&v_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&s_full[i], 1);
+            mbar_init(&s_empty[i], 128);
+        }
+        mbar_init(&p_full, 128);
+        mbar_init(&o_done, 1);
+        mbar_init(&mma_done, 1);
+        fence_barrier_init();
+    }
+    if (warp == 5) {
+        tmem_alloc(&tmem_slot, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+    WSched sched;
+    sched.init(&p, blockIdx.x >> 1, gridDim.x >> 1);
+    WItem it;
+
+    if (warp == 4) {
+        // ------------------------------------------------ TMA producer
+        if (lane_id() == 0) {
+            tma_prefetch_desc(&qmap);
+            tma_prefetch_desc(&kmap);
+            tma_prefetch_desc(&vmap);
+            WRing kr(kWStages), vr(kWStages);
+            uint32_t qn = 0, kcnt[kWStages] = {0, 0}, vcnt[kWStages] = {0, 0};
+            while (sched.next(it)) {
+                const int hu = wunit_head(p, it.u);
+                const int rt = it.u % p.row_tiles;
+                mbar_wait(&q_empty, (qn & 1) ^ 1, wc);
+                if (!aborted(wc)) {
+                    mbar_arrive_expect_tx(&q_full, kWQBytes);
+                    for (int a = 0; a < 8; ++a)
+                        tma_load_3d(smem + kWOffQ + a * (kWRows * 128), &qmap, &q_full, a * 64, rt * kWRows, hu);
+                }
+                ++qn;
+                for (int t = it.t0; t < it.t1; ++t) {
+                    mbar_wait(&k_empty[kr.idx], kr.phase ^ 1, wc);
+                    if (!aborted(wc)) {
+                        uint8_t* dst = smem + kWOffK + kr.idx * kWKBytes;
+                        mbar_arrive_expect_tx(&k_full[kr.idx], kWKBytes);
+                        for (int a = 0; a < 8; ++a)
+                            tma_load_3d(dst + a * (kWKeys * 128), &kmap, &k_full[kr.idx], a * 64, t * kWKeys, hu);
+                        ++kcnt[kr.idx];
+                    }
+                    kr.advance();
+                    mbar_wait(&v_empty[vr.idx], vr.phase ^ 1, wc);
+                    if (!aborted(wc)) {
+                        uint8_t* dst = smem + kWOffV + vr.idx * kWVBytes;
+                        mbar_arrive_expect_tx(&v_full[vr.idx], kWVBytes);
+                        for (int a = 0; a < 4; ++a)
+                            tma_load_3d(dst + a * (kWKeys * 128), &vmap, &v_full[vr.idx], half * kWHalf + a * 64,
+                                        t * kWKeys, hu);
+                        ++vcnt[vr.idx];
+                    }
+                    vr.advance();
+                }
+            }
+            for (int i = 0; i < kWStages; ++i) {
+                if (kcnt[i]) wdrain(&k_full[i], (kcnt[i] - 1) & 1, p.limit);
+                if (vcnt[i]) wdrain(&v_full[i], (vcnt[i] - 1) & 1, p.limit);
+            }
+            if (qn) wdrain(&q_full, (qn - 1) & 1, p.limit);
+        }
+    } else if (warp == 5) {
+        // ------------------------------------------------ MMA issuer
+        if (lane_id() == 0) {
+            constexpr uint32_t idesc_qk = idesc_bf16_f32(kWRows, kWKeys, false, false);
+            constexpr uint32_t idesc_pv = idesc_bf16_f32(kWRows, kWHalf, false, true);
+            WRing kr(kWStages), vr(kWStages), sr(2);
+            uint32_t qn = 0, np = 0;
+            const uint32_t sQ = smem_u32(smem + kWOffQ);
+            while (sched.next(it)) {
+                mbar_wait(&q_full, qn & 1, wc);
+                ++qn;
+                auto pv = [&](bool first) {
+                    mbar_wait(&p_full, np & 1, wc);
+                    mbar_wait(&v_full[vr.idx], vr.phase, wc);
+                    tc_fence_after();
+                    if (!aborted(wc)) {
+                        const uint32_t sV = smem_u32(smem + kWOffV + vr.idx * kWVBytes);
+#pragma unroll
+                        for (int ks = 0; ks < kWKeys / 16; ++ks) {
+                            const uint64_t db = sdesc_sw128(sV + ks * 2048, kWKeys * 128, 1024);
+                            mma_ts(tmem + kWColO, tmem + kWColP + ks * 8, db, idesc_pv, (!first || ks > 0) ? 1u : 0u);
+                        }
+                        mma_commit(&o_done);
+                        mma_commit(&v_empty[vr.idx]);
+                    }
+                    ++np;
+                    vr.advance();
+                };
+                for (int t = it.t0; t < it.t1; ++t) {
+                    mbar_wait(&k_full[kr.idx], kr.phase, wc);
+                    mbar_wait(&s_empty[sr.idx], sr.phase ^ 1, wc);
+                    tc_fence_after();
+                    if (!aborted(wc)) {
+                        const uint32_t sK = smem_u32(smem + kWOffK + kr.idx * kWKBytes);
+#pragma unroll
+                        for (int kk = 0; kk < kWD / 16; ++kk) {
+                            const uint64_t da = sdesc_sw128(sQ + (kk >> 2) * (kWRows * 128) + (kk & 3) * 32, 16, 1024);
+                            const uint64_t db = sdesc_sw128(sK + (kk >> 2) * (kWKeys * 128) + (kk & 3) * 32, 16, 1024);
+                            mma_ss(tmem + kWColS + sr.idx * kWKeys, da, db, idesc_qk, kk > 0 ? 1u : 0u);
+                        }
+                        mma_commit(&s_full[sr.idx]);
+                        mma_commit(&k_empty[kr.idx]);
+                    }
+                    kr.advance();
+                    sr.advance();
+                    if (t > it.t0) pv(t - 1 == it.t0);
+                }
+                pv(it.t1 - 1 == it.t0);
+                if (!aborted(wc)) mma_commit(&q_empty);
+            }
+            mma_commit(&mma_done);
+            wdrain(&mma_done, 0, p.limit);
+        }
+    } else {
+        // ------------------------------------------------ softmax / epilogue, one query row per thread
+        const int row_in_tile = warp * 32 + static_cast<int>(lane_id());
+        const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+        WRing sr(2), vr(kWStages);
+        uint32_t g = 0;   // P tiles produced = PVs issued for this CTA
+        while (sched.next(it)) {
+            const int hu = wunit_head(p, it.u);
+            const int row = (it.u % p.row_tiles) * kWRows + row_in_tile;
+            float m_run = -INFINITY, l = 0.f;
+            for (int t = it.t0; t < it.t1; ++t, ++g) {
+                mbar_wait(&s_full[sr.idx], sr.phase, wc);
+                tc_fence_after();
+                float s[kWKeys];
+                tmem_ld32p(tmem + lane_base + kWColS + sr.idx * kWKeys, reinterpret_cast<uint32_t*>(s));
+                tmem_ld_wait();
+                tc_fence_before();
+                mbar_arrive(&s_empty[sr.idx]);
+                sr.advance();
+                const bool partial = (t + 1) * kWKeys > it.n;
+                if (partial) {
+#pragma unroll
+                    for (int i = 0; i < kWKeys; ++i)
+                        if (t * kWKeys + i >= it.n) s[i] = -INFINITY;
+                }
+                float mx = s[0];
+#pragma unroll
+                for (int i = 1; i < kWKeys; ++i) mx = fmaxf(mx, s[i]);
+                const float mt = mx * p.c;
+                const bool rescale = mt > m_run + kRescaleW;
+                float alpha = 1.f;
+                if (rescale) {
+                    alpha = ex2_approx(m_run - mt);
+                    m_run = mt;
+                }
+                uint32_t pk[16];
+                float sum = 0.f;
+#pragma unroll
+                for (int i = 0; i < kWKeys; i += 2) {
+                    const float p0 = ex2_approx(fmaf(s[i], p.c, -m_run));
+                    const float p1 = ex2_approx(fmaf(s[i + 1], p.c, -m_run));
+                    sum += p0 + p1;
+                    pk[i >> 1] = pack_bf16x2(p0, p1);
+                }
+                l = fmaf(l, alpha, sum);
+                // the previous PV must be done: the P buffer is reused and O must be stable
+                if (t > it.t0) mbar_wait(&o_done, (g - 1) & 1, wc);
+                tc_fence_after();
+                // ragged keys: V rows at or beyond n may hold NaN; P = 0 does not cancel it
+                if (p.seqlens && partial) {
+                    mbar_wait(&v_full[vr.idx], vr.phase, wc);
+                    const int r = row_in_tile;
+                    if (r < kWKeys && t * kWKeys + r >= it.n) {
+                        uint8_t* rowp = smem + kWOffV + vr.idx * kWVBytes + r * 128;
+                        for (int a = 0; a < 4; ++a)
+                            for (int i = 0; i < 8; ++i)
+                                reinterpret_cast<uint4*>(rowp + a * (kWKeys * 128))[i] = make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
+                }
+                vr.advance();
+                __syncwarp();
+                if (__any_sync(0xffffffffu, rescale) && t > it.t0) {
+                    for (int c4 = 0; c4 < kWHalf / 32; ++c4) {
+                        uint32_t o[32];
+                        tmem_ld32p(tmem + lane_base + kWColO + c4 * 32, o);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                        tmem_st32(tmem + lane_base + kWColO + c4 * 32, o);
+                    }
+                }
+                tmem_st16(tmem + lane_base + kWColP, pk);
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(&p_full);
+            }
+            // ---- epilogue
+            mbar_wait(&o_done, (g - 1) & 1, wc);
+            tc_fence_after();
+            const bool store = row < p.R && !aborted(wc);
+            const int rr = row < p.R ? row : 0;
+            const float inv_l = 1.f / l;
+            const float lse_v = (m_run + __log2f(l)) * kLn2W;
+            float amax = 0.f;
+            __syncwarp();
+            for (int c4 = 0; c4 < kWHalf / 32; ++c4) {
+                uint32_t o[32];
+                tmem_ld32p(tmem + lane_base + kWColO + c4 * 32, o);
+                tmem_ld_wait();
+                if (store) {
+                    const int col = half * kWHalf + c4 * 32;
+                    float v[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(o[i]) * inv_l;
+                    if (it.whole) {
+                        const size_t orow = static_cast<size_t>(hu) * p.R + rr;
+                        if (p.o_stage) {
+                            float4* dst = reinterpret_cast<float4*>(p.o_stage + orow * kWD + col);
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+                        }
+                        if (p.out) {
+                            if (p.out_f32) {
+                                float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow * kWD + col);
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                            } else {
+                                uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + orow * kWD + col);
+#pragma unroll
+                                for (int i = 0; i < 4; ++i)
+                                    dst[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                                                        pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+                            }
+                        }
+                    } else {
+                        float4* dst = reinterpret_cast<float4*>(p.part_o + (static_cast<size_t>(it.slot) * kWRows + row_in_tile) * kWD + col);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                    }
+                }
+            }
+            if (store && half == 0) {
+                if (it.whole) {
+                    if (p.lse) p.lse[static_cast<size_t>(hu) * p.R + rr] = lse_v;
+                } else {
+                    p.part_lse[static_cast<size_t>(it.slot) * kWRows + row_in_tile] = lse_v;
+                }
+            }
+            if (store && it.whole && p.amax_bits && amax > 0.f) atomicMax(p.amax_bits, __float_as_uint(amax));
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) tmem_dealloc(tmem, 512);
+}
+
+// Exclusive prefix of per-unit 32-key tile counts (ragged keys), one block.
+__global__ void __launch_bounds__(1024) wide_prefix_kernel(const int32_t* seqlens, int Hkv, int row_tiles, int U,
+                                                          int32_t* prefix)
+{
+    __shared__ int part[1024];
+    const int per = (U + 1023) / 1024;
+    const int b0 = threadIdx.x * per;
+    auto tiles = [&](int u) { return (seqlens[(u / row_tiles) / Hkv] + kWKeys - 1) / kWKeys; };
+    int s = 0;
+    for (int u = b0; u < min(U, b0 + per); ++u) s += tiles(u);
+    part[threadIdx.x] = s;
+    __syncthreads();
+    for (int off = 1; off < 1024; off <<= 1) {
+        const int v = threadIdx.x >= off ? part[threadIdx.x - off] : 0;
+        __syncthreads();
+        part[threadIdx.x] += v;
+        __syncthreads();
+    }
+    int run = threadIdx.x ? part[threadIdx.x - 1] : 0;
+    for (int u = b0; u < min(U, b0 + per); ++u) {
+        prefix[u] = run;
+        run += tiles(u);
+    }
+    if (threadIdx.x == 1023) prefix[U] = part[1023];
+}
+
+// Merges split units (lse = log sum exp lse_i, O = sum exp(lse_i - lse) O_i) and writes units
+// without keys (O = 0, LSE = -inf).  One block of 256 threads (2 columns each) per query row.
+__global__ void __launch_bounds__(256) wide_combine_kernel(const __grid_constant__ WideParams p, int npairs)
+{
+    const int u = blockIdx.x / kWRows;
+    const int r = blockIdx.x % kWRows;
+    const int hu = wunit_head(p, u);
+    const int row = (u % p.row_tiles) * kWRows + r;
+    if (row >= p.R) return;
+    const int tiles = wunit_tiles(p, u);
+    const long long Tu = wunit_start(p, u);
+    const long long T = p.prefix ? p.prefix[p.U] : static_cast<long long>(p.U) * p.tiles_uniform;
+    float o[2] = {0.f, 0.f};
+    float lse_v = -INFINITY;
+    if (tiles > 0) {
+        const long long P = npairs;
+        const int c0 = static_cast<int>(min((((Tu + 1) * P) - 1) / T, P - 1));
+        const int c1 = static_cast<int>(min((((Tu + tiles) * P) - 1) / T, P - 1));
+        if (c0 == c1) return;   // one pair held the whole unit and wrote it
+        auto has_work = [&](int c) { return (c * T) / P != ((c + 1) * T) / P; };
+        float mx = -INFINITY;
+        for (int c = c0; c <= c1; ++c)
+            if (has_work(c)) mx = fmaxf(mx, p.part_lse[static_cast<size_t>(u + c) * kWRows + r]);
+        float sum = 0.f;
+        for (int c = c0; c <= c1; ++c)
+            if (has_work(c)) sum += __expf(p.part_lse[static_cast<size_t>(u + c) * kWRows + r] - mx);
+        lse_v = mx + __logf(sum);
+        for (int c = c0; c <= c1; ++c) {
+            if (!has_work(c)) continue;
+            const size_t sl = static_cast<size_t>(u + c) * kWRows + r;
+            const float wgt = __expf(p.part_lse[sl] - lse_v);
+            const float2 v = reinterpret_cast<const float2*>(p.part_o + sl * kWD)[threadIdx.x];
+            o[0] = fmaf(wgt, v.x, o[0]);
+            o[1] = fmaf(wgt, v.y, o[1]);
+        }
+    }
+    const size_t orow = static_cast<size_t>(hu) * p.R + row;
+    const int col = 2 * threadIdx.x;
+    if (p.o_stage) reinterpret_cast<float2*>(p.o_stage + orow * kWD)[threadIdx.x] = make_float2(o[0], o[1]);
+    if (p.out) {
+        if (p.out_f32)
+            reinterpret_cast<float2*>(static_cast<float*>(p.out) + orow * kWD)[threadIdx.x] = make_float2(o[0], o[1]);
+        else
+            reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(p.out) + orow * kWD)[threadIdx.x] = pack_bf16x2(o[0], o[1]);
+    }
+    (void)col;
+    if (threadIdx.x == 0 && p.lse) p.lse[orow] = lse_v;
+    if (p.amax_bits) {
+        float m = fmaxf(fabsf(o[0]), fabsf(o[1]));
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+        if ((threadIdx.x & 31) == 0 && m > 0.f) atomicMax(p.amax_bits, __float_as_uint(m));
+    }
+}
+
+struct WideWs {
+    size_t prefix_off, lse_off, o_off, stage_off, total;
+};
+
+WideWs wide_ws_layout(const AttnArgs& a, int npairs)
+{
+    auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
+    const int R = (a.Hq / a.Hkv) * a.Sq;
+    const size_t U = static_cast<size_t>(a.B) * a.Hkv * ((R + kWRows - 1) / kWRows);
+    const size_t slots = U + npairs;
+    WideWs w{};
+    size_t off = 0;
+    w.prefix_off = off;
+    off += a.seqlens ? al((U + 1) * 4) : 0;
+    w.lse_off = off;
+    off += al(slots * kWRows * 4);
+    w.o_off = off;
+    off += al(slots * kWRows * kWD * 4);
+    w.stage_off = off;
+    const bool stage = (a.out_kind == FMHA_OUT_NVFP4) && !a.out_f32;
+    off += stage ? al(static_cast<size_t>(a.B) * a.Hq * a.Sq * kWD * 4) : 0;
+    w.total = off;
+    return w;
+}
+
+}  // namespace
+
+size_t wide_workspace_bytes(const AttnArgs& a)
+{
+    const int nsm = num_sms() > 0 ? num_sms() : 256;
+    return wide_ws_layout(a, nsm / 2).total;
+}
+
+int launch_wide(const AttnArgs& a, void* ws, size_t ws_bytes, cudaStream_t st)
+{
+    const int nsm = num_sms();
+    if (nsm < 2) return set_error(FMHA_ERR_CUDA, "cannot query the SM count");
+    const int npairs = nsm / 2;
+    const WideWs w = wide_ws_layout(a, npairs);
+    if (!ws || ws_bytes < w.total) return set_error(FMHA_ERR_WORKSPACE, "wide-head path: workspace too small");
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    const int Hq_per = a.Hq / a.Hkv;
+    const int R = Hq_per * a.Sq;
+    const int row_tiles = (R + kWRows - 1) / kWRows;
+    const int heads = a.B * a.Hkv;
+    CUtensorMap qmap, kmap, vmap;
+    {
+        const uint64_t dims[3] = {static_cast<uint64_t>(kWD), static_cast<uint64_t>(R), static_cast<uint64_t>(heads)};
+        const uint64_t strides[2] = {static_cast<uint64_t>(kWD) * 2, static_cast<uint64_t>(R) * kWD * 2};
+        const uint32_t box[3] = {64, static_cast<uint32_t>(kWRows), 1};
+        int rc = make_tmap_bf16(&qmap, a.q, 3, dims, strides, box);
+        if (rc) return rc;
+    }
+    {
+        const uint64_t dims[3] = {static_cast<uint64_t>(kWD), static_cast<uint64_t>(a.Skv), static_cast<uint64_t>(heads)};
+        const uint64_t strides[2] = {static_cast<uint64_t>(kWD) * 2, static_cast<uint64_t>(a.Skv) * kWD * 2};
+        const uint32_t box[3] = {64, static_cast<uint32_t>(kWKeys), 1};
+        int rc = make_tmap_bf16(&kmap, a.k, 3, dims, strides, box);
+        if (rc) return rc;
+        rc = make_tmap_bf16(&vmap, a.v, 3, dims, strides, box);
+        if (rc) return rc;
+    }
+    WideParams p{};
+    p.U = heads * row_tiles;
+    p.row_tiles = row_tiles;
+    p.Hkv = a.Hkv;
+    p.R = R;
+    p.Skv = a.Skv;
+    p.c = a.scale * kLog2eW;
+    p.seqlens = a.seqlens;
+    p.prefix = a.seqlens ? reinterpret_cast<const int32_t*>(base + w.prefix_off) : nullptr;
+    p.tiles_uniform = (a.Skv + kWKeys - 1) / kWKeys;
+    const bool nvfp4 = a.out_kind == FMHA_OUT_NVFP4;
+    p.out = nvfp4 ? nullptr : a.out;
+    p.out_f32 = a.out_kind == FMHA_OUT_F32 ? 1 : 0;
+    p.lse = a.lse;
+    p.o_stage = nvfp4 ? (a.out_f32 ? a.out_f32 : reinterpret_cast<float*>(base + w.stage_off)) : nullptr;
+    p.amax_bits = nvfp4 ? reinterpret_cast<unsigned*>(a.amax_slot) : nullptr;
+    p.part_lse = reinterpret_cast<float*>(base + w.lse_off);
+    p.part_o = reinterpret_cast<float*>(base + w.o_off);
+    p.status = device_status_ptr();
+    p.limit = wait_limit();
+    if (p.prefix) {
+        wide_prefix_kernel<<<1, 1024, 0, st>>>(a.seqlens, a.Hkv, row_tiles, p.U, const_cast<int32_t*>(p.prefix));
+        FMHA_CHECK_LAUNCH("wide_prefix_kernel");
+        count_launch();
+    }
+    FMHA_CHECK_CUDA(cudaFuncSetAttribute(wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kWSmem));
+    timing_mark_begin(st);
+    wide_kernel<<<2 * npairs, kWThreads, kWSmem, st>>>(qmap, kmap, vmap, p);
+    timing_mark_end(st);
+    FMHA_CHECK_LAUNCH("wide_kernel");
+    count_launch();
+    wide_combine_kernel<<<p.U * kWRows, 256, 0, st>>>(p, npairs);
+    FMHA_CHECK_LAUNCH("wide_combine_kernel");
+    count_launch();
+    return FMHA_OK;
+}
+
+}  // namespace fmha

@@ -72,7 +72,8 @@ typedef struct {
  * Attention forward with default options (BF16 output, dense keys, no workspace).
  *   q: BF16 [B,Hq,Sq,D]; k, v: BF16 [B,Hkv,Skv,D]; out: BF16 [B,Hq,Sq,D];
  *   lse: FP32 [B,Hq,Sq] or NULL; scale: multiplies Q K^T before the softmax.
- * Same as fmha_fwd_ex(..., opts = NULL).
+ * Same as fmha_fwd_ex(..., opts = NULL).  D = 512 always needs a workspace (its value columns are
+ * split over CTA pairs whose partial results are merged), so it goes through fmha_fwd_ex.
  */
 int fmha_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq, int Hkv,
              int Sq, int Skv, int D, float scale, fmha_stream_t stream);

@@ -1,0 +1,76 @@
+"""GPU parity of the wide-head (D = 512) path against the FP64 oracle, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from attention_tensor_cores_gb300 import inputs
+from attn_util import check_o_lse, oracle_rows, run_attention
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def F():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import attention_tensor_cores_gb300 as F
+    F.load()
+    return F
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Sq,Skv", [
+    (2, 128, 1, 1, 300),     # 128 heads on one key/value head, 10 key tiles with a tail of 12
+    (1, 8, 1, 1, 1000),      # 8 query rows: rows 8..127 of the MMA tile are padding
+    (1, 64, 1, 3, 200),      # 192 rows per key/value head: two 128-row blocks
+    (3, 16, 2, 1, 33),       # GQA 8, two key tiles, the second with one key
+])
+@pytest.mark.parametrize("out_kind", ["bf16", "f32"])
+def test_shapes(F, B, Hq, Hkv, Sq, Skv, out_kind):
+    w = inputs.Workload("t", B, Hq, Hkv, Sq, Skv, 512, 0.5, "bf16", 51)
+    q, k, v, _ = w.make("cuda")
+    res = run_attention(F, q, k, v, w.scale, out_kind=out_kind, num_splits=0)
+    o_ref, l_ref = oracle.attention(q.cpu(), k.cpu(), v.cpu(), w.scale)
+    check_o_lse(res["o"], res["lse"], o_ref, l_ref, out_kind)
+
+
+def test_ragged_nan_padding_and_empty(F):
+    B, Hq, Hkv, Skv = 4, 16, 2, 500
+    sl = [0, 1, 33, 500]
+    w = inputs.Workload("t", B, Hq, Hkv, 1, Skv, 512, 0.5, "bf16", 52)
+    q, k, v, _ = w.make("cuda")
+    for b, n in enumerate(sl):
+        k[b, :, n:] = float("nan")
+        v[b, :, n:] = float("nan")
+    sl_t = torch.tensor(sl, dtype=torch.int32, device="cuda")
+    res = run_attention(F, q, k, v, w.scale, seqlens=sl_t, num_splits=0)
+    o_ref, l_ref = oracle.attention(q.cpu(), k.cpu(), v.cpu(), w.scale, seqlens_k=np.array(sl, np.int32))
+    check_o_lse(res["o"], res["lse"], o_ref, l_ref, "ragged wide")
+    assert np.all(res["o"][:Hq] == 0.0) and np.all(np.isneginf(res["lse"][:Hq]))
+
+
+def test_nvfp4_output_bit_exact(F):
+    w = inputs.Workload("t", 2, 32, 1, 1, 700, 512, 0.5, "bf16", 53)
+    q, k, v, _ = w.make("cuda")
+    res = run_attention(F, q, k, v, w.scale, out_kind="nvfp4", num_splits=0, want_f32=True)
+    o_ref, l_ref = oracle.attention(q.cpu(), k.cpu(), v.cpu(), w.scale)
+    check_o_lse(res["o"], res["lse"], o_ref, l_ref, "wide nvfp4 fp32 O")
+    codes, scales, sg = oracle.nvfp4_quantize(res["o"].reshape(-1))
+    assert sg == res["tensor_scale"]
+    np.testing.assert_array_equal(res["scales"], scales)
+    np.testing.assert_array_equal(res["codes"], codes)
+
+
+def test_wide_full_size_sampled(F):
+    """B32 Hq128 Hkv1 Sq1 Skv16384 D512, N(0, 0.5), BF16 O + LSE: 40 rows from 8 batch entries."""
+    w = inputs.workloads()[3]
+    q, k, v, _ = w.make("cuda")
+    res = run_attention(F, q, k, v, w.scale, num_splits=0)
+    rng = np.random.default_rng(4)
+    bs = sorted(rng.choice(w.B, 8, replace=False).tolist())
+    rows = np.array(sorted(b * w.Hq + h for b in bs for h in rng.choice(w.Hq, 5, replace=False)), dtype=np.int64)
+    o_ref, l_ref = oracle_rows(w, rows)
+    check_o_lse(res["o"][rows], res["lse"][rows], o_ref, l_ref, "wide full size")
+    assert np.all(np.isfinite(res["o"])) and np.all(np.isfinite(res["lse"]))
+    del q, k, v
+    torch.cuda.empty_cache()
