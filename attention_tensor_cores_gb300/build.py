@@ -33,8 +33,13 @@ def _headers() -> list[str]:
         [os.path.join(ROOT, "include", "fmha.h")]
 
 
+# Per-file register ceilings: the row-tile kernel runs 10 warps per SM, so up to 200 registers per
+# thread fit, and the softmax keeps a 128-column row of S in registers.
+PER_FILE_FLAGS = {"prefill.cu": ["-maxrregcount=200"]}
+
+
 def _compile(src: str, obj: str, extra: list[str]) -> tuple[str, str]:
-    cmd = [_nvcc()] + ARCH + NVCC_FLAGS + extra + ["-c", src, "-o", obj]
+    cmd = [_nvcc()] + ARCH + NVCC_FLAGS + PER_FILE_FLAGS.get(os.path.basename(src), []) + extra + ["-c", src, "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc failed for {os.path.basename(src)}:\n{r.stdout}\n{r.stderr}")

@@ -218,6 +218,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 const uint32_t sQ = smem_u32(smem + C::kOffQ + qr.idx * C::kQBytes);
                 int jq[2] = {0, 0}, jp[2] = {0, 0};
                 long long t_idle = clock64();
+                int idle_polls = 0;
                 while ((jp[0] < T || jp[1] < T) && !aborted(wc)) {
                     bool did = false;
 #pragma unroll
@@ -271,7 +272,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     }
                     if (did) {
                         t_idle = clock64();
-                    } else if (clock64() - t_idle > p.limit) {
+                        idle_polls = 0;
+                    } else if (++idle_polls > 4) {
+                        __nanosleep(40);   // leave issue slots to the softmax warps on this SM quarter
+                    }
+                    if (!did && clock64() - t_idle > p.limit) {
                         abort_flag = 1;
                         atomicExch(p.status, kDevTimeout);
                     }
@@ -314,32 +319,42 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     for (int i = 0; i < kTN; ++i)
                         if (j * kTN + i >= n) s[i] = -INFINITY;
                 }
-                float mx[8];
+                float mx[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
-                for (int k = 0; k < 8; ++k) mx[k] = s[k];
-#pragma unroll
-                for (int i = 8; i < kTN; ++i) mx[i & 7] = fmaxf(mx[i & 7], s[i]);
-                const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                       fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * p.c;
+                for (int i = 4; i < kTN; i += 8) {
+                    mx[0] = fmax3(mx[0], s[i], s[i + 1]);
+                    mx[1] = fmax3(mx[1], s[i + 2], s[i + 3]);
+                    if (i + 4 < kTN) {
+                        mx[2] = fmax3(mx[2], s[i + 4], s[i + 5]);
+                        mx[3] = fmax3(mx[3], s[i + 6], s[i + 7]);
+                    }
+                }
+                const float mt = fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]) * p.c;
                 const bool rescale = mt > m_run + kRescaleLog2;
                 float alpha = 1.f;
                 if (rescale) {
                     alpha = ex2_approx(m_run - mt);
                     m_run = mt;
                 }
-                const float neg_m = -m_run;
+                // p = 2^(s*c - m) with packed FP32x2 scale-subtract and sums
+                const uint64_t cc = f32x2(p.c, p.c);
+                const uint64_t nm = f32x2(-m_run, -m_run);
                 uint32_t pk[kTN / 2];
-                float ls[8];
-#pragma unroll
-                for (int k = 0; k < 8; ++k) ls[k] = 0.f;
+                uint64_t ls[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
                 for (int i = 0; i < kTN; i += 2) {
-                    const float p0 = ex2_approx(fmaf(s[i], p.c, neg_m));
-                    const float p1 = ex2_approx(fmaf(s[i + 1], p.c, neg_m));
-                    ls[(i >> 1) & 7] += p0 + p1;
+                    float x0, x1;
+                    f32x2_split(ffma2(f32x2(s[i], s[i + 1]), cc, nm), x0, x1);
+                    const float p0 = ex2_approx(x0);
+                    const float p1 = ex2_approx(x1);
+                    ls[(i >> 1) & 3] = fadd2(ls[(i >> 1) & 3], f32x2(p0, p1));
                     pk[i >> 1] = pack_bf16x2(p0, p1);
                 }
-                l = fmaf(l, alpha, ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7])));
+                float la, lb, lc, ld;
+                f32x2_split(fadd2(fadd2(ls[0], ls[1]), fadd2(ls[2], ls[3])), la, lb);
+                (void)lc;
+                (void)ld;
+                l = fmaf(l, alpha, la + lb);
                 // PV of the previous tile must be done: its P buffer is reused and O must be stable.
                 if (j > 0) mbar_wait(&o_done[q], (gt - 1) & 1, wc);
                 tc_fence_after();
