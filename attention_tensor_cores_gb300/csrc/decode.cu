@@ -554,43 +554,67 @@ __global__ void __launch_bounds__(1024) tile_prefix_kernel(const int32_t* seqlen
 }
 
 // Merges the partial results of units whose tiles were split over several CTAs, and writes the
-// result of units without keys (O = 0, LSE = -inf).  One block of D threads per query row.
+// result of units without keys (O = 0, LSE = -inf).  One block of D threads per query row; warp 0
+// finds the CTAs holding partials of the unit once per block (64-bit divisions).
+constexpr int kMaxPartsD = 512;
+
 __global__ void combine_kernel(const __grid_constant__ DecodeParams p, int nctas)
 {
+    __shared__ int slots[kMaxPartsD];
+    __shared__ int nslots;
     const int row = blockIdx.x;
     const int u = row / p.G;
     const int q = row % p.G;
     const int d = threadIdx.x;
     const int D = p.D;
-    int tiles;
-    long long Tu, T;
-    if (p.prefix) {
-        tiles = p.prefix[u + 1] - p.prefix[u];
-        Tu = p.prefix[u];
-        T = p.prefix[p.U];
-    } else {
-        tiles = p.tiles_uniform;
-        Tu = static_cast<long long>(u) * tiles;
-        T = static_cast<long long>(p.U) * tiles;
+    if (threadIdx.x < 32) {
+        int tiles;
+        long long Tu, T;
+        if (p.prefix) {
+            tiles = p.prefix[u + 1] - p.prefix[u];
+            Tu = p.prefix[u];
+            T = p.prefix[p.U];
+        } else {
+            tiles = p.tiles_uniform;
+            Tu = static_cast<long long>(u) * tiles;
+            T = static_cast<long long>(p.U) * tiles;
+        }
+        int cnt = 0;
+        if (tiles > 0) {
+            const long long P = nctas;
+            const int c0 = static_cast<int>(min((((Tu + 1) * P) - 1) / T, P - 1));
+            const int c1 = static_cast<int>(min((((Tu + tiles) * P) - 1) / T, P - 1));
+            if (c0 == c1) {
+                cnt = -1;   // one CTA held the whole unit and wrote it
+            } else {
+                for (int cw = c0; cw <= c1; cw += 32) {
+                    const int c = cw + static_cast<int>(threadIdx.x);
+                    // CTAs with an empty tile range (possible when T < P) hold no partial
+                    const bool ok = c <= c1 && (c * T) / P != ((c + 1) * T) / P;
+                    const unsigned m = __ballot_sync(0xffffffffu, ok);
+                    if (ok) {
+                        const int idx = cnt + __popc(m & ((1u << threadIdx.x) - 1u));
+                        if (idx < kMaxPartsD) slots[idx] = u + c;
+                    }
+                    cnt += __popc(m);
+                }
+                cnt = min(cnt, kMaxPartsD);
+            }
+        }
+        if (threadIdx.x == 0) nslots = cnt;
     }
+    __syncthreads();
+    const int ns = nslots;
+    if (ns < 0) return;
     float o = 0.f, lse_v = -INFINITY;
-    if (tiles > 0) {
-        const long long P = nctas;
-        const int c0 = static_cast<int>(min((((Tu + 1) * P) - 1) / T, P - 1));
-        const int c1 = static_cast<int>(min((((Tu + tiles) * P) - 1) / T, P - 1));
-        if (c0 == c1) return;   // one CTA held the whole unit and wrote it
-        // CTAs with an empty tile range (possible when T < P) hold no partial
-        auto has_work = [&](int c) { return (c * T) / P != ((c + 1) * T) / P; };
+    if (ns > 0) {
         float mx = -INFINITY;
-        for (int c = c0; c <= c1; ++c)
-            if (has_work(c)) mx = fmaxf(mx, p.part_lse[static_cast<size_t>(u + c) * kN + q]);
+        for (int i = 0; i < ns; ++i) mx = fmaxf(mx, p.part_lse[static_cast<size_t>(slots[i]) * kN + q]);
         float sum = 0.f;
-        for (int c = c0; c <= c1; ++c)
-            if (has_work(c)) sum += __expf(p.part_lse[static_cast<size_t>(u + c) * kN + q] - mx);
+        for (int i = 0; i < ns; ++i) sum += __expf(p.part_lse[static_cast<size_t>(slots[i]) * kN + q] - mx);
         lse_v = mx + __logf(sum);
-        for (int c = c0; c <= c1; ++c) {
-            if (!has_work(c)) continue;
-            const size_t sl = static_cast<size_t>(u + c) * kN + q;
+        for (int i = 0; i < ns; ++i) {
+            const size_t sl = static_cast<size_t>(slots[i]) * kN + q;
             o = fmaf(__expf(p.part_lse[sl] - lse_v), p.part_o[sl * D + d], o);
         }
     }

@@ -15,8 +15,10 @@
 //    end and pair p of P takes [p*T/P, (p+1)*T/P); a run that covers a whole unit writes O and LSE,
 //    otherwise a normalised partial goes to slot unit + p and the combine kernel merges them.
 //  * Roles: warps 0-3 softmax (one query row per thread, lazy rescale as in the row-tile kernel),
-//    warp 4 TMA producer, warp 5 MMA issuer.  S and P are double-buffered in TMEM so the QK of the
-//    next tile overlaps the softmax of this one.  All waits are bounded.
+//    warp 4 loads Q and K, warp 6 loads V (so a V slot that frees late never holds back the next K
+//    tile), warp 5 issues MMAs by polling: a QK may run up to two tiles ahead of the PVs (S is
+//    double-buffered in TMEM), so the tensor pipe does not wait on the softmax.  All waits are
+//    bounded.
 #include <cuda_runtime.h>
 
 #include "internal.h"
@@ -30,7 +32,7 @@ constexpr int kWHalf = 256;         // value columns per CTA
 constexpr int kWRows = 128;         // query rows per unit (MMA M)
 constexpr int kWKeys = 32;          // keys per tile (QK N, PV K)
 constexpr int kWStages = 2;
-constexpr int kWThreads = 192;
+constexpr int kWThreads = 224;   // 4 softmax warps, Q/K producer, MMA issuer, V producer
 constexpr float kLog2eW = 1.4426950408889634f;
 constexpr float kLn2W = 0.6931471805599453f;
 constexpr float kRescaleW = 8.0f;
@@ -200,8 +202,8 @@ __global__ void __launch_bounds__(kWThreads, 1)
             tma_prefetch_desc(&qmap);
             tma_prefetch_desc(&kmap);
             tma_prefetch_desc(&vmap);
-            WRing kr(kWStages), vr(kWStages);
-            uint32_t qn = 0, kcnt[kWStages] = {0, 0}, vcnt[kWStages] = {0, 0};
+            WRing kr(kWStages);
+            uint32_t qn = 0, kcnt[kWStages] = {0, 0};
             while (sched.next(it)) {
                 const int hu = wunit_head(p, it.u);
                 const int rt = it.u % p.row_tiles;
@@ -222,6 +224,20 @@ __global__ void __launch_bounds__(kWThreads, 1)
                         ++kcnt[kr.idx];
                     }
                     kr.advance();
+                }
+            }
+            for (int i = 0; i < kWStages; ++i)
+                if (kcnt[i]) wdrain(&k_full[i], (kcnt[i] - 1) & 1, p.limit);
+            if (qn) wdrain(&q_full, (qn - 1) & 1, p.limit);
+        }
+    } else if (warp == 6) {
+        // ------------------------------------------------ V producer (this CTA's half of the columns)
+        if (lane_id() == 0) {
+            WRing vr(kWStages);
+            uint32_t vcnt[kWStages] = {0, 0};
+            while (sched.next(it)) {
+                const int hu = wunit_head(p, it.u);
+                for (int t = it.t0; t < it.t1; ++t) {
                     mbar_wait(&v_empty[vr.idx], vr.phase ^ 1, wc);
                     if (!aborted(wc)) {
                         uint8_t* dst = smem + kWOffV + vr.idx * kWVBytes;
@@ -234,60 +250,80 @@ __global__ void __launch_bounds__(kWThreads, 1)
                     vr.advance();
                 }
             }
-            for (int i = 0; i < kWStages; ++i) {
-                if (kcnt[i]) wdrain(&k_full[i], (kcnt[i] - 1) & 1, p.limit);
+            for (int i = 0; i < kWStages; ++i)
                 if (vcnt[i]) wdrain(&v_full[i], (vcnt[i] - 1) & 1, p.limit);
-            }
-            if (qn) wdrain(&q_full, (qn - 1) & 1, p.limit);
         }
     } else if (warp == 5) {
         // ------------------------------------------------ MMA issuer
         if (lane_id() == 0) {
             constexpr uint32_t idesc_qk = idesc_bf16_f32(kWRows, kWKeys, false, false);
             constexpr uint32_t idesc_pv = idesc_bf16_f32(kWRows, kWHalf, false, true);
-            WRing kr(kWStages), vr(kWStages), sr(2);
-            uint32_t qn = 0, np = 0;
+            uint32_t qn = 0;
+            uint32_t nk = 0, nv = 0, ns = 0, np = 0;   // K tiles, V tiles, QKs and PVs so far (kernel life)
             const uint32_t sQ = smem_u32(smem + kWOffQ);
             while (sched.next(it)) {
                 mbar_wait(&q_full, qn & 1, wc);
                 ++qn;
-                auto pv = [&](bool first) {
-                    mbar_wait(&p_full, np & 1, wc);
-                    mbar_wait(&v_full[vr.idx], vr.phase, wc);
-                    tc_fence_after();
-                    if (!aborted(wc)) {
-                        const uint32_t sV = smem_u32(smem + kWOffV + vr.idx * kWVBytes);
+                const int T = it.t1 - it.t0;
+                int jq = 0, jp = 0;
+                long long t_idle = clock64();
+                int idle = 0;
+                while (jp < T && !aborted(wc)) {
+                    bool did = false;
+                    // QK of tile jq: its K tile landed and its S buffer was read (up to 2 ahead of PV)
+                    if (jq < T) {
+                        const uint32_t ks = nk % kWStages, sb = ns & 1;
+                        bool ok = mbar_test(&k_full[ks], (nk / kWStages) & 1);
+                        if (ok) ok = mbar_test(&s_empty[sb], ((ns >> 1) & 1) ^ 1);
+                        if (ok) {
+                            tc_fence_after();
+                            const uint32_t sK = smem_u32(smem + kWOffK + ks * kWKBytes);
 #pragma unroll
-                        for (int ks = 0; ks < kWKeys / 16; ++ks) {
-                            const uint64_t db = sdesc_sw128(sV + ks * 2048, kWKeys * 128, 1024);
-                            mma_ts(tmem + kWColO, tmem + kWColP + ks * 8, db, idesc_pv, (!first || ks > 0) ? 1u : 0u);
+                            for (int kk = 0; kk < kWD / 16; ++kk) {
+                                const uint64_t da = sdesc_sw128(sQ + (kk >> 2) * (kWRows * 128) + (kk & 3) * 32, 16, 1024);
+                                const uint64_t db = sdesc_sw128(sK + (kk >> 2) * (kWKeys * 128) + (kk & 3) * 32, 16, 1024);
+                                mma_ss(tmem + kWColS + sb * kWKeys, da, db, idesc_qk, kk > 0 ? 1u : 0u);
+                            }
+                            mma_commit(&s_full[sb]);
+                            mma_commit(&k_empty[ks]);
+                            ++nk;
+                            ++ns;
+                            ++jq;
+                            did = true;
                         }
-                        mma_commit(&o_done);
-                        mma_commit(&v_empty[vr.idx]);
                     }
-                    ++np;
-                    vr.advance();
-                };
-                for (int t = it.t0; t < it.t1; ++t) {
-                    mbar_wait(&k_full[kr.idx], kr.phase, wc);
-                    mbar_wait(&s_empty[sr.idx], sr.phase ^ 1, wc);
-                    tc_fence_after();
-                    if (!aborted(wc)) {
-                        const uint32_t sK = smem_u32(smem + kWOffK + kr.idx * kWKBytes);
+                    // PV of tile jp: its P is written and its V tile landed
+                    if (jp < jq) {
+                        const uint32_t vs = nv % kWStages;
+                        bool ok = mbar_test(&p_full, np & 1);
+                        if (ok) ok = mbar_test(&v_full[vs], (nv / kWStages) & 1);
+                        if (ok) {
+                            tc_fence_after();
+                            const uint32_t sV = smem_u32(smem + kWOffV + vs * kWVBytes);
 #pragma unroll
-                        for (int kk = 0; kk < kWD / 16; ++kk) {
-                            const uint64_t da = sdesc_sw128(sQ + (kk >> 2) * (kWRows * 128) + (kk & 3) * 32, 16, 1024);
-                            const uint64_t db = sdesc_sw128(sK + (kk >> 2) * (kWKeys * 128) + (kk & 3) * 32, 16, 1024);
-                            mma_ss(tmem + kWColS + sr.idx * kWKeys, da, db, idesc_qk, kk > 0 ? 1u : 0u);
+                            for (int kq = 0; kq < kWKeys / 16; ++kq) {
+                                const uint64_t db = sdesc_sw128(sV + kq * 2048, kWKeys * 128, 1024);
+                                mma_ts(tmem + kWColO, tmem + kWColP + kq * 8, db, idesc_pv, (jp > 0 || kq > 0) ? 1u : 0u);
+                            }
+                            mma_commit(&o_done);
+                            mma_commit(&v_empty[vs]);
+                            ++nv;
+                            ++np;
+                            ++jp;
+                            did = true;
                         }
-                        mma_commit(&s_full[sr.idx]);
-                        mma_commit(&k_empty[kr.idx]);
                     }
-                    kr.advance();
-                    sr.advance();
-                    if (t > it.t0) pv(t - 1 == it.t0);
+                    if (did) {
+                        t_idle = clock64();
+                        idle = 0;
+                    } else {
+                        if (++idle > 8) __nanosleep(32);
+                        if (clock64() - t_idle > p.limit) {
+                            *reinterpret_cast<volatile int*>(&abort_flag) = 1;
+                            atomicExch(p.status, kDevTimeout);
+                        }
+                    }
                 }
-                pv(it.t1 - 1 == it.t0);
                 if (!aborted(wc)) mma_commit(&q_empty);
             }
             mma_commit(&mma_done);
@@ -459,35 +495,60 @@ __global__ void __launch_bounds__(1024) wide_prefix_kernel(const int32_t* seqlen
 }
 
 // Merges split units (lse = log sum exp lse_i, O = sum exp(lse_i - lse) O_i) and writes units
-// without keys (O = 0, LSE = -inf).  One block of 256 threads (2 columns each) per query row.
+// without keys (O = 0, LSE = -inf).  One block of 256 threads (2 columns each) per query row.  The
+// pairs that hold partials of the unit are found once per block (64-bit divisions) by warp 0.
+constexpr int kMaxParts = 512;
+
 __global__ void __launch_bounds__(256) wide_combine_kernel(const __grid_constant__ WideParams p, int npairs)
 {
+    __shared__ int slots[kMaxParts];
+    __shared__ int nslots;
     const int u = blockIdx.x / kWRows;
     const int r = blockIdx.x % kWRows;
     const int hu = wunit_head(p, u);
     const int row = (u % p.row_tiles) * kWRows + r;
     if (row >= p.R) return;
     const int tiles = wunit_tiles(p, u);
-    const long long Tu = wunit_start(p, u);
-    const long long T = p.prefix ? p.prefix[p.U] : static_cast<long long>(p.U) * p.tiles_uniform;
+    if (threadIdx.x < 32) {
+        int cnt = 0;
+        if (tiles > 0) {
+            const long long Tu = wunit_start(p, u);
+            const long long T = p.prefix ? p.prefix[p.U] : static_cast<long long>(p.U) * p.tiles_uniform;
+            const long long P = npairs;
+            const int c0 = static_cast<int>(min((((Tu + 1) * P) - 1) / T, P - 1));
+            const int c1 = static_cast<int>(min((((Tu + tiles) * P) - 1) / T, P - 1));
+            if (c0 == c1) {
+                cnt = -1;   // one pair held the whole unit and wrote it
+            } else {
+                for (int c0w = c0; c0w <= c1; c0w += 32) {
+                    const int c = c0w + static_cast<int>(threadIdx.x);
+                    // pairs with an empty tile range (possible when T < P) hold no partial
+                    const bool ok = c <= c1 && (c * T) / P != ((c + 1) * T) / P;
+                    const unsigned m = __ballot_sync(0xffffffffu, ok);
+                    if (ok) {
+                        const int idx = cnt + __popc(m & ((1u << threadIdx.x) - 1u));
+                        if (idx < kMaxParts) slots[idx] = u + c;
+                    }
+                    cnt += __popc(m);
+                }
+                cnt = min(cnt, kMaxParts);
+            }
+        }
+        if (threadIdx.x == 0) nslots = cnt;
+    }
+    __syncthreads();
+    const int ns = nslots;
+    if (ns < 0) return;
     float o[2] = {0.f, 0.f};
     float lse_v = -INFINITY;
-    if (tiles > 0) {
-        const long long P = npairs;
-        const int c0 = static_cast<int>(min((((Tu + 1) * P) - 1) / T, P - 1));
-        const int c1 = static_cast<int>(min((((Tu + tiles) * P) - 1) / T, P - 1));
-        if (c0 == c1) return;   // one pair held the whole unit and wrote it
-        auto has_work = [&](int c) { return (c * T) / P != ((c + 1) * T) / P; };
+    if (ns > 0) {
         float mx = -INFINITY;
-        for (int c = c0; c <= c1; ++c)
-            if (has_work(c)) mx = fmaxf(mx, p.part_lse[static_cast<size_t>(u + c) * kWRows + r]);
+        for (int i = 0; i < ns; ++i) mx = fmaxf(mx, p.part_lse[static_cast<size_t>(slots[i]) * kWRows + r]);
         float sum = 0.f;
-        for (int c = c0; c <= c1; ++c)
-            if (has_work(c)) sum += __expf(p.part_lse[static_cast<size_t>(u + c) * kWRows + r] - mx);
+        for (int i = 0; i < ns; ++i) sum += __expf(p.part_lse[static_cast<size_t>(slots[i]) * kWRows + r] - mx);
         lse_v = mx + __logf(sum);
-        for (int c = c0; c <= c1; ++c) {
-            if (!has_work(c)) continue;
-            const size_t sl = static_cast<size_t>(u + c) * kWRows + r;
+        for (int i = 0; i < ns; ++i) {
+            const size_t sl = static_cast<size_t>(slots[i]) * kWRows + r;
             const float wgt = __expf(p.part_lse[sl] - lse_v);
             const float2 v = reinterpret_cast<const float2*>(p.part_o + sl * kWD)[threadIdx.x];
             o[0] = fmaf(wgt, v.x, o[0]);
@@ -495,7 +556,6 @@ __global__ void __launch_bounds__(256) wide_combine_kernel(const __grid_constant
         }
     }
     const size_t orow = static_cast<size_t>(hu) * p.R + row;
-    const int col = 2 * threadIdx.x;
     if (p.o_stage) reinterpret_cast<float2*>(p.o_stage + orow * kWD)[threadIdx.x] = make_float2(o[0], o[1]);
     if (p.out) {
         if (p.out_f32)
@@ -503,7 +563,6 @@ __global__ void __launch_bounds__(256) wide_combine_kernel(const __grid_constant
         else
             reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(p.out) + orow * kWD)[threadIdx.x] = pack_bf16x2(o[0], o[1]);
     }
-    (void)col;
     if (threadIdx.x == 0 && p.lse) p.lse[orow] = lse_v;
     if (p.amax_bits) {
         float m = fmaxf(fabsf(o[0]), fabsf(o[1]));
