@@ -310,11 +310,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // nothing may still be landing in shared memory when the CTA exits
             for (int i = 0; i < S; ++i) {
-                if (kcnt[i]) drain_wait(&k_full[i], (kcnt[i] - 1) & 1, p.limit);
-                if (vcnt[i]) drain_wait(&v_full[i], (vcnt[i] - 1) & 1, p.limit);
+                if (kcnt[i]) drain_wait(&k_full[i], (kcnt[i] - 1) & 1, kDrainLimit);
+                if (vcnt[i]) drain_wait(&v_full[i], (vcnt[i] - 1) & 1, kDrainLimit);
             }
             for (int i = 0; i < 2; ++i)
-                if (qcnt[i]) drain_wait(&q_full[i], (qcnt[i] - 1) & 1, p.limit);
+                if (qcnt[i]) drain_wait(&q_full[i], (qcnt[i] - 1) & 1, kDrainLimit);
         }
     } else if (warp == 5) {
         // ------------------------------------------------ MMA issuer
@@ -375,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 qr.advance();
             }
             mma_commit(&mma_done);
-            drain_wait(&mma_done, 0, p.limit);
+            drain_wait(&mma_done, 0, kDrainLimit);
         }
     } else {
         // ------------------------------------------------ softmax / correction / epilogue (128 threads)

@@ -194,11 +194,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 }
             }
             for (int i = 0; i < S; ++i) {
-                if (kcnt[i]) drain_wait_p(&k_full[i], (kcnt[i] - 1) & 1, p.limit);
-                if (vcnt[i]) drain_wait_p(&v_full[i], (vcnt[i] - 1) & 1, p.limit);
+                if (kcnt[i]) drain_wait_p(&k_full[i], (kcnt[i] - 1) & 1, kDrainLimit);
+                if (vcnt[i]) drain_wait_p(&v_full[i], (vcnt[i] - 1) & 1, kDrainLimit);
             }
             for (int i = 0; i < QS; ++i)
-                if (qcnt[i]) drain_wait_p(&q_full[i], (qcnt[i] - 1) & 1, p.limit);
+                if (qcnt[i]) drain_wait_p(&q_full[i], (qcnt[i] - 1) & 1, kDrainLimit);
         }
     } else if (warp == 9) {
         // ------------------------------------------------ MMA issuer (polls, issues whatever is ready)
@@ -286,7 +286,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 gtile += T;
             }
             mma_commit(&mma_done);
-            drain_wait_p(&mma_done, 0, p.limit);
+            drain_wait_p(&mma_done, 0, kDrainLimit);
         }
     } else {
         // ------------------------------------------------ softmax / rescale / epilogue, one row per thread

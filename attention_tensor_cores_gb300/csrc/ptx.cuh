@@ -96,6 +96,12 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity)
     return ok != 0;
 }
 
+// Limit (clock64 cycles, about 2 s) of the teardown waits that make sure no copy or MMA is still
+// in flight when a CTA exits.  It is independent of the wait limit, which a caller may set very
+// small: an expired wait must never let a CTA leave while a TMA copy is still landing in its
+// shared memory.
+constexpr long long kDrainLimit = 4000000000LL;
+
 // Status codes a kernel can leave in the device status word.
 enum : int { kDevOk = 0, kDevTimeout = 5 };
 
@@ -122,18 +128,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
     if (mbar_try_wait(a, parity))
         return true;
     const long long t0 = clock64();
-    for (uint32_t it = 1;; ++it) {
+    for (;;) {
+        // each failed try_wait may already have suspended the thread for a while: check the
+        // abort flag and the clock after every one
+        if (aborted(w))
+            return false;
+        if (clock64() - t0 > w.limit) {
+            *reinterpret_cast<volatile int*>(w.abort_flag) = 1;
+            atomicExch(w.status, kDevTimeout);
+            return false;
+        }
         if (mbar_try_wait(a, parity))
             return true;
-        if ((it & 63) == 0) {
-            if (aborted(w))
-                return false;
-            if (clock64() - t0 > w.limit) {
-                *reinterpret_cast<volatile int*>(w.abort_flag) = 1;
-                atomicExch(w.status, kDevTimeout);
-                return false;
-            }
-        }
     }
 }
 
@@ -195,18 +201,16 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
     if (mbar_try_wait_cluster(a, parity))
         return true;
     const long long t0 = clock64();
-    for (uint32_t it = 1;; ++it) {
+    for (;;) {
+        if (aborted(w))
+            return false;
+        if (clock64() - t0 > w.limit) {
+            *reinterpret_cast<volatile int*>(w.abort_flag) = 1;
+            atomicExch(w.status, kDevTimeout);
+            return false;
+        }
         if (mbar_try_wait_cluster(a, parity))
             return true;
-        if ((it & 63) == 0) {
-            if (aborted(w))
-                return false;
-            if (clock64() - t0 > w.limit) {
-                *reinterpret_cast<volatile int*>(w.abort_flag) = 1;
-                atomicExch(w.status, kDevTimeout);
-                return false;
-            }
-        }
     }
 }
 

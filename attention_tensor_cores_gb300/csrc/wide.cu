@@ -227,8 +227,8 @@ __global__ void __launch_bounds__(kWThreads, 1)
                 }
             }
             for (int i = 0; i < kWStages; ++i)
-                if (kcnt[i]) wdrain(&k_full[i], (kcnt[i] - 1) & 1, p.limit);
-            if (qn) wdrain(&q_full, (qn - 1) & 1, p.limit);
+                if (kcnt[i]) wdrain(&k_full[i], (kcnt[i] - 1) & 1, kDrainLimit);
+            if (qn) wdrain(&q_full, (qn - 1) & 1, kDrainLimit);
         }
     } else if (warp == 6) {
         // ------------------------------------------------ V producer (this CTA's half of the columns)
@@ -251,7 +251,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
                 }
             }
             for (int i = 0; i < kWStages; ++i)
-                if (vcnt[i]) wdrain(&v_full[i], (vcnt[i] - 1) & 1, p.limit);
+                if (vcnt[i]) wdrain(&v_full[i], (vcnt[i] - 1) & 1, kDrainLimit);
         }
     } else if (warp == 5) {
         // ------------------------------------------------ MMA issuer
@@ -327,7 +327,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
                 if (!aborted(wc)) mma_commit(&q_empty);
             }
             mma_commit(&mma_done);
-            wdrain(&mma_done, 0, p.limit);
+            wdrain(&mma_done, 0, kDrainLimit);
         }
     } else {
         // ------------------------------------------------ softmax / epilogue, one query row per thread
