@@ -287,13 +287,20 @@ def cpu_baseline(w, metric_unit: str, budget_s: float = 8.0, rows_per_step: int 
 # ------------------------------------------------------------------------------------------------
 # arms
 # ------------------------------------------------------------------------------------------------
-def _max_over_ranks(x: float, dist):
+def _max_over_ranks(x: float, dist, device="cuda"):
+    """Largest value of x over all ranks (the timed region is the slowest rank's)."""
     if dist is None:
         return x
     import torch
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def aggregate_rate(units_per_rank_per_step: float, steps: int, world: int, region_ms_max: float) -> float:
+    """Whole-job throughput: the units every rank processed over the slowest rank's timed region
+    (replicas: each rank runs the same workload on its own GPU)."""
+    return world * steps * units_per_rank_per_step / (region_ms_max / 1e3)
 
 
 def _workload_entry(F, w, idx, steps, warmup, peaks):
@@ -350,7 +357,7 @@ def run_ours(args, rank, world, local):
     r = time_case(F, head, args.steps, args.warmup, sampler, dist)
     region_ms = _max_over_ranks(r["region_ms"], dist)
     step_ms = region_ms / args.steps
-    value = world * args.steps * w.kv_bytes() / (region_ms / 1e3) / 1e9
+    value = aggregate_rate(w.kv_bytes(), args.steps, world, region_ms) / 1e9
     kern_ms = statistics.mean(r["kernel_ms"])
     achieved = head.algorithmic_bytes() / (kern_ms / 1e3) / 1e9
     roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
