@@ -277,13 +277,16 @@ __global__ void __launch_bounds__(kWThreads, 1)
                         if (ok) ok = mbar_test(&s_empty[sb], ((ns >> 1) & 1) ^ 1);
                         if (ok) {
                             tc_fence_after();
-                            const uint32_t sK = smem_u32(smem + kWOffK + ks * kWKBytes);
+                            // descriptors once per tile; K steps add constant offsets to their address
+                            // fields (addr >> 4 in 14 bits covers all of shared memory: no carry leaves it)
+                            const uint64_t dq = sdesc_sw128(sQ, 16, 1024);
+                            const uint64_t dk = sdesc_sw128(smem_u32(smem + kWOffK + ks * kWKBytes), 16, 1024);
+                            const uint32_t ds = tmem + kWColS + sb * kWKeys;
+                            mma_ss(ds, dq, dk, idesc_qk, 0u);
 #pragma unroll
-                            for (int kk = 0; kk < kWD / 16; ++kk) {
-                                const uint64_t da = sdesc_sw128(sQ + (kk >> 2) * (kWRows * 128) + (kk & 3) * 32, 16, 1024);
-                                const uint64_t db = sdesc_sw128(sK + (kk >> 2) * (kWKeys * 128) + (kk & 3) * 32, 16, 1024);
-                                mma_ss(tmem + kWColS + sb * kWKeys, da, db, idesc_qk, kk > 0 ? 1u : 0u);
-                            }
+                            for (int kk = 1; kk < kWD / 16; ++kk)
+                                mma_ss(ds, dq + (((kk >> 2) * (kWRows * 128) + (kk & 3) * 32) >> 4),
+                                       dk + (((kk >> 2) * (kWKeys * 128) + (kk & 3) * 32) >> 4), idesc_qk, 1u);
                             mma_commit(&s_full[sb]);
                             mma_commit(&k_empty[ks]);
                             ++nk;
