@@ -561,7 +561,9 @@ constexpr int kMaxPartsD = 512;
 __global__ void combine_kernel(const __grid_constant__ DecodeParams p, int nctas)
 {
     __shared__ int slots[kMaxPartsD];
+    __shared__ float weights[kMaxPartsD];
     __shared__ int nslots;
+    __shared__ float lse_sh;
     const int row = blockIdx.x;
     const int u = row / p.G;
     const int q = row % p.G;
@@ -601,23 +603,30 @@ __global__ void combine_kernel(const __grid_constant__ DecodeParams p, int nctas
                 cnt = min(cnt, kMaxPartsD);
             }
         }
-        if (threadIdx.x == 0) nslots = cnt;
+        __syncwarp();
+        // LSE of the merged row and each partial's weight exp(lse_i - lse), once per block
+        float mx = -INFINITY;
+        for (int i = static_cast<int>(threadIdx.x); i < cnt; i += 32) mx = fmaxf(mx, p.part_lse[static_cast<size_t>(slots[i]) * kN + q]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        float sum = 0.f;
+        for (int i = static_cast<int>(threadIdx.x); i < cnt; i += 32) sum += __expf(p.part_lse[static_cast<size_t>(slots[i]) * kN + q] - mx);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        const float lse_all = cnt > 0 ? mx + __logf(sum) : -INFINITY;
+        for (int i = static_cast<int>(threadIdx.x); i < cnt; i += 32) weights[i] = __expf(p.part_lse[static_cast<size_t>(slots[i]) * kN + q] - lse_all);
+        if (threadIdx.x == 0) {
+            nslots = cnt;
+            lse_sh = lse_all;
+        }
     }
     __syncthreads();
     const int ns = nslots;
     if (ns < 0) return;
-    float o = 0.f, lse_v = -INFINITY;
-    if (ns > 0) {
-        float mx = -INFINITY;
-        for (int i = 0; i < ns; ++i) mx = fmaxf(mx, p.part_lse[static_cast<size_t>(slots[i]) * kN + q]);
-        float sum = 0.f;
-        for (int i = 0; i < ns; ++i) sum += __expf(p.part_lse[static_cast<size_t>(slots[i]) * kN + q] - mx);
-        lse_v = mx + __logf(sum);
-        for (int i = 0; i < ns; ++i) {
-            const size_t sl = static_cast<size_t>(slots[i]) * kN + q;
-            o = fmaf(__expf(p.part_lse[sl] - lse_v), p.part_o[sl * D + d], o);
-        }
-    }
+    float o = 0.f;
+    const float lse_v = lse_sh;
+#pragma unroll 4
+    for (int i = 0; i < ns; ++i) o = fmaf(weights[i], p.part_o[(static_cast<size_t>(slots[i]) * kN + q) * D + d], o);
     const size_t r = static_cast<size_t>(row);
     if (p.o_stage) p.o_stage[r * D + d] = o;
     if (p.out) {

@@ -232,15 +232,14 @@ __global__ void __launch_bounds__(kPThreads, 1)
                                 ok = npv[q] == nqk[q] && mbar_test(&o_done[q], (npv[q] - 1) & 1);
                             if (ok) {
                                 tc_fence_after();
-                                const uint32_t sK = smem_u32(smem + C::kOffK + (g % S) * C::kKVBytes);
-                                const uint32_t sQq = sQ + q * C::kQTileBytes;
+                                // descriptors once; K steps add constant offsets to the address fields
+                                const uint64_t dq = sdesc_sw128(sQ + q * C::kQTileBytes, 16, 1024);
+                                const uint64_t dk = sdesc_sw128(smem_u32(smem + C::kOffK + (g % S) * C::kKVBytes), 16, 1024);
                                 const uint32_t dS = tmem + q * 128;
 #pragma unroll
-                                for (int kk = 0; kk < D / 16; ++kk) {
-                                    const uint64_t da = sdesc_sw128(sQq + (kk >> 2) * (kTM * 128) + (kk & 3) * 32, 16, 1024);
-                                    const uint64_t db = sdesc_sw128(sK + (kk >> 2) * (kTN * 128) + (kk & 3) * 32, 16, 1024);
-                                    mma_ss(dS, da, db, idesc_qk, kk > 0 ? 1u : 0u);
-                                }
+                                for (int kk = 0; kk < D / 16; ++kk)
+                                    mma_ss(dS, dq + (((kk >> 2) * (kTM * 128) + (kk & 3) * 32) >> 4),
+                                           dk + (((kk >> 2) * (kTN * 128) + (kk & 3) * 32) >> 4), idesc_qk, kk > 0 ? 1u : 0u);
                                 mma_commit(&s_full[q]);
                                 ++nqk[q];
                                 ++jq[q];
@@ -254,14 +253,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
                             if (ok) ok = mbar_test(&v_full[g % S], (g / S) & 1);
                             if (ok) {
                                 tc_fence_after();
-                                const uint32_t sV = smem_u32(smem + C::kOffV + (g % S) * C::kKVBytes);
+                                const uint64_t dv = sdesc_sw128(smem_u32(smem + C::kOffV + (g % S) * C::kKVBytes), kTN * 128, 1024);
                                 const uint32_t dO = tmem + C::kColO + q * D;
                                 const uint32_t aP = tmem + C::kColP + q * C::kPStride;
 #pragma unroll
-                                for (int ks = 0; ks < kTN / 16; ++ks) {
-                                    const uint64_t db = sdesc_sw128(sV + ks * 2048, kTN * 128, 1024);
-                                    mma_ts(dO, aP + ks * 8, db, idesc_pv, (jp[q] > 0 || ks > 0) ? 1u : 0u);
-                                }
+                                for (int ks = 0; ks < kTN / 16; ++ks)
+                                    mma_ts(dO, aP + ks * 8, dv + ((ks * 2048) >> 4), idesc_pv, (jp[q] > 0 || ks > 0) ? 1u : 0u);
                                 mma_commit(&o_done[q]);
                                 ++npv[q];
                                 ++jp[q];

@@ -498,19 +498,20 @@ __global__ void __launch_bounds__(1024) wide_prefix_kernel(const int32_t* seqlen
 }
 
 // Merges split units (lse = log sum exp lse_i, O = sum exp(lse_i - lse) O_i) and writes units
-// without keys (O = 0, LSE = -inf).  One block of 256 threads (2 columns each) per query row.  The
-// pairs that hold partials of the unit are found once per block (64-bit divisions) by warp 0.
+// without keys (O = 0, LSE = -inf).  A block serves 8 query rows of one unit: warp 0 finds the
+// pairs that hold partials of the unit once (64-bit divisions), then warp w merges row w: lane i
+// holds partial i's weight, and each lane sums 16 of the row's 512 columns over the partials.
 constexpr int kMaxParts = 512;
+constexpr int kCombRows = 8;
 
-__global__ void __launch_bounds__(256) wide_combine_kernel(const __grid_constant__ WideParams p, int npairs)
+__global__ void __launch_bounds__(32 * kCombRows) wide_combine_kernel(const __grid_constant__ WideParams p, int npairs)
 {
     __shared__ int slots[kMaxParts];
     __shared__ int nslots;
-    const int u = blockIdx.x / kWRows;
-    const int r = blockIdx.x % kWRows;
+    const int u = blockIdx.x / (kWRows / kCombRows);
+    const int r = (blockIdx.x % (kWRows / kCombRows)) * kCombRows + static_cast<int>(threadIdx.x / 32);
+    const int lane = static_cast<int>(threadIdx.x & 31);
     const int hu = wunit_head(p, u);
-    const int row = (u % p.row_tiles) * kWRows + r;
-    if (row >= p.R) return;
     const int tiles = wunit_tiles(p, u);
     if (threadIdx.x < 32) {
         int cnt = 0;
@@ -523,13 +524,13 @@ __global__ void __launch_bounds__(256) wide_combine_kernel(const __grid_constant
             if (c0 == c1) {
                 cnt = -1;   // one pair held the whole unit and wrote it
             } else {
-                for (int c0w = c0; c0w <= c1; c0w += 32) {
-                    const int c = c0w + static_cast<int>(threadIdx.x);
+                for (int cw = c0; cw <= c1; cw += 32) {
+                    const int c = cw + lane;
                     // pairs with an empty tile range (possible when T < P) hold no partial
                     const bool ok = c <= c1 && (c * T) / P != ((c + 1) * T) / P;
                     const unsigned m = __ballot_sync(0xffffffffu, ok);
                     if (ok) {
-                        const int idx = cnt + __popc(m & ((1u << threadIdx.x) - 1u));
+                        const int idx = cnt + __popc(m & ((1u << lane) - 1u));
                         if (idx < kMaxParts) slots[idx] = u + c;
                     }
                     cnt += __popc(m);
@@ -537,41 +538,70 @@ __global__ void __launch_bounds__(256) wide_combine_kernel(const __grid_constant
                 cnt = min(cnt, kMaxParts);
             }
         }
-        if (threadIdx.x == 0) nslots = cnt;
+        if (lane == 0) nslots = cnt;
     }
     __syncthreads();
     const int ns = nslots;
-    if (ns < 0) return;
-    float o[2] = {0.f, 0.f};
-    float lse_v = -INFINITY;
-    if (ns > 0) {
-        float mx = -INFINITY;
-        for (int i = 0; i < ns; ++i) mx = fmaxf(mx, p.part_lse[static_cast<size_t>(slots[i]) * kWRows + r]);
-        float sum = 0.f;
-        for (int i = 0; i < ns; ++i) sum += __expf(p.part_lse[static_cast<size_t>(slots[i]) * kWRows + r] - mx);
-        lse_v = mx + __logf(sum);
-        for (int i = 0; i < ns; ++i) {
-            const size_t sl = static_cast<size_t>(slots[i]) * kWRows + r;
-            const float wgt = __expf(p.part_lse[sl] - lse_v);
-            const float2 v = reinterpret_cast<const float2*>(p.part_o + sl * kWD)[threadIdx.x];
-            o[0] = fmaf(wgt, v.x, o[0]);
-            o[1] = fmaf(wgt, v.y, o[1]);
+    const int row = (u % p.row_tiles) * kWRows + r;
+    if (ns < 0 || row >= p.R) return;
+    // merged LSE of this row
+    float mx = -INFINITY;
+    for (int i = lane; i < ns; i += 32) mx = fmaxf(mx, p.part_lse[static_cast<size_t>(slots[i]) * kWRows + r]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    float sum = 0.f;
+    for (int i = lane; i < ns; i += 32) sum += __expf(p.part_lse[static_cast<size_t>(slots[i]) * kWRows + r] - mx);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    const float lse_v = ns > 0 ? mx + __logf(sum) : -INFINITY;
+    // weighted sum of the partial rows, 16 columns per lane
+    float acc[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) acc[k] = 0.f;
+    for (int c0 = 0; c0 < ns; c0 += 32) {
+        const int mine = c0 + lane;
+        const float w = mine < ns ? __expf(p.part_lse[static_cast<size_t>(slots[mine]) * kWRows + r] - lse_v) : 0.f;
+        const int cnt = min(32, ns - c0);
+        for (int j = 0; j < cnt; ++j) {
+            const float wj = __shfl_sync(0xffffffffu, w, j);
+            const float4* src = reinterpret_cast<const float4*>(p.part_o + (static_cast<size_t>(slots[c0 + j]) * kWRows + r) * kWD) + lane * 4;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float4 v = src[k];
+                acc[4 * k] = fmaf(wj, v.x, acc[4 * k]);
+                acc[4 * k + 1] = fmaf(wj, v.y, acc[4 * k + 1]);
+                acc[4 * k + 2] = fmaf(wj, v.z, acc[4 * k + 2]);
+                acc[4 * k + 3] = fmaf(wj, v.w, acc[4 * k + 3]);
+            }
         }
     }
     const size_t orow = static_cast<size_t>(hu) * p.R + row;
-    if (p.o_stage) reinterpret_cast<float2*>(p.o_stage + orow * kWD)[threadIdx.x] = make_float2(o[0], o[1]);
-    if (p.out) {
-        if (p.out_f32)
-            reinterpret_cast<float2*>(static_cast<float*>(p.out) + orow * kWD)[threadIdx.x] = make_float2(o[0], o[1]);
-        else
-            reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(p.out) + orow * kWD)[threadIdx.x] = pack_bf16x2(o[0], o[1]);
-    }
-    if (threadIdx.x == 0 && p.lse) p.lse[orow] = lse_v;
-    if (p.amax_bits) {
-        float m = fmaxf(fabsf(o[0]), fabsf(o[1]));
+    if (p.o_stage) {
+        float4* dst = reinterpret_cast<float4*>(p.o_stage + orow * kWD) + lane * 4;
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-        if ((threadIdx.x & 31) == 0 && m > 0.f) atomicMax(p.amax_bits, __float_as_uint(m));
+        for (int k = 0; k < 4; ++k) dst[k] = make_float4(acc[4 * k], acc[4 * k + 1], acc[4 * k + 2], acc[4 * k + 3]);
+    }
+    if (p.out) {
+        if (p.out_f32) {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow * kWD) + lane * 4;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) dst[k] = make_float4(acc[4 * k], acc[4 * k + 1], acc[4 * k + 2], acc[4 * k + 3]);
+        } else {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + orow * kWD) + lane * 2;
+#pragma unroll
+            for (int k = 0; k < 2; ++k)
+                dst[k] = make_uint4(pack_bf16x2(acc[8 * k], acc[8 * k + 1]), pack_bf16x2(acc[8 * k + 2], acc[8 * k + 3]),
+                                    pack_bf16x2(acc[8 * k + 4], acc[8 * k + 5]), pack_bf16x2(acc[8 * k + 6], acc[8 * k + 7]));
+        }
+    }
+    if (lane == 0 && p.lse) p.lse[orow] = lse_v;
+    if (p.amax_bits) {
+        float m = 0.f;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) m = fmaxf(m, fabsf(acc[k]));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (lane == 0 && m > 0.f) atomicMax(p.amax_bits, __float_as_uint(m));
     }
 }
 
@@ -668,7 +698,7 @@ int launch_wide(const AttnArgs& a, void* ws, size_t ws_bytes, cudaStream_t st)
     timing_mark_end(st);
     FMHA_CHECK_LAUNCH("wide_kernel");
     count_launch();
-    wide_combine_kernel<<<p.U * kWRows, 256, 0, st>>>(p, npairs);
+    wide_combine_kernel<<<p.U * (kWRows / kCombRows), 32 * kCombRows, 0, st>>>(p, npairs);
     FMHA_CHECK_LAUNCH("wide_combine_kernel");
     count_launch();
     return FMHA_OK;
