@@ -46,7 +46,7 @@ class ClockSampler:
     REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown", 0x2: "applications_clocks"}
 
-    def __init__(self, device_index: int = 0, period_s: float = 0.002):
+    def __init__(self, device_index: int = 0, period_s: float = 0.0002):
         self.ok = False
         self.samples = []
         self.period = period_s
@@ -72,14 +72,17 @@ class ClockSampler:
         except OSError:
             pass
 
-    def _run(self):
+    def _sample(self):
         clk = ctypes.c_uint()
         rs = ctypes.c_ulonglong()
+        self.nvml.nvmlDeviceGetClockInfo(self.dev, 1, ctypes.byref(clk))
+        if self.nvml.nvmlDeviceGetCurrentClocksEventReasons(self.dev, ctypes.byref(rs)) != 0:
+            self.nvml.nvmlDeviceGetCurrentClocksThrottleReasons(self.dev, ctypes.byref(rs))
+        self.samples.append((clk.value, rs.value))
+
+    def _run(self):
         while not self._stop.is_set():
-            self.nvml.nvmlDeviceGetClockInfo(self.dev, 1, ctypes.byref(clk))
-            if self.nvml.nvmlDeviceGetCurrentClocksEventReasons(self.dev, ctypes.byref(rs)) != 0:
-                self.nvml.nvmlDeviceGetCurrentClocksThrottleReasons(self.dev, ctypes.byref(rs))
-            self.samples.append((clk.value, rs.value))
+            self._sample()
             time.sleep(self.period)
 
     def start(self):
@@ -92,6 +95,7 @@ class ClockSampler:
     def stop(self):
         if not self.ok:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvml unavailable"], "samples": 0}
+        self._sample()          # one more at the end of the timed region
         self._stop.set()
         self._t.join()
         mhz = [s[0] for s in self.samples]
