@@ -49,7 +49,7 @@ def _load():
             I = ctypes.c_int
             I64 = ctypes.c_int64
             lib.oracle_attention_f64.argtypes = [P, P, P, I, I, I, I, I, I, ctypes.c_double,
-                                                 P, P, I64, P, P]
+                                                 P, I, P, I64, P, P]
             lib.oracle_attention_f64.restype = I
             lib.oracle_qk_f64.argtypes = [P, P, I, I, I, P]
             lib.oracle_qk_f64.restype = I
@@ -83,10 +83,11 @@ def _bf16_bits(t) -> np.ndarray:
     return np.ascontiguousarray(t.detach().cpu().contiguous().view(torch.int16).numpy()).view(np.uint16)
 
 
-def attention(q, k, v, scale: float, seqlens_k=None, rows=None):
+def attention(q, k, v, scale: float, seqlens_k=None, rows=None, causal: bool = False):
     """FP64 attention for query rows `rows` (flat (b*Hq+hq)*Sq+i; None = all).
 
-    q: [B,Hq,Sq,D], k/v: [B,Hkv,Skv,D] BF16 (torch bf16 or uint16 bits).
+    q: [B,Hq,Sq,D], k/v: [B,Hkv,Skv,D] BF16 (torch bf16 or uint16 bits).  causal: bottom-right
+    aligned mask (query i of Sq sees keys j <= i + n - Sq).
     Returns (o [nrows, D] float64, lse [nrows] float64)."""
     lib = _load()
     B, Hq, Sq, D = q.shape
@@ -105,7 +106,7 @@ def attention(q, k, v, scale: float, seqlens_k=None, rows=None):
     o = np.zeros((nrows, D), dtype=np.float64)
     lse = np.zeros((nrows,), dtype=np.float64)
     rc = lib.oracle_attention_f64(_ptr(qb), _ptr(kb), _ptr(vb), B, Hq, Hkv, Sq, Skv, D,
-                                  float(scale), _ptr(sl), _ptr(rr), nrows, _ptr(o), _ptr(lse))
+                                  float(scale), _ptr(sl), 1 if causal else 0, _ptr(rr), nrows, _ptr(o), _ptr(lse))
     if rc != 0:
         raise ValueError("oracle_attention_f64: bad arguments")
     return o, lse

@@ -13,6 +13,9 @@
  * Readings where the pages are silent: grouped-query attention maps query head hq to key/value
  * head hq / (Hq/Hkv); LSE is the natural log of sum_j exp(s_j) with the scale included; keys at
  * or beyond seqlens_k[b] do not exist; an empty key set gives O = 0 and LSE = -inf.
+ * The causal variant (the pages aim at decode; causal masking is the usual companion of prefill
+ * and of multi-token decode) aligns the mask bottom-right: with n keys, query i of Sq sees keys
+ * 0 .. i + n - Sq, i.e. the last query sees every key.
  */
 #include "oracle.h"
 #include <math.h>
@@ -42,7 +45,7 @@ int oracle_num_threads(void)
 
 int oracle_attention_f64(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                          int B, int Hq, int Hkv, int Sq, int Skv, int D, double scale,
-                         const int32_t* seqlens_k, const int64_t* rows, int64_t nrows,
+                         const int32_t* seqlens_k, int causal, const int64_t* rows, int64_t nrows,
                          double* o, double* lse)
 {
     if (!q || !k || !v || !o || B < 0 || Hq <= 0 || Hkv <= 0 || Sq < 0 || Skv < 0 || D <= 0)
@@ -62,6 +65,7 @@ int oracle_attention_f64(const uint16_t* q, const uint16_t* k, const uint16_t* v
             bad |= 1;
             continue;
         }
+        const int64_t i = r % Sq;
         const int64_t hq = (r / Sq) % Hq;
         const int64_t b = r / ((int64_t)Sq * Hq);
         const int64_t kvh = hq / group;
@@ -69,6 +73,11 @@ int oracle_attention_f64(const uint16_t* q, const uint16_t* k, const uint16_t* v
         if (n < 0 || n > Skv) {
             bad |= 1;
             continue;
+        }
+        if (causal) {
+            /* keys 0 .. i + n - Sq are visible */
+            const int64_t last = i + n - Sq;
+            n = last < 0 ? 0 : (last + 1 < n ? last + 1 : n);
         }
         const uint16_t* qrow = q + r * D;
         const uint16_t* kbase = k + (b * Hkv + kvh) * (int64_t)Skv * D;

@@ -29,12 +29,14 @@ extern "C" {
 /* Attention rows.  q [B,Hq,Sq,D], k/v [B,Hkv,Skv,D], BF16 bit patterns, contiguous.
  * rows: flat query-row indices r = (b*Hq + hq)*Sq + i (NULL = all B*Hq*Sq rows, in order).
  * seqlens_k: int32[B] valid keys per batch (NULL = Skv for all).
+ * causal: 0, or 1 for the bottom-right aligned causal mask: with n valid keys, query i
+ *         (0 <= i < Sq) sees keys j <= i + n - Sq only.
  * o: double[nrows][D]; lse: double[nrows] (natural log of sum_j exp(s_j)).
- * Empty key set (seqlens_k[b] == 0): o = 0, lse = -inf.
+ * Empty key set (no visible key): o = 0, lse = -inf.
  * Returns 0, or -1 on bad arguments.  Uses OpenMP threads when built with -fopenmp. */
 int oracle_attention_f64(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                          int B, int Hq, int Hkv, int Sq, int Skv, int D, double scale,
-                         const int32_t* seqlens_k, const int64_t* rows, int64_t nrows,
+                         const int32_t* seqlens_k, int causal, const int64_t* rows, int64_t nrows,
                          double* o, double* lse);
 
 /* Raw scores S[i][j] = sum_d q[i][d]*k[j][d], no scale. q [Sq,D], k [Skv,D] BF16 bits. */

@@ -177,3 +177,55 @@ def test_generator_distribution():
     assert abs(float(t.mean())) < 0.01 and abs(float(t.std()) - 1.0) < 0.01
     t = inputs.normal_bf16_torch((1 << 18,), 1, 0, 0.5).double()
     assert abs(float(t.std()) - 0.5) < 0.005
+
+
+def _bottom_right_mask(Sq, n):
+    i = torch.arange(Sq)[:, None]
+    j = torch.arange(n)[None, :]
+    return j <= i + (n - Sq)
+
+
+@pytest.mark.parametrize("Sq,Skv", [(37, 37), (5, 300), (1, 64), (130, 129)])
+def test_causal_matches_masked_sdpa(Sq, Skv):
+    """Bottom-right aligned causal mask against torch FP64 SDPA with the explicit boolean mask
+    (and is_causal=True when Sq == Skv, where both alignments coincide)."""
+    B, Hq, Hkv, D = 2, 4, 2, 16
+    q, k, v = _bf16((B, Hq, Sq, D), 31), _bf16((B, Hkv, Skv, D), 32), _bf16((B, Hkv, Skv, D), 33)
+    o, lse = oracle.attention(q, k, v, 0.3, causal=True)
+    kr, vr = k.repeat_interleave(Hq // Hkv, dim=1), v.repeat_interleave(Hq // Hkv, dim=1)
+    mask = _bottom_right_mask(Sq, Skv)
+    ref = F.scaled_dot_product_attention(q.double(), kr.double(), vr.double(), attn_mask=mask, scale=0.3)
+    valid = mask.any(dim=1)                       # rows with at least one visible key
+    o4, lse4 = o.reshape(B, Hq, Sq, D), lse.reshape(B, Hq, Sq)
+    np.testing.assert_allclose(o4[:, :, valid.numpy()], ref[:, :, valid].numpy(), atol=1e-12)
+    s = 0.3 * (q.double() @ kr.double().transpose(-1, -2))
+    s = s.masked_fill(~mask, float("-inf"))
+    np.testing.assert_allclose(lse4[:, :, valid.numpy()], torch.logsumexp(s, -1)[:, :, valid].numpy(), atol=1e-12)
+    assert np.all(o4[:, :, ~valid.numpy()] == 0.0) and np.all(np.isneginf(lse4[:, :, ~valid.numpy()]))
+    if Sq == Skv:
+        ref2 = F.scaled_dot_product_attention(q.double(), kr.double(), vr.double(), is_causal=True, scale=0.3)
+        np.testing.assert_allclose(o4, ref2.numpy(), atol=1e-12)
+
+
+def test_causal_ragged_is_relative_to_each_length():
+    B, H, Sq, Skv, D = 3, 2, 4, 50, 8
+    q, k, v = _bf16((B, H, Sq, D), 34), _bf16((B, H, Skv, D), 35), _bf16((B, H, Skv, D), 36)
+    sl = np.array([10, 2, 50], dtype=np.int32)
+    o, lse = oracle.attention(q, k, v, 0.5, seqlens_k=sl, causal=True)
+    o = o.reshape(B, H, Sq, D)
+    for b in range(B):
+        n = int(sl[b])
+        mask = _bottom_right_mask(Sq, n)
+        valid = mask.any(dim=1)
+        ref = F.scaled_dot_product_attention(q[b:b+1].double(), k[b:b+1, :, :n].double(), v[b:b+1, :, :n].double(),
+                                             attn_mask=mask, scale=0.5)
+        np.testing.assert_allclose(o[b][:, valid.numpy()], ref[0][:, valid].numpy(), atol=1e-12)
+        assert np.all(o[b][:, ~valid.numpy()] == 0.0)
+
+
+def test_causal_single_query_is_dense():
+    q, k, v = _bf16((1, 2, 1, 32), 37), _bf16((1, 2, 77, 32), 38), _bf16((1, 2, 77, 32), 39)
+    a = oracle.attention(q, k, v, 0.2, causal=True)
+    b = oracle.attention(q, k, v, 0.2)
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[1], b[1])
