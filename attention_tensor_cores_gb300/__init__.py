@@ -47,6 +47,7 @@ class fmha_opts(ctypes.Structure):
         ("out_scales", ctypes.c_void_p),
         ("out_tensor_scale", ctypes.c_void_p),
         ("out_f32", ctypes.c_void_p),
+        ("causal", ctypes.c_int),
     ]
 
 
@@ -133,8 +134,9 @@ def fmha_fwd(q, k, v, out, lse, scale: float, stream=None):
 
 
 def make_opts(out_kind=FMHA_OUT_BF16, seqlens_k=None, num_splits=0, workspace=None,
-              out_scales=None, out_tensor_scale=None, out_f32=None) -> fmha_opts:
+              out_scales=None, out_tensor_scale=None, out_f32=None, causal=False) -> fmha_opts:
     o = fmha_opts()
+    o.causal = 1 if causal else 0
     o.out_kind = out_kind
     o.seqlens_k = None if seqlens_k is None else seqlens_k.data_ptr()
     o.num_splits = num_splits

@@ -270,6 +270,7 @@ static AttnArgs make_args(const void* q, const void* k, const void* v, void* out
     a.seqlens = o ? o->seqlens_k : nullptr;
     a.out_kind = o ? o->out_kind : FMHA_OUT_BF16;
     a.out_f32 = (o && o->out_kind == FMHA_OUT_NVFP4) ? o->out_f32 : nullptr;
+    a.causal = (o && o->causal) ? 1 : 0;
     return a;
 }
 

@@ -64,6 +64,8 @@ struct DecodeParams {
     int G;              // real query rows per unit
     int Skv;
     int D;
+    int Sq;             // query rows per head (column q of a unit is query q % Sq)
+    int causal;         // bottom-right aligned causal mask
     float c;            // scale * log2(e)
     const int32_t* seqlens;
     const int32_t* prefix;   // [U+1] tile prefix (ragged split mode), else NULL
@@ -210,7 +212,7 @@ __device__ __forceinline__ float warp_sum(float v)
     return v;
 }
 
-template <int D>
+template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                   const __grid_constant__ CUtensorMap vmap, const __grid_constant__ DecodeParams p)
@@ -387,6 +389,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t tile_ctr = 0;
         while (sched.next(it)) {
             float m[kN], l[kN], acc[kN], alpha_prev[kN];
+            // keys visible to column q: 0 .. lim[q] - 1 (causal: query q % Sq sees keys up to
+            // (q % Sq) + n - Sq; otherwise all n)
+            int lim[kN];
+#pragma unroll
+            for (int q = 0; q < kN; ++q) lim[q] = CAUSAL ? it.n - p.Sq + 1 + (q % p.Sq) : it.n;
 #pragma unroll
             for (int q = 0; q < kN; ++q) {
                 m[q] = -INFINITY;
@@ -416,10 +423,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive(&s_empty[sr.idx]);
                 sr.advance();
 
-                const bool valid = t * kTileKV + tid < it.n;
+                const int kv = t * kTileKV + tid;
+                const bool valid = kv < it.n;
                 float x[kN];
 #pragma unroll
-                for (int q = 0; q < kN; ++q) x[q] = valid ? __uint_as_float(sv[q]) * p.c : -INFINITY;
+                for (int q = 0; q < kN; ++q) x[q] = (CAUSAL ? kv < lim[q] : valid) ? __uint_as_float(sv[q]) * p.c : -INFINITY;
                 float(*rb)[kN] = red_max[tile_ctr & 1];
 #pragma unroll
                 for (int q = 0; q < kN; ++q)
@@ -435,9 +443,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (q < G) {
                         const float mt = fmaxf(fmaxf(rb[0][q], rb[1][q]), fmaxf(rb[2][q], rb[3][q]));
                         const float mn = fmaxf(m[q], mt);
-                        alpha[q] = ex2_approx(m[q] - mn);
+                        // causal: a column with no visible key so far keeps m = -inf (no -inf - -inf)
+                        alpha[q] = (CAUSAL && m[q] == -INFINITY) ? 0.f : ex2_approx(m[q] - mn);
                         m[q] = mn;
-                        pv[q] = ex2_approx(x[q] - mn);
+                        pv[q] = ex2_approx(x[q] - ((CAUSAL && mn == -INFINITY) ? 0.f : mn));
                         l[q] = fmaf(l[q], alpha[q], pv[q]);
                     } else {
                         alpha[q] = 0.f;
@@ -496,8 +505,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int q = 0; q < kN; ++q) {
                     if (q >= G) break;
-                    const float o = empty ? 0.f : acc[q] / L[q];
-                    const float lse_v = empty ? -INFINITY : (m[q] + __log2f(L[q])) * kLn2;
+                    const bool none = empty || !(L[q] > 0.f);   // no visible key in this range
+                    const float o = none ? 0.f : acc[q] / L[q];
+                    const float lse_v = none ? -INFINITY : (m[q] + __log2f(L[q])) * kLn2;
                     const size_t row = static_cast<size_t>(it.u) * G + q;
                     if (it.whole) {
                         if (p.o_stage) {
@@ -609,12 +619,16 @@ __global__ void combine_kernel(const __grid_constant__ DecodeParams p, int nctas
         for (int i = static_cast<int>(threadIdx.x); i < cnt; i += 32) mx = fmaxf(mx, p.part_lse[static_cast<size_t>(slots[i]) * kN + q]);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        // partials without a visible key carry lse = -inf and weigh 0; all of them -> empty row
+        const bool any = mx > -INFINITY;
         float sum = 0.f;
-        for (int i = static_cast<int>(threadIdx.x); i < cnt; i += 32) sum += __expf(p.part_lse[static_cast<size_t>(slots[i]) * kN + q] - mx);
+        if (any)
+            for (int i = static_cast<int>(threadIdx.x); i < cnt; i += 32) sum += __expf(p.part_lse[static_cast<size_t>(slots[i]) * kN + q] - mx);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-        const float lse_all = cnt > 0 ? mx + __logf(sum) : -INFINITY;
-        for (int i = static_cast<int>(threadIdx.x); i < cnt; i += 32) weights[i] = __expf(p.part_lse[static_cast<size_t>(slots[i]) * kN + q] - lse_all);
+        const float lse_all = (cnt > 0 && any) ? mx + __logf(sum) : -INFINITY;
+        for (int i = static_cast<int>(threadIdx.x); i < cnt; i += 32)
+            weights[i] = any ? __expf(p.part_lse[static_cast<size_t>(slots[i]) * kN + q] - lse_all) : 0.f;
         if (threadIdx.x == 0) {
             nslots = cnt;
             lse_sh = lse_all;
@@ -671,7 +685,7 @@ DecodeWs decode_ws_layout(const AttnArgs& a, bool split, int nsm)
     return w;
 }
 
-template <int D>
+template <int D, bool CAUSAL>
 int run_decode(const AttnArgs& a, bool split, void* ws, cudaStream_t st)
 {
     using C = DecodeCfg<D>;
@@ -706,6 +720,8 @@ int run_decode(const AttnArgs& a, bool split, void* ws, cudaStream_t st)
     p.G = G;
     p.Skv = a.Skv;
     p.D = D;
+    p.Sq = a.Sq > 0 ? a.Sq : 1;
+    p.causal = a.causal;
     p.c = a.scale * kLog2e;
     p.seqlens = a.seqlens;
     p.tiles_uniform = (a.Skv + kTileKV - 1) / kTileKV;
@@ -727,11 +743,11 @@ int run_decode(const AttnArgs& a, bool split, void* ws, cudaStream_t st)
         FMHA_CHECK_LAUNCH("tile_prefix_kernel");
         count_launch();
     }
-    FMHA_CHECK_CUDA(cudaFuncSetAttribute(decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes));
+    FMHA_CHECK_CUDA(cudaFuncSetAttribute(decode_kernel<D, CAUSAL>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes));
     const int grid = split ? nsm : (U < nsm ? U : nsm);
     if (grid > 0) {
         timing_mark_begin(st);
-        decode_kernel<D><<<grid, kThreads, C::kSmemBytes, st>>>(qmap, kmap, vmap, p);
+        decode_kernel<D, CAUSAL><<<grid, kThreads, C::kSmemBytes, st>>>(qmap, kmap, vmap, p);
         timing_mark_end(st);
         FMHA_CHECK_LAUNCH("decode_kernel");
         count_launch();
@@ -760,8 +776,8 @@ int launch_decode(const AttnArgs& a, int num_splits, void* ws, size_t ws_bytes, 
     const DecodeWs w = decode_ws_layout(a, split, nsm);
     if (w.total > 0 && (!ws || ws_bytes < w.total)) return set_error(FMHA_ERR_WORKSPACE, "decode: workspace too small");
     switch (a.D) {
-        case 64: return run_decode<64>(a, split, ws, st);
-        case 128: return run_decode<128>(a, split, ws, st);
+        case 64: return a.causal ? run_decode<64, true>(a, split, ws, st) : run_decode<64, false>(a, split, ws, st);
+        case 128: return a.causal ? run_decode<128, true>(a, split, ws, st) : run_decode<128, false>(a, split, ws, st);
         default: return set_error(FMHA_ERR_UNSUPPORTED, "decode path: D must be 64 or 128");
     }
 }

@@ -58,6 +58,7 @@ struct AttnArgs {
     int out_kind;            // FMHA_OUT_*
     float* out_f32;          // FP32 O destination (NVFP4 path), else NULL
     float* amax_slot;        // NVFP4 path: |O| max accumulator (uint bits), else NULL
+    int causal;              // bottom-right aligned causal mask
 };
 
 // Decode / small-group path (query rows per key/value head <= 16): swap-AB kernels.

@@ -59,6 +59,8 @@ struct PrefillParams {
     int R;          // query rows per unit = (Hq / Hkv) * Sq
     int Skv;
     int pairs;      // ceil(R / 256)
+    int Sq;         // query rows per head: row r of a unit is query r % Sq
+    int causal;     // bottom-right aligned causal mask
     float c;        // scale * log2(e)
     const int32_t* seqlens;
     void* out;
@@ -73,6 +75,32 @@ struct PrefillParams {
 __device__ __forceinline__ int unit_keys(const PrefillParams& p, int u)
 {
     return p.seqlens ? p.seqlens[u / p.Hkv] : p.Skv;
+}
+
+// Query-tile pair of a work item.  With the causal mask later rows see more keys, so the pairs of
+// each unit run from the last one down: the heaviest items start first and the light ones fill the
+// tail of the persistent grid.
+template <bool CAUSAL>
+__device__ __forceinline__ int item_pair(const PrefillParams& p, int item)
+{
+    const int i = item % p.pairs;
+    return CAUSAL ? p.pairs - 1 - i : i;
+}
+
+// Key tiles query tile q of a pair needs: none when its rows are all past R; with the causal
+// mask only those up to the last key its rows can see (row r sees keys < r % Sq + n - Sq + 1).
+template <bool CAUSAL>
+__device__ __forceinline__ int tile_count(const PrefillParams& p, int pair, int q, int n)
+{
+    const int a = pair * 2 * kTM + q * kTM;
+    if (a >= p.R || n <= 0) return 0;
+    const int T = (n + kTN - 1) / kTN;
+    if (!CAUSAL) return T;
+    const int b = min(a + kTM - 1, p.R - 1);
+    const int sa = a % p.Sq, sb = b % p.Sq;
+    const int max_s = (b - a + 1 >= p.Sq || sa > sb) ? p.Sq - 1 : sb;
+    const int lim = max_s + n - p.Sq + 1;   // keys 0 .. lim - 1 visible to some row of the tile
+    return lim <= 0 ? 0 : min(T, (lim + kTN - 1) / kTN);
 }
 
 __device__ __forceinline__ void drain_wait_p(uint64_t* bar, uint32_t parity, long long limit)
@@ -97,7 +125,7 @@ struct PRing {
     }
 };
 
-template <int D>
+template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kPThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap, const __grid_constant__ PrefillParams p)
@@ -158,8 +186,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
             for (int i = 0; i < QS; ++i) qcnt[i] = 0;
             for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
                 const int u = item / p.pairs;
-                const int r0 = (item % p.pairs) * 2 * kTM;
-                const int T = (unit_keys(p, u) + kTN - 1) / kTN;
+                const int r0 = (item_pair<CAUSAL>(p, item)) * 2 * kTM;
+                const int n = unit_keys(p, u);
+                const int T = max(tile_count<CAUSAL>(p, item_pair<CAUSAL>(p, item), 0, n), tile_count<CAUSAL>(p, item_pair<CAUSAL>(p, item), 1, n));
                 if (T == 0) continue;
                 mbar_wait(&q_empty[qr.idx], qr.phase ^ 1, wc);
                 if (!aborted(wc)) {
@@ -211,7 +240,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
             uint32_t npv[2] = {0, 0};    // PVs issued per query tile
             for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
                 const int u = item / p.pairs;
-                const int T = (unit_keys(p, u) + kTN - 1) / kTN;
+                const int n = unit_keys(p, u);
+                const int Tq[2] = {tile_count<CAUSAL>(p, item_pair<CAUSAL>(p, item), 0, n), tile_count<CAUSAL>(p, item_pair<CAUSAL>(p, item), 1, n)};
+                const int T = max(Tq[0], Tq[1]);
                 if (T == 0) continue;
                 mbar_wait(&q_full[qr.idx], qr.phase, wc);
                 tc_fence_after();
@@ -219,11 +250,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 int jq[2] = {0, 0}, jp[2] = {0, 0};
                 long long t_idle = clock64();
                 int idle_polls = 0;
-                while ((jp[0] < T || jp[1] < T) && !aborted(wc)) {
+                while ((jp[0] < Tq[0] || jp[1] < Tq[1]) && !aborted(wc)) {
                     bool did = false;
 #pragma unroll
                     for (int q = 0; q < 2; ++q) {
-                        if (jq[q] < T) {
+                        if (jq[q] < Tq[q]) {
                             const uint32_t g = gtile + jq[q];
                             bool ok = mbar_test(&k_full[g % S], (g / S) & 1);
                             if (ok && nqk[q] > 0) ok = mbar_test(&s_free[q], (nqk[q] - 1) & 1);
@@ -243,7 +274,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
                                 mma_commit(&s_full[q]);
                                 ++nqk[q];
                                 ++jq[q];
-                                if (jq[q] <= jq[q ^ 1]) mma_commit(&k_empty[g % S]);   // both tiles read K_g
+                                // the last of the query tiles that need K_g releases it
+                                if (Tq[q ^ 1] <= jq[q] - 1 || jq[q ^ 1] >= jq[q]) mma_commit(&k_empty[g % S]);
                                 did = true;
                             }
                         }
@@ -262,7 +294,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                                 mma_commit(&o_done[q]);
                                 ++npv[q];
                                 ++jp[q];
-                                if (jp[q] <= jp[q ^ 1]) mma_commit(&v_empty[g % S]);   // both tiles read V_g
+                                if (Tq[q ^ 1] <= jp[q] - 1 || jp[q ^ 1] >= jp[q]) mma_commit(&v_empty[g % S]);
                                 did = true;
                             }
                         }
@@ -294,12 +326,15 @@ __global__ void __launch_bounds__(kPThreads, 1)
         const uint32_t tS = tmem + lane_base + q * 128;
         const uint32_t tP = tmem + lane_base + C::kColP + q * C::kPStride;
         const uint32_t tO = tmem + lane_base + C::kColO + q * D;
-        uint32_t gt = 0;   // tiles processed by this warpgroup over the kernel's life (= K/V ring position)
+        uint32_t gt = 0;     // tiles processed by this warpgroup over the kernel's life (S/P/O rings)
+        uint32_t gring = 0;  // K/V ring position of the current item's first tile
         for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
             const int u = item / p.pairs;
-            const int row = (item % p.pairs) * 2 * kTM + q * kTM + row_in_tile;
+            const int row = (item_pair<CAUSAL>(p, item)) * 2 * kTM + q * kTM + row_in_tile;
             const int n = unit_keys(p, u);
-            const int T = (n + kTN - 1) / kTN;
+            const int T = tile_count<CAUSAL>(p, item_pair<CAUSAL>(p, item), q, n);
+            // keys this row sees: 0 .. lim - 1
+            const int lim = CAUSAL ? min(n, (row < p.R ? row : 0) % p.Sq + n - p.Sq + 1) : n;
             float m_run = -INFINITY, l = 0.f;
             for (int j = 0; j < T; ++j, ++gt) {
                 mbar_wait(&s_full[q], gt & 1, wc);
@@ -311,10 +346,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 tmem_ld_wait();
                 tc_fence_before();
                 mbar_arrive(&s_free[q]);
-                if ((j + 1) * kTN > n) {
+                if ((j + 1) * kTN > lim) {
 #pragma unroll
                     for (int i = 0; i < kTN; ++i)
-                        if (j * kTN + i >= n) s[i] = -INFINITY;
+                        if (j * kTN + i >= lim) s[i] = -INFINITY;
                 }
                 float mx[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
@@ -335,7 +370,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 }
                 // p = 2^(s*c - m) with packed FP32x2 scale-subtract and sums
                 const uint64_t cc = f32x2(p.c, p.c);
-                const uint64_t nm = f32x2(-m_run, -m_run);
+                // causal: a row with no visible key yet keeps m = -inf (no -inf - -inf = NaN)
+                const float mu = (CAUSAL && m_run == -INFINITY) ? 0.f : -m_run;
+                const uint64_t nm = f32x2(mu, mu);
                 uint32_t pk[kTN / 2];
                 uint64_t ls[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
@@ -372,9 +409,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 // P = 0 does not cancel NaN in the MMA: zero those V rows of a partial tile.  Both
                 // warpgroups write the same zeros; each makes them visible before its own p_full.
                 if (p.seqlens && (j + 1) * kTN > n) {
-                    mbar_wait(&v_full[gt % S], (gt / S) & 1, wc);
+                    const uint32_t gr = gring + j;   // K/V ring position of this tile
+                    mbar_wait(&v_full[gr % S], (gr / S) & 1, wc);
                     for (int r = n - j * kTN + row_in_tile; r < kTN; r += kTM) {
-                        uint8_t* rowp = smem + C::kOffV + (gt % S) * C::kKVBytes + r * 128;
+                        uint8_t* rowp = smem + C::kOffV + (gr % S) * C::kKVBytes + r * 128;
 #pragma unroll
                         for (int a = 0; a < C::kAtoms; ++a)
 #pragma unroll
@@ -397,9 +435,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
             }
             // The TMEM loads below are warp-collective: every lane executes them; only the stores
             // are predicated on the row existing.
+            gring += max(tile_count<CAUSAL>(p, item_pair<CAUSAL>(p, item), 0, n), tile_count<CAUSAL>(p, item_pair<CAUSAL>(p, item), 1, n));
             const bool store = row < p.R && !aborted(wc);
             const size_t orow = static_cast<size_t>(u) * p.R + (row < p.R ? row : 0);
-            const float inv_l = T > 0 ? 1.f / l : 0.f;
+            const bool none = !(l > 0.f);   // no visible key: O = 0, LSE = -inf
+            const float inv_l = none ? 0.f : 1.f / l;
             float amax = 0.f;
             __syncwarp();
 #pragma unroll
@@ -438,7 +478,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     }
                 }
             }
-            if (store && p.lse) p.lse[orow] = T > 0 ? (m_run + __log2f(l)) * kLn2P : -INFINITY;
+            if (store && p.lse) p.lse[orow] = none ? -INFINITY : (m_run + __log2f(l)) * kLn2P;
             if (store && p.amax_bits && amax > 0.f) atomicMax(p.amax_bits, __float_as_uint(amax));
         }
     }
@@ -449,7 +489,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
 }
 
 // ---- host side ------------------------------------------------------------------------------------
-template <int D>
+template <int D, bool CAUSAL>
 int run_prefill(const AttnArgs& a, void* ws, cudaStream_t st)
 {
     using C = PrefillCfg<D>;
@@ -480,6 +520,8 @@ int run_prefill(const AttnArgs& a, void* ws, cudaStream_t st)
     p.R = R;
     p.Skv = a.Skv;
     p.pairs = (R + 2 * kTM - 1) / (2 * kTM);
+    p.Sq = a.Sq > 0 ? a.Sq : 1;
+    p.causal = a.causal;
     p.c = a.scale * kLog2eP;
     p.seqlens = a.seqlens;
     const bool nvfp4 = a.out_kind == FMHA_OUT_NVFP4;
@@ -492,10 +534,10 @@ int run_prefill(const AttnArgs& a, void* ws, cudaStream_t st)
     p.limit = wait_limit();
     const long long items = static_cast<long long>(U) * p.pairs;
     const int grid = static_cast<int>(items < nsm ? items : nsm);
-    FMHA_CHECK_CUDA(cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes));
+    FMHA_CHECK_CUDA(cudaFuncSetAttribute(prefill_kernel<D, CAUSAL>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes));
     if (grid > 0) {
         timing_mark_begin(st);
-        prefill_kernel<D><<<grid, kPThreads, C::kSmemBytes, st>>>(qmap, kmap, vmap, p);
+        prefill_kernel<D, CAUSAL><<<grid, kPThreads, C::kSmemBytes, st>>>(qmap, kmap, vmap, p);
         timing_mark_end(st);
         FMHA_CHECK_LAUNCH("prefill_kernel");
         count_launch();
@@ -517,8 +559,8 @@ int launch_prefill(const AttnArgs& a, void* ws, size_t ws_bytes, cudaStream_t st
 {
     if (ws_bytes < prefill_workspace_bytes(a)) return set_error(FMHA_ERR_WORKSPACE, "row-tile path: workspace too small");
     switch (a.D) {
-        case 64: return run_prefill<64>(a, ws, st);
-        case 128: return run_prefill<128>(a, ws, st);
+        case 64: return a.causal ? run_prefill<64, true>(a, ws, st) : run_prefill<64, false>(a, ws, st);
+        case 128: return a.causal ? run_prefill<128, true>(a, ws, st) : run_prefill<128, false>(a, ws, st);
         default: return set_error(FMHA_ERR_UNSUPPORTED, "row-tile path: D must be 64 or 128 (D = 512 not built yet)");
     }
 }

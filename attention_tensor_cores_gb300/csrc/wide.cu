@@ -53,6 +53,8 @@ struct WideParams {
     int Hkv;
     int R;          // query rows per (b, kv-head) = (Hq / Hkv) * Sq
     int Skv;
+    int Sq;         // query rows per head: row r of a (b, kv-head) is query r % Sq
+    int causal;     // bottom-right aligned causal mask
     float c;
     const int32_t* seqlens;
     const int32_t* prefix;   // [U+1] tile prefix (ragged), else NULL
@@ -341,6 +343,8 @@ __global__ void __launch_bounds__(kWThreads, 1)
         while (sched.next(it)) {
             const int hu = wunit_head(p, it.u);
             const int row = (it.u % p.row_tiles) * kWRows + row_in_tile;
+            // keys this row sees: 0 .. lim - 1
+            const int lim = p.causal ? min(it.n, (row < p.R ? row : 0) % p.Sq + it.n - p.Sq + 1) : it.n;
             float m_run = -INFINITY, l = 0.f;
             for (int t = it.t0; t < it.t1; ++t, ++g) {
                 mbar_wait(&s_full[sr.idx], sr.phase, wc);
@@ -352,10 +356,10 @@ __global__ void __launch_bounds__(kWThreads, 1)
                 mbar_arrive(&s_empty[sr.idx]);
                 sr.advance();
                 const bool partial = (t + 1) * kWKeys > it.n;
-                if (partial) {
+                if ((t + 1) * kWKeys > lim) {
 #pragma unroll
                     for (int i = 0; i < kWKeys; ++i)
-                        if (t * kWKeys + i >= it.n) s[i] = -INFINITY;
+                        if (t * kWKeys + i >= lim) s[i] = -INFINITY;
                 }
                 float mx = s[0];
 #pragma unroll
@@ -367,12 +371,13 @@ __global__ void __launch_bounds__(kWThreads, 1)
                     alpha = ex2_approx(m_run - mt);
                     m_run = mt;
                 }
+                const float mu = m_run == -INFINITY ? 0.f : -m_run;   // a row with no visible key yet
                 uint32_t pk[16];
                 float sum = 0.f;
 #pragma unroll
                 for (int i = 0; i < kWKeys; i += 2) {
-                    const float p0 = ex2_approx(fmaf(s[i], p.c, -m_run));
-                    const float p1 = ex2_approx(fmaf(s[i + 1], p.c, -m_run));
+                    const float p0 = ex2_approx(fmaf(s[i], p.c, mu));
+                    const float p1 = ex2_approx(fmaf(s[i + 1], p.c, mu));
                     sum += p0 + p1;
                     pk[i >> 1] = pack_bf16x2(p0, p1);
                 }
@@ -414,8 +419,9 @@ __global__ void __launch_bounds__(kWThreads, 1)
             tc_fence_after();
             const bool store = row < p.R && !aborted(wc);
             const int rr = row < p.R ? row : 0;
-            const float inv_l = 1.f / l;
-            const float lse_v = (m_run + __log2f(l)) * kLn2W;
+            const bool none = !(l > 0.f);   // no visible key in this range: O = 0, LSE = -inf
+            const float inv_l = none ? 0.f : 1.f / l;
+            const float lse_v = none ? -INFINITY : (m_run + __log2f(l)) * kLn2W;
             float amax = 0.f;
             __syncwarp();
             for (int c4 = 0; c4 < kWHalf / 32; ++c4) {
@@ -549,18 +555,21 @@ __global__ void __launch_bounds__(32 * kCombRows) wide_combine_kernel(const __gr
     for (int i = lane; i < ns; i += 32) mx = fmaxf(mx, p.part_lse[static_cast<size_t>(slots[i]) * kWRows + r]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    // partials without a visible key carry lse = -inf and weigh 0; all of them -> empty row
+    const bool any = mx > -INFINITY;
     float sum = 0.f;
-    for (int i = lane; i < ns; i += 32) sum += __expf(p.part_lse[static_cast<size_t>(slots[i]) * kWRows + r] - mx);
+    if (any)
+        for (int i = lane; i < ns; i += 32) sum += __expf(p.part_lse[static_cast<size_t>(slots[i]) * kWRows + r] - mx);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    const float lse_v = ns > 0 ? mx + __logf(sum) : -INFINITY;
+    const float lse_v = (ns > 0 && any) ? mx + __logf(sum) : -INFINITY;
     // weighted sum of the partial rows, 16 columns per lane
     float acc[16];
 #pragma unroll
     for (int k = 0; k < 16; ++k) acc[k] = 0.f;
     for (int c0 = 0; c0 < ns; c0 += 32) {
         const int mine = c0 + lane;
-        const float w = mine < ns ? __expf(p.part_lse[static_cast<size_t>(slots[mine]) * kWRows + r] - lse_v) : 0.f;
+        const float w = (mine < ns && any) ? __expf(p.part_lse[static_cast<size_t>(slots[mine]) * kWRows + r] - lse_v) : 0.f;
         const int cnt = min(32, ns - c0);
         for (int j = 0; j < cnt; ++j) {
             const float wj = __shfl_sync(0xffffffffu, w, j);
@@ -674,6 +683,8 @@ int launch_wide(const AttnArgs& a, void* ws, size_t ws_bytes, cudaStream_t st)
     p.R = R;
     p.Skv = a.Skv;
     p.c = a.scale * kLog2eW;
+    p.Sq = a.Sq > 0 ? a.Sq : 1;
+    p.causal = a.causal;
     p.seqlens = a.seqlens;
     p.prefix = a.seqlens ? reinterpret_cast<const int32_t*>(base + w.prefix_off) : nullptr;
     p.tiles_uniform = (a.Skv + kWKeys - 1) / kWKeys;

@@ -133,9 +133,10 @@ def traffic_for(kernel: str, src: str, launches_per_step: int = 1):
 class Case:
     """Device inputs/outputs of one workload and the library call that processes them."""
 
-    def __init__(self, F, w, num_splits=0, pad_fill=None):
+    def __init__(self, F, w, num_splits=0, pad_fill=None, causal=False):
         import torch
         self.F, self.w = F, w
+        self.causal = causal
         self.q, self.k, self.v, self.sl = w.make("cuda", pad_fill=pad_fill)
         B, Hq, Sq, D = self.q.shape
         self.n_out = B * Hq * Sq * D
@@ -149,10 +150,10 @@ class Case:
             dt = torch.bfloat16 if w.out_kind == "bf16" else torch.float32
             self.out = torch.empty(B, Hq, Sq, D, dtype=dt, device="cuda")
         self.lse = torch.empty(B, Hq, Sq, dtype=torch.float32, device="cuda")
-        opts = F.make_opts(kind, self.sl, num_splits, None, self.scales, self.ts, None)
+        opts = F.make_opts(kind, self.sl, num_splits, None, self.scales, self.ts, None, causal)
         wsb = F.fmha_workspace_size(B, Hq, w.Hkv, Sq, w.Skv, D, opts)
         self.ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device="cuda") if wsb else None
-        self.opts = F.make_opts(kind, self.sl, num_splits, self.ws, self.scales, self.ts, None)
+        self.opts = F.make_opts(kind, self.sl, num_splits, self.ws, self.scales, self.ts, None, causal)
 
     def call(self, q=None, k=None, v=None):
         self.F.fmha_fwd_ex(self.q if q is None else q, self.k if k is None else k, self.v if v is None else v,
@@ -307,17 +308,20 @@ def aggregate_rate(units_per_rank_per_step: float, steps: int, world: int, regio
     return world * steps * units_per_rank_per_step / (region_ms_max / 1e3)
 
 
-def _workload_entry(F, w, idx, steps, warmup, peaks):
+def _workload_entry(F, w, idx, steps, warmup, peaks, causal=False):
     """Timing + roofline of one extra workload (rank 0 only)."""
     import torch
-    case = Case(F, w, num_splits=0)
+    case = Case(F, w, num_splits=0, causal=causal)
     r = time_case(F, case, steps, warmup)
     step_ms = r["region_ms"] / steps
     kern_ms = statistics.mean(r["kernel_ms"])
     e = {"workload": w.name, "ms_per_step": step_ms, "kernel_ms": kern_ms, "gpu_launches_per_step": r["launches"] / steps}
     if idx == 2:   # prefill: tensor-bound
-        tf = w.flops() / (step_ms / 1e3) / 1e12
-        ach = w.flops() / (kern_ms / 1e3) / 1e12
+        # causal (Sq = Skv): query i sees i + 1 keys, so the contractions do 4 D sum_i (i + 1) FLOP per head
+        flops = 4 * w.D * w.B * w.Hq * (w.Sq * (w.Sq + 1) // 2) if causal else w.flops()
+        tf = flops / (step_ms / 1e3) / 1e12
+        ach = flops / (kern_ms / 1e3) / 1e12
+        e["flops"] = flops
         e.update({"value": tf, "unit": "TFLOP/s",
                   "roofline": {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                                "frac": ach / peaks["bf16_tflops"], "traffic": None}})
@@ -381,6 +385,11 @@ def run_ours(args, rank, world, local):
                 extra[f"c{idx + 1}"] = _workload_entry(F, wl[idx], idx, min(args.steps, 10), args.warmup, peaks)
             except F.FmhaError as ex:
                 extra[f"c{idx + 1}"] = {"workload": wl[idx].name, "unsupported": str(ex)}
+        try:   # the prefill workload with the causal mask
+            extra["c3_causal"] = _workload_entry(F, wl[2], 2, min(args.steps, 10), args.warmup, peaks, causal=True)
+            extra["c3_causal"]["workload"] = wl[2].name.replace("non-causal", "causal")
+        except F.FmhaError as ex:
+            extra["c3_causal"] = {"workload": "causal prefill", "unsupported": str(ex)}
     cpu = cpu_baseline(w, "GB/s") if (rank == 0 and world == 1) else None
     if dist is not None:
         dist.barrier()

@@ -66,6 +66,9 @@ typedef struct {
     uint8_t* out_scales;      /* NVFP4: E4M3 block scales [B,Hq,Sq,D/16] */
     float* out_tensor_scale;  /* NVFP4: device float[1], the per-tensor scale s_g */
     float* out_f32;           /* optional, NVFP4 only: the FP32 O that was quantised */
+    int causal;               /* 1: bottom-right aligned causal mask: with n keys, query i of Sq sees
+                                 keys 0 .. i + n - Sq (a query that sees none gets O = 0,
+                                 LSE = -inf); 0 = all keys */
 } fmha_opts;
 
 /*

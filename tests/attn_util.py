@@ -16,13 +16,13 @@ O_MEAN = 2e-3
 LSE_REL = 1e-3
 
 
-def run_attention(F, q, k, v, scale, out_kind="bf16", seqlens=None, num_splits=None, want_f32=False):
+def run_attention(F, q, k, v, scale, out_kind="bf16", seqlens=None, num_splits=None, want_f32=False, causal=False):
     """Calls fmha_fwd (no options) or fmha_fwd_ex; returns dict of host numpy results."""
     B, Hq, Sq, D = q.shape
     Hkv, Skv = k.shape[1], k.shape[2]
     lse = torch.full((B, Hq, Sq), float("nan"), dtype=torch.float32, device="cuda")
     res = {}
-    if out_kind == "bf16" and seqlens is None and num_splits is None:
+    if out_kind == "bf16" and seqlens is None and num_splits is None and not causal:
         out = torch.full((B, Hq, Sq, D), float("nan"), dtype=torch.bfloat16, device="cuda")
         F.fmha_fwd(q, k, v, out, lse, scale)
         torch.cuda.synchronize()
@@ -40,10 +40,10 @@ def run_attention(F, q, k, v, scale, out_kind="bf16", seqlens=None, num_splits=N
             out = torch.full((B, Hq, Sq, D), float("nan"), dtype=dt, device="cuda")
             scales = ts = f32 = None
         ns = 0 if num_splits is None else num_splits
-        opts = F.make_opts(kind, seqlens, ns, None, scales, ts, f32)
+        opts = F.make_opts(kind, seqlens, ns, None, scales, ts, f32, causal)
         wsb = F.fmha_workspace_size(B, Hq, Hkv, Sq, Skv, D, opts)
         ws = torch.empty(max(wsb, 1), dtype=torch.uint8, device="cuda") if wsb else None
-        opts = F.make_opts(kind, seqlens, ns, ws, scales, ts, f32)
+        opts = F.make_opts(kind, seqlens, ns, ws, scales, ts, f32, causal)
         F.fmha_fwd_ex(q, k, v, out, lse, scale, opts)
         torch.cuda.synchronize()
         if out_kind == "nvfp4":
@@ -73,7 +73,7 @@ def check_o_lse(o, lse, o_ref, lse_ref, what=""):
     return float(err.max()), float(err.mean())
 
 
-def oracle_rows(w: inputs.Workload, rows):
+def oracle_rows(w: inputs.Workload, rows, causal: bool = False):
     """FP64 oracle for flat query rows of workload `w`, from regenerated slices only."""
     sl = w.seqlens()
     g = w.Hq // w.Hkv
@@ -94,7 +94,17 @@ def oracle_rows(w: inputs.Workload, rows):
             o[i] = 0.0
             lse[i] = -math.inf
             continue
-        oi, li = oracle.attention(qs[i].reshape(1, 1, 1, w.D), kk.reshape(1, 1, n, w.D), vv.reshape(1, 1, n, w.D), w.scale)
+        s_idx = r % w.Sq
+        if causal:   # bottom-right aligned: query s of Sq sees keys 0 .. s + n - Sq
+            n_vis = max(0, min(n, s_idx + n - w.Sq + 1))
+            if n_vis == 0:
+                o[i] = 0.0
+                lse[i] = -math.inf
+                continue
+        else:
+            n_vis = n
+        oi, li = oracle.attention(qs[i].reshape(1, 1, 1, w.D), kk[:n_vis].reshape(1, 1, n_vis, w.D),
+                                  vv[:n_vis].reshape(1, 1, n_vis, w.D), w.scale)
         o[i] = oi[0]
         lse[i] = li[0]
     return o, lse
