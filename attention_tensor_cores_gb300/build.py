@@ -35,7 +35,7 @@ def _headers() -> list[str]:
 
 # Per-file register ceilings: the row-tile kernel runs 10 warps per SM, so up to 200 registers per
 # thread fit, and the softmax keeps a 128-column row of S in registers.
-PER_FILE_FLAGS = {"prefill.cu": ["-maxrregcount=200"]}
+PER_FILE_FLAGS = {}
 
 
 def _compile(src: str, obj: str, extra: list[str]) -> tuple[str, str]:

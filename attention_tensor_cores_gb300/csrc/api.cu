@@ -212,11 +212,12 @@ static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 static bool use_decode_path(int Hq, int Hkv, int Sq) { return static_cast<long long>(Hq / Hkv) * Sq <= 16; }
 
 // Workspace: [path scratch][NVFP4 amax word].  The path scratch of the decode path holds the
-// tile prefix, the split partials and (NVFP4 without out_f32) the FP32 staging of O.
+// tile prefix, the split partials and (NVFP4 without out_f32) the FP32 staging of O; that of the
+// row-tile path the work-item counter (causal or ragged) and the FP32 staging of O, last.
 static size_t workspace_bytes(const AttnArgs& a, int num_splits)
 {
     size_t w = a.D == 512 ? wide_workspace_bytes(a)
-               : use_decode_path(a.Hq, a.Hkv, a.Sq) ? decode_workspace_bytes(a, num_splits) : prefill_workspace_bytes(a);
+               : use_decode_path(a.Hq, a.Hkv, a.Sq) ? decode_workspace_bytes(a, num_splits) : prefill_workspace_bytes(a, num_splits);
     w = align256(w);
     if (a.out_kind == FMHA_OUT_NVFP4) w += 256;
     return w;
@@ -291,7 +292,8 @@ int fmha_fwd_ex(const void* q, const void* k, const void* v, void* out, float* l
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     AttnArgs a = make_args(q, k, v, out, lse, B, Hq, Hkv, Sq, Skv, D, scale, opts);
     void* ws = opts ? opts->workspace : nullptr;
-    // automatic split-KV when the caller supplied a workspace, whole units otherwise
+    // automatic split-KV (decode) or work-item counter (row-tile) when the caller supplied a
+    // workspace; whole units in a fixed order otherwise
     const int num_splits = (opts && (opts->num_splits != 0 || ws)) ? opts->num_splits : 1;
     const size_t ws_bytes = opts ? opts->workspace_bytes : 0;
     const size_t need = workspace_bytes(a, num_splits);
@@ -310,7 +312,7 @@ int fmha_fwd_ex(const void* q, const void* k, const void* v, void* out, float* l
     else if (use_decode_path(Hq, Hkv, Sq))
         rc = launch_decode(a, num_splits, ws, path_bytes, st);
     else
-        rc = launch_prefill(a, ws, path_bytes, st);
+        rc = launch_prefill(a, num_splits, ws, path_bytes, st);
     if (rc) return rc;
     if (nvfp4) {
         // the FP32 O the quantiser reads: caller's out_f32, else the staging area of the workspace

@@ -65,9 +65,10 @@ struct AttnArgs {
 size_t decode_workspace_bytes(const AttnArgs& a, int splits_mode);
 int launch_decode(const AttnArgs& a, int num_splits, void* ws, size_t ws_bytes, cudaStream_t st);
 
-// Row-tile path (128 query rows per tile): prefill and wide-head decode.
-size_t prefill_workspace_bytes(const AttnArgs& a);
-int launch_prefill(const AttnArgs& a, void* ws, size_t ws_bytes, cudaStream_t st);
+// Row-tile path (128 query rows per tile).  sched_mode != 1 (a caller workspace is in use): causal
+// and ragged problems take their work items from a counter in the workspace.
+size_t prefill_workspace_bytes(const AttnArgs& a, int sched_mode);
+int launch_prefill(const AttnArgs& a, int sched_mode, void* ws, size_t ws_bytes, cudaStream_t st);
 
 // Wide-head path (D = 512): CTA pairs split the value columns, stream-K over 32-key tiles.
 size_t wide_workspace_bytes(const AttnArgs& a);

@@ -18,6 +18,12 @@
 //    stays <= 256, and the final O / l and LSE use the same m, so the result is exact.
 //  * One MMA thread polls the readiness of every pending QK / PV (non-blocking mbarrier tests)
 //    and issues whichever can go, so a slow softmax of one tile never blocks the other's MMAs.
+//  * Work items (unit, query-tile pair) come from a global atomic counter when the caller gives a
+//    workspace (causal and ragged problems, whose items differ in size), else in a fixed strided
+//    order.  The TMA warp claims the next item once it has issued the loads of the current one and
+//    hands item numbers to the MMA and softmax warps through a small shared-memory ring.  Causal
+//    items are numbered heaviest first within groups of units whose K/V fit comfortably in L2, so
+//    the greedy claim order approximates longest-job-first and the light items fill the tail.
 //  * Every wait is bounded (clock64 limit); a timeout sets the device status word and the CTA
 //    drains without issuing more copies or MMAs.
 #include <cuda_runtime.h>
@@ -30,10 +36,23 @@ namespace {
 
 constexpr int kTM = 128;          // query rows per tile (MMA M)
 constexpr int kTN = 128;          // keys per tile
-constexpr int kPThreads = 320;    // 2 softmax warpgroups + TMA warp + MMA warp
+// Threads: 2 softmax warpgroups + TMA warp + MMA warp.  The counter-order kernel adds two idle warps
+// so that its third warpgroup is whole (setmaxnreg acts on whole warpgroups) and splits registers:
+// the launch gives every thread 168 (384 x 168 = 64512 of the SM's 65536); the third warpgroup drops
+// to kRegsCtl and the softmax warpgroups rise to kRegsSoftmax, which holds a whole row of S (128
+// floats) and its packed P without spilling: 2*128*208 + 128*88 = 64512, and on each SM quarter
+// (warps w, w+4, w+8) the control warp frees exactly what its two softmax warps take.  The
+// fixed-order kernel keeps 10 warps at 168 registers, which measured faster for dense problems.
+template <bool DYN>
+constexpr int prefill_threads() { return DYN ? 384 : 320; }
+constexpr uint32_t kRegsSoftmax = 208;
+constexpr uint32_t kRegsCtl = 88;
+static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsCtl <= prefill_threads<true>() * 168, "register split exceeds the launch allocation");
+static_assert(2 * kRegsSoftmax + kRegsCtl <= 512, "register split exceeds an SM quarter");
 constexpr float kLog2eP = 1.4426950408889634f;
 constexpr float kLn2P = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f;
+constexpr int kItemSlots = 4;     // work-item ring between the TMA warp and the consumers
 
 template <int D>
 struct PrefillCfg {
@@ -61,6 +80,8 @@ struct PrefillParams {
     int pairs;      // ceil(R / 256)
     int Sq;         // query rows per head: row r of a unit is query r % Sq
     int causal;     // bottom-right aligned causal mask
+    int group;      // causal item order: units per group
+    int* sched;     // global work-item counter (zeroed before the launch), NULL = fixed order
     float c;        // scale * log2(e)
     const int32_t* seqlens;
     void* out;
@@ -77,14 +98,24 @@ __device__ __forceinline__ int unit_keys(const PrefillParams& p, int u)
     return p.seqlens ? p.seqlens[u / p.Hkv] : p.Skv;
 }
 
-// Query-tile pair of a work item.  With the causal mask later rows see more keys, so the pairs of
-// each unit run from the last one down: the heaviest items start first and the light ones fill the
-// tail of the persistent grid.
+// Unit and query-tile pair of work item r.  Without the mask: unit-major.  With it, later rows see
+// more keys, so items go group by group (p.group units at a time) and within a group from the last
+// pair of every unit down to the first: heaviest first, units of a group side by side.
 template <bool CAUSAL>
-__device__ __forceinline__ int item_pair(const PrefillParams& p, int item)
+__device__ __forceinline__ void item_coords(const PrefillParams& p, int r, int& u, int& pair)
 {
-    const int i = item % p.pairs;
-    return CAUSAL ? p.pairs - 1 - i : i;
+    if (!CAUSAL) {
+        u = r / p.pairs;
+        pair = r - u * p.pairs;
+        return;
+    }
+    const int per_group = p.group * p.pairs;
+    const int g = r / per_group;
+    const int rr = r - g * per_group;
+    const int gsz = min(p.group, p.U - g * p.group);
+    const int level = rr / gsz;
+    u = g * p.group + (rr - level * gsz);
+    pair = p.pairs - 1 - level;
 }
 
 // Key tiles query tile q of a pair needs: none when its rows are all past R; with the causal
@@ -125,8 +156,8 @@ struct PRing {
     }
 };
 
-template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(kPThreads, 1)
+template <int D, bool CAUSAL, bool DYN>
+__global__ void __launch_bounds__(prefill_threads<DYN>(), 1)
     prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap, const __grid_constant__ PrefillParams p)
 {
@@ -138,6 +169,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
 
     __shared__ uint64_t q_full[QS], q_empty[QS], k_full[S], k_empty[S], v_full[S], v_empty[S];
     __shared__ uint64_t s_full[2], s_free[2], p_full[2], o_done[2], mma_done;
+    __shared__ uint64_t item_full[kItemSlots], item_empty[kItemSlots];
+    __shared__ int item_q[kItemSlots];
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
 
@@ -162,6 +195,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
             mbar_init(&o_done[i], 1);
         }
         mbar_init(&mma_done, 1);
+        for (int i = 0; i < kItemSlots; ++i) {
+            mbar_init(&item_full[i], 1);
+            mbar_init(&item_empty[i], 1 + 8);   // the MMA thread and one lane of each softmax warp
+        }
         fence_barrier_init();
     }
     if (warp == 9) {
@@ -174,150 +211,190 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const uint32_t tmem = tmem_slot;
     const int n_items = p.U * p.pairs;
 
-    if (warp == 8) {
-        // ------------------------------------------------ TMA producer
-        if (lane_id() == 0) {
-            tma_prefetch_desc(&qmap);
-            tma_prefetch_desc(&kmap);
-            tma_prefetch_desc(&vmap);
-            PRing qr(QS), kr(S), vr(S);
-            uint32_t kcnt[S], vcnt[S], qcnt[QS];
-            for (int i = 0; i < S; ++i) kcnt[i] = vcnt[i] = 0;
-            for (int i = 0; i < QS; ++i) qcnt[i] = 0;
-            for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-                const int u = item / p.pairs;
-                const int r0 = (item_pair<CAUSAL>(p, item)) * 2 * kTM;
-                const int n = unit_keys(p, u);
-                const int T = max(tile_count<CAUSAL>(p, item_pair<CAUSAL>(p, item), 0, n), tile_count<CAUSAL>(p, item_pair<CAUSAL>(p, item), 1, n));
-                if (T == 0) continue;
-                mbar_wait(&q_empty[qr.idx], qr.phase ^ 1, wc);
-                if (!aborted(wc)) {
-                    uint8_t* dst = smem + C::kOffQ + qr.idx * C::kQBytes;
-                    mbar_arrive_expect_tx(&q_full[qr.idx], C::kQBytes);
-                    for (int q = 0; q < 2; ++q)
-                        for (int a = 0; a < C::kAtoms; ++a)
-                            tma_load_3d(dst + q * C::kQTileBytes + a * (kTM * 128), &qmap, &q_full[qr.idx], a * 64,
-                                        r0 + q * kTM, u);
-                    ++qcnt[qr.idx];
-                }
-                qr.advance();
-                for (int t = 0; t < T; ++t) {
-                    mbar_wait(&k_empty[kr.idx], kr.phase ^ 1, wc);
-                    if (!aborted(wc)) {
-                        uint8_t* dst = smem + C::kOffK + kr.idx * C::kKVBytes;
-                        mbar_arrive_expect_tx(&k_full[kr.idx], C::kKVBytes);
-                        for (int a = 0; a < C::kAtoms; ++a)
-                            tma_load_3d(dst + a * (kTN * 128), &kmap, &k_full[kr.idx], a * 64, t * kTN, u);
-                        ++kcnt[kr.idx];
+    // Each setmaxnreg dominates only its own role's code (the register budget of code after a join
+    // would be the smaller one) and is executed by whole warpgroups.
+    if (warp >= 8) {
+        if constexpr (DYN) setmaxnreg_dec<kRegsCtl>();
+        if (warp == 8) {
+            // ------------------------------------------------ TMA producer
+            if (lane_id() == 0) {
+                tma_prefetch_desc(&qmap);
+                tma_prefetch_desc(&kmap);
+                tma_prefetch_desc(&vmap);
+                PRing qr(QS), kr(S), vr(S);
+                uint32_t kcnt[S], vcnt[S], qcnt[QS];
+                for (int i = 0; i < S; ++i) kcnt[i] = vcnt[i] = 0;
+                for (int i = 0; i < QS; ++i) qcnt[i] = 0;
+                PRing ir(kItemSlots);
+                int item = DYN ? atomicAdd(p.sched, 1) : static_cast<int>(blockIdx.x);
+                for (;;) {
+                    const bool more = item < n_items;
+                    if constexpr (DYN) {
+                        // hand the item (or the end mark) to the MMA and softmax warps
+                        if (!mbar_wait(&item_empty[ir.idx], ir.phase ^ 1, wc)) break;
+                        item_q[ir.idx] = more ? item : -1;
+                        mbar_arrive(&item_full[ir.idx]);
+                        ir.advance();
                     }
-                    kr.advance();
-                    mbar_wait(&v_empty[vr.idx], vr.phase ^ 1, wc);
-                    if (!aborted(wc)) {
-                        uint8_t* dst = smem + C::kOffV + vr.idx * C::kKVBytes;
-                        mbar_arrive_expect_tx(&v_full[vr.idx], C::kKVBytes);
-                        for (int a = 0; a < C::kAtoms; ++a)
-                            tma_load_3d(dst + a * (kTN * 128), &vmap, &v_full[vr.idx], a * 64, t * kTN, u);
-                        ++vcnt[vr.idx];
+                    if (!more) break;
+                    int u, pair;
+                    item_coords<CAUSAL>(p, item, u, pair);
+                    const int r0 = pair * 2 * kTM;
+                    const int n = unit_keys(p, u);
+                    const int T = max(tile_count<CAUSAL>(p, pair, 0, n), tile_count<CAUSAL>(p, pair, 1, n));
+                    // the next item is claimed once this one's loads are issued, so a CTA takes new
+                    // work only shortly before it runs out
+                    const int next = DYN ? -1 : item + static_cast<int>(gridDim.x);
+                    if (T == 0) {
+                        item = DYN ? atomicAdd(p.sched, 1) : next;
+                        continue;
                     }
-                    vr.advance();
+                    mbar_wait(&q_empty[qr.idx], qr.phase ^ 1, wc);
+                    if (!aborted(wc)) {
+                        uint8_t* dst = smem + C::kOffQ + qr.idx * C::kQBytes;
+                        mbar_arrive_expect_tx(&q_full[qr.idx], C::kQBytes);
+                        for (int q = 0; q < 2; ++q)
+                            for (int a = 0; a < C::kAtoms; ++a)
+                                tma_load_3d(dst + q * C::kQTileBytes + a * (kTM * 128), &qmap, &q_full[qr.idx], a * 64,
+                                            r0 + q * kTM, u);
+                        ++qcnt[qr.idx];
+                    }
+                    qr.advance();
+                    for (int t = 0; t < T; ++t) {
+                        mbar_wait(&k_empty[kr.idx], kr.phase ^ 1, wc);
+                        if (!aborted(wc)) {
+                            uint8_t* dst = smem + C::kOffK + kr.idx * C::kKVBytes;
+                            mbar_arrive_expect_tx(&k_full[kr.idx], C::kKVBytes);
+                            for (int a = 0; a < C::kAtoms; ++a)
+                                tma_load_3d(dst + a * (kTN * 128), &kmap, &k_full[kr.idx], a * 64, t * kTN, u);
+                            ++kcnt[kr.idx];
+                        }
+                        kr.advance();
+                        mbar_wait(&v_empty[vr.idx], vr.phase ^ 1, wc);
+                        if (!aborted(wc)) {
+                            uint8_t* dst = smem + C::kOffV + vr.idx * C::kKVBytes;
+                            mbar_arrive_expect_tx(&v_full[vr.idx], C::kKVBytes);
+                            for (int a = 0; a < C::kAtoms; ++a)
+                                tma_load_3d(dst + a * (kTN * 128), &vmap, &v_full[vr.idx], a * 64, t * kTN, u);
+                            ++vcnt[vr.idx];
+                        }
+                        vr.advance();
+                    }
+                    item = DYN ? atomicAdd(p.sched, 1) : next;
                 }
+                for (int i = 0; i < S; ++i) {
+                    if (kcnt[i]) drain_wait_p(&k_full[i], (kcnt[i] - 1) & 1, kDrainLimit);
+                    if (vcnt[i]) drain_wait_p(&v_full[i], (vcnt[i] - 1) & 1, kDrainLimit);
+                }
+                for (int i = 0; i < QS; ++i)
+                    if (qcnt[i]) drain_wait_p(&q_full[i], (qcnt[i] - 1) & 1, kDrainLimit);
             }
-            for (int i = 0; i < S; ++i) {
-                if (kcnt[i]) drain_wait_p(&k_full[i], (kcnt[i] - 1) & 1, kDrainLimit);
-                if (vcnt[i]) drain_wait_p(&v_full[i], (vcnt[i] - 1) & 1, kDrainLimit);
-            }
-            for (int i = 0; i < QS; ++i)
-                if (qcnt[i]) drain_wait_p(&q_full[i], (qcnt[i] - 1) & 1, kDrainLimit);
-        }
-    } else if (warp == 9) {
-        // ------------------------------------------------ MMA issuer (polls, issues whatever is ready)
-        if (lane_id() == 0) {
-            constexpr uint32_t idesc_qk = idesc_bf16_f32(kTM, kTN, false, false);
-            constexpr uint32_t idesc_pv = idesc_bf16_f32(kTM, D, false, true);
-            PRing qr(QS);
-            uint32_t gtile = 0;          // global K/V tile counter (ring position of tile 0 of an item)
-            uint32_t nqk[2] = {0, 0};    // QKs issued per query tile over the kernel's life
-            uint32_t npv[2] = {0, 0};    // PVs issued per query tile
-            for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-                const int u = item / p.pairs;
-                const int n = unit_keys(p, u);
-                const int Tq[2] = {tile_count<CAUSAL>(p, item_pair<CAUSAL>(p, item), 0, n), tile_count<CAUSAL>(p, item_pair<CAUSAL>(p, item), 1, n)};
-                const int T = max(Tq[0], Tq[1]);
-                if (T == 0) continue;
-                mbar_wait(&q_full[qr.idx], qr.phase, wc);
-                tc_fence_after();
-                const uint32_t sQ = smem_u32(smem + C::kOffQ + qr.idx * C::kQBytes);
-                int jq[2] = {0, 0}, jp[2] = {0, 0};
-                long long t_idle = clock64();
-                int idle_polls = 0;
-                while ((jp[0] < Tq[0] || jp[1] < Tq[1]) && !aborted(wc)) {
-                    bool did = false;
-#pragma unroll
-                    for (int q = 0; q < 2; ++q) {
-                        if (jq[q] < Tq[q]) {
-                            const uint32_t g = gtile + jq[q];
-                            bool ok = mbar_test(&k_full[g % S], (g / S) & 1);
-                            if (ok && nqk[q] > 0) ok = mbar_test(&s_free[q], (nqk[q] - 1) & 1);
-                            // P aliases S: the previous PV must have been issued and have finished reading P
-                            if (ok && C::kAliasP && nqk[q] > 0)
-                                ok = npv[q] == nqk[q] && mbar_test(&o_done[q], (npv[q] - 1) & 1);
-                            if (ok) {
-                                tc_fence_after();
-                                // descriptors once; K steps add constant offsets to the address fields
-                                const uint64_t dq = sdesc_sw128(sQ + q * C::kQTileBytes, 16, 1024);
-                                const uint64_t dk = sdesc_sw128(smem_u32(smem + C::kOffK + (g % S) * C::kKVBytes), 16, 1024);
-                                const uint32_t dS = tmem + q * 128;
-#pragma unroll
-                                for (int kk = 0; kk < D / 16; ++kk)
-                                    mma_ss(dS, dq + (((kk >> 2) * (kTM * 128) + (kk & 3) * 32) >> 4),
-                                           dk + (((kk >> 2) * (kTN * 128) + (kk & 3) * 32) >> 4), idesc_qk, kk > 0 ? 1u : 0u);
-                                mma_commit(&s_full[q]);
-                                ++nqk[q];
-                                ++jq[q];
-                                // the last of the query tiles that need K_g releases it
-                                if (Tq[q ^ 1] <= jq[q] - 1 || jq[q ^ 1] >= jq[q]) mma_commit(&k_empty[g % S]);
-                                did = true;
+        } else if (warp == 9) {
+            // ------------------------------------------------ MMA issuer (polls, issues whatever is ready)
+            if (lane_id() == 0) {
+                constexpr uint32_t idesc_qk = idesc_bf16_f32(kTM, kTN, false, false);
+                constexpr uint32_t idesc_pv = idesc_bf16_f32(kTM, D, false, true);
+                PRing qr(QS);
+                uint32_t gtile = 0;          // global K/V tile counter (ring position of tile 0 of an item)
+                uint32_t nqk[2] = {0, 0};    // QKs issued per query tile over the kernel's life
+                uint32_t npv[2] = {0, 0};    // PVs issued per query tile
+                PRing ir(kItemSlots);
+                int next_fixed = static_cast<int>(blockIdx.x);
+                for (;;) {
+                    int item;
+                    if constexpr (DYN) {
+                        if (!mbar_wait(&item_full[ir.idx], ir.phase, wc)) break;
+                        item = item_q[ir.idx];
+                        mbar_arrive(&item_empty[ir.idx]);
+                        ir.advance();
+                        if (item < 0) break;
+                    } else {
+                        item = next_fixed;
+                        if (item >= n_items) break;
+                        next_fixed += static_cast<int>(gridDim.x);
+                    }
+                    int u, pair;
+                    item_coords<CAUSAL>(p, item, u, pair);
+                    const int n = unit_keys(p, u);
+                    const int Tq[2] = {tile_count<CAUSAL>(p, pair, 0, n), tile_count<CAUSAL>(p, pair, 1, n)};
+                    const int T = max(Tq[0], Tq[1]);
+                    if (T == 0) continue;
+                    mbar_wait(&q_full[qr.idx], qr.phase, wc);
+                    tc_fence_after();
+                    const uint32_t sQ = smem_u32(smem + C::kOffQ + qr.idx * C::kQBytes);
+                    int jq[2] = {0, 0}, jp[2] = {0, 0};
+                    long long t_idle = clock64();
+                    int idle_polls = 0;
+                    while ((jp[0] < Tq[0] || jp[1] < Tq[1]) && !aborted(wc)) {
+                        bool did = false;
+    #pragma unroll
+                        for (int q = 0; q < 2; ++q) {
+                            if (jq[q] < Tq[q]) {
+                                const uint32_t g = gtile + jq[q];
+                                bool ok = mbar_test(&k_full[g % S], (g / S) & 1);
+                                if (ok && nqk[q] > 0) ok = mbar_test(&s_free[q], (nqk[q] - 1) & 1);
+                                // P aliases S: the previous PV must have been issued and have finished reading P
+                                if (ok && C::kAliasP && nqk[q] > 0)
+                                    ok = npv[q] == nqk[q] && mbar_test(&o_done[q], (npv[q] - 1) & 1);
+                                if (ok) {
+                                    tc_fence_after();
+                                    // descriptors once; K steps add constant offsets to the address fields
+                                    const uint64_t dq = sdesc_sw128(sQ + q * C::kQTileBytes, 16, 1024);
+                                    const uint64_t dk = sdesc_sw128(smem_u32(smem + C::kOffK + (g % S) * C::kKVBytes), 16, 1024);
+                                    const uint32_t dS = tmem + q * 128;
+    #pragma unroll
+                                    for (int kk = 0; kk < D / 16; ++kk)
+                                        mma_ss(dS, dq + (((kk >> 2) * (kTM * 128) + (kk & 3) * 32) >> 4),
+                                               dk + (((kk >> 2) * (kTN * 128) + (kk & 3) * 32) >> 4), idesc_qk, kk > 0 ? 1u : 0u);
+                                    mma_commit(&s_full[q]);
+                                    ++nqk[q];
+                                    ++jq[q];
+                                    // the last of the query tiles that need K_g releases it
+                                    if (Tq[q ^ 1] <= jq[q] - 1 || jq[q ^ 1] >= jq[q]) mma_commit(&k_empty[g % S]);
+                                    did = true;
+                                }
+                            }
+                            if (jp[q] < jq[q]) {
+                                const uint32_t g = gtile + jp[q];
+                                bool ok = mbar_test(&p_full[q], npv[q] & 1);
+                                if (ok) ok = mbar_test(&v_full[g % S], (g / S) & 1);
+                                if (ok) {
+                                    tc_fence_after();
+                                    const uint64_t dv = sdesc_sw128(smem_u32(smem + C::kOffV + (g % S) * C::kKVBytes), kTN * 128, 1024);
+                                    const uint32_t dO = tmem + C::kColO + q * D;
+                                    const uint32_t aP = tmem + C::kColP + q * C::kPStride;
+    #pragma unroll
+                                    for (int ks = 0; ks < kTN / 16; ++ks)
+                                        mma_ts(dO, aP + ks * 8, dv + ((ks * 2048) >> 4), idesc_pv, (jp[q] > 0 || ks > 0) ? 1u : 0u);
+                                    mma_commit(&o_done[q]);
+                                    ++npv[q];
+                                    ++jp[q];
+                                    if (Tq[q ^ 1] <= jp[q] - 1 || jp[q ^ 1] >= jp[q]) mma_commit(&v_empty[g % S]);
+                                    did = true;
+                                }
                             }
                         }
-                        if (jp[q] < jq[q]) {
-                            const uint32_t g = gtile + jp[q];
-                            bool ok = mbar_test(&p_full[q], npv[q] & 1);
-                            if (ok) ok = mbar_test(&v_full[g % S], (g / S) & 1);
-                            if (ok) {
-                                tc_fence_after();
-                                const uint64_t dv = sdesc_sw128(smem_u32(smem + C::kOffV + (g % S) * C::kKVBytes), kTN * 128, 1024);
-                                const uint32_t dO = tmem + C::kColO + q * D;
-                                const uint32_t aP = tmem + C::kColP + q * C::kPStride;
-#pragma unroll
-                                for (int ks = 0; ks < kTN / 16; ++ks)
-                                    mma_ts(dO, aP + ks * 8, dv + ((ks * 2048) >> 4), idesc_pv, (jp[q] > 0 || ks > 0) ? 1u : 0u);
-                                mma_commit(&o_done[q]);
-                                ++npv[q];
-                                ++jp[q];
-                                if (Tq[q ^ 1] <= jp[q] - 1 || jp[q ^ 1] >= jp[q]) mma_commit(&v_empty[g % S]);
-                                did = true;
-                            }
+                        if (did) {
+                            t_idle = clock64();
+                            idle_polls = 0;
+                        } else if (++idle_polls > 4) {
+                            __nanosleep(40);   // leave issue slots to the softmax warps on this SM quarter
+                        }
+                        if (!did && clock64() - t_idle > p.limit) {
+                            abort_flag = 1;
+                            atomicExch(p.status, kDevTimeout);
                         }
                     }
-                    if (did) {
-                        t_idle = clock64();
-                        idle_polls = 0;
-                    } else if (++idle_polls > 4) {
-                        __nanosleep(40);   // leave issue slots to the softmax warps on this SM quarter
-                    }
-                    if (!did && clock64() - t_idle > p.limit) {
-                        abort_flag = 1;
-                        atomicExch(p.status, kDevTimeout);
-                    }
+                    if (!aborted(wc)) mma_commit(&q_empty[qr.idx]);
+                    qr.advance();
+                    gtile += T;
                 }
-                if (!aborted(wc)) mma_commit(&q_empty[qr.idx]);
-                qr.advance();
-                gtile += T;
+                mma_commit(&mma_done);
+                drain_wait_p(&mma_done, 0, kDrainLimit);
             }
-            mma_commit(&mma_done);
-            drain_wait_p(&mma_done, 0, kDrainLimit);
         }
     } else {
+        if constexpr (DYN) setmaxnreg_inc<kRegsSoftmax>();
         // ------------------------------------------------ softmax / rescale / epilogue, one row per thread
         const int q = warp / 4;
         const int wl = warp % 4;
@@ -328,11 +405,28 @@ __global__ void __launch_bounds__(kPThreads, 1)
         const uint32_t tO = tmem + lane_base + C::kColO + q * D;
         uint32_t gt = 0;     // tiles processed by this warpgroup over the kernel's life (S/P/O rings)
         uint32_t gring = 0;  // K/V ring position of the current item's first tile
-        for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-            const int u = item / p.pairs;
-            const int row = (item_pair<CAUSAL>(p, item)) * 2 * kTM + q * kTM + row_in_tile;
+        PRing ir(kItemSlots);
+        int next_fixed = static_cast<int>(blockIdx.x);
+        for (;;) {
+            int item;
+            if constexpr (DYN) {
+                // the whole warp leaves together (the TMEM accesses below are warp-collective)
+                if (!__all_sync(0xffffffffu, mbar_wait(&item_full[ir.idx], ir.phase, wc))) break;
+                item = item_q[ir.idx];
+                __syncwarp();
+                if (lane_id() == 0) mbar_arrive(&item_empty[ir.idx]);
+                ir.advance();
+                if (item < 0) break;
+            } else {
+                item = next_fixed;
+                if (item >= n_items) break;
+                next_fixed += static_cast<int>(gridDim.x);
+            }
+            int u, pair;
+            item_coords<CAUSAL>(p, item, u, pair);
+            const int row = pair * 2 * kTM + q * kTM + row_in_tile;
             const int n = unit_keys(p, u);
-            const int T = tile_count<CAUSAL>(p, item_pair<CAUSAL>(p, item), q, n);
+            const int T = tile_count<CAUSAL>(p, pair, q, n);
             // keys this row sees: 0 .. lim - 1
             const int lim = CAUSAL ? min(n, (row < p.R ? row : 0) % p.Sq + n - p.Sq + 1) : n;
             float m_run = -INFINITY, l = 0.f;
@@ -435,7 +529,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
             }
             // The TMEM loads below are warp-collective: every lane executes them; only the stores
             // are predicated on the row existing.
-            gring += max(tile_count<CAUSAL>(p, item_pair<CAUSAL>(p, item), 0, n), tile_count<CAUSAL>(p, item_pair<CAUSAL>(p, item), 1, n));
+            gring += max(tile_count<CAUSAL>(p, pair, 0, n), tile_count<CAUSAL>(p, pair, 1, n));
             const bool store = row < p.R && !aborted(wc);
             const size_t orow = static_cast<size_t>(u) * p.R + (row < p.R ? row : 0);
             const bool none = !(l > 0.f);   // no visible key: O = 0, LSE = -inf
@@ -489,7 +583,20 @@ __global__ void __launch_bounds__(kPThreads, 1)
 }
 
 // ---- host side ------------------------------------------------------------------------------------
-template <int D, bool CAUSAL>
+constexpr size_t kSchedBytes = 256;
+
+// Work-item counter: causal or ragged problems (items of different sizes) when a workspace is in use.
+bool prefill_dynamic(const AttnArgs& a, int sched_mode) { return sched_mode != 1 && (a.causal || a.seqlens); }
+
+size_t stage_bytes(const AttnArgs& a)
+{
+    // NVFP4 output without a caller-provided FP32 buffer: FP32 staging of O (last in the scratch)
+    if (a.out_kind == FMHA_OUT_NVFP4 && !a.out_f32)
+        return (static_cast<size_t>(a.B) * a.Hq * a.Sq * a.D * 4 + 255) & ~size_t(255);
+    return 0;
+}
+
+template <int D, bool CAUSAL, bool DYN>
 int run_prefill(const AttnArgs& a, void* ws, cudaStream_t st)
 {
     using C = PrefillCfg<D>;
@@ -522,22 +629,29 @@ int run_prefill(const AttnArgs& a, void* ws, cudaStream_t st)
     p.pairs = (R + 2 * kTM - 1) / (2 * kTM);
     p.Sq = a.Sq > 0 ? a.Sq : 1;
     p.causal = a.causal;
+    // causal item groups: as many units as keep their K and V within 32 MiB of L2
+    const size_t unit_kv = static_cast<size_t>(a.Skv) * D * 2 * 2;
+    const size_t g = (size_t(32) << 20) / (unit_kv ? unit_kv : 1);
+    p.group = static_cast<int>(g < 1 ? 1 : (g > static_cast<size_t>(U) ? U : g));
+    p.sched = DYN ? static_cast<int*>(ws) : nullptr;
     p.c = a.scale * kLog2eP;
     p.seqlens = a.seqlens;
     const bool nvfp4 = a.out_kind == FMHA_OUT_NVFP4;
     p.out = nvfp4 ? nullptr : a.out;
     p.out_f32 = a.out_kind == FMHA_OUT_F32 ? 1 : 0;
     p.lse = a.lse;
-    p.o_stage = nvfp4 ? (a.out_f32 ? a.out_f32 : static_cast<float*>(ws)) : nullptr;
+    float* stage = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + (DYN ? kSchedBytes : 0));
+    p.o_stage = nvfp4 ? (a.out_f32 ? a.out_f32 : stage) : nullptr;
     p.amax_bits = nvfp4 ? reinterpret_cast<unsigned*>(a.amax_slot) : nullptr;
     p.status = device_status_ptr();
     p.limit = wait_limit();
     const long long items = static_cast<long long>(U) * p.pairs;
     const int grid = static_cast<int>(items < nsm ? items : nsm);
-    FMHA_CHECK_CUDA(cudaFuncSetAttribute(prefill_kernel<D, CAUSAL>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes));
+    FMHA_CHECK_CUDA(cudaFuncSetAttribute(prefill_kernel<D, CAUSAL, DYN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes));
     if (grid > 0) {
+        if (DYN) FMHA_CHECK_CUDA(cudaMemsetAsync(p.sched, 0, sizeof(int), st));
         timing_mark_begin(st);
-        prefill_kernel<D, CAUSAL><<<grid, kPThreads, C::kSmemBytes, st>>>(qmap, kmap, vmap, p);
+        prefill_kernel<D, CAUSAL, DYN><<<grid, prefill_threads<DYN>(), C::kSmemBytes, st>>>(qmap, kmap, vmap, p);
         timing_mark_end(st);
         FMHA_CHECK_LAUNCH("prefill_kernel");
         count_launch();
@@ -545,23 +659,27 @@ int run_prefill(const AttnArgs& a, void* ws, cudaStream_t st)
     return FMHA_OK;
 }
 
-}  // namespace
-
-size_t prefill_workspace_bytes(const AttnArgs& a)
+template <int D>
+int run_prefill_d(const AttnArgs& a, bool dyn, void* ws, cudaStream_t st)
 {
-    // NVFP4 output without a caller-provided FP32 buffer: FP32 staging of O at offset 0
-    if (a.out_kind == FMHA_OUT_NVFP4 && !a.out_f32)
-        return (static_cast<size_t>(a.B) * a.Hq * a.Sq * a.D * 4 + 255) & ~size_t(255);
-    return 0;
+    if (a.causal) return dyn ? run_prefill<D, true, true>(a, ws, st) : run_prefill<D, true, false>(a, ws, st);
+    return dyn ? run_prefill<D, false, true>(a, ws, st) : run_prefill<D, false, false>(a, ws, st);
 }
 
-int launch_prefill(const AttnArgs& a, void* ws, size_t ws_bytes, cudaStream_t st)
+}  // namespace
+
+size_t prefill_workspace_bytes(const AttnArgs& a, int sched_mode)
 {
-    if (ws_bytes < prefill_workspace_bytes(a)) return set_error(FMHA_ERR_WORKSPACE, "row-tile path: workspace too small");
+    return (prefill_dynamic(a, sched_mode) ? kSchedBytes : 0) + stage_bytes(a);
+}
+
+int launch_prefill(const AttnArgs& a, int sched_mode, void* ws, size_t ws_bytes, cudaStream_t st)
+{
+    if (ws_bytes < prefill_workspace_bytes(a, sched_mode)) return set_error(FMHA_ERR_WORKSPACE, "row-tile path: workspace too small");
     switch (a.D) {
-        case 64: return a.causal ? run_prefill<64, true>(a, ws, st) : run_prefill<64, false>(a, ws, st);
-        case 128: return a.causal ? run_prefill<128, true>(a, ws, st) : run_prefill<128, false>(a, ws, st);
-        default: return set_error(FMHA_ERR_UNSUPPORTED, "row-tile path: D must be 64 or 128 (D = 512 not built yet)");
+        case 64: return run_prefill_d<64>(a, prefill_dynamic(a, sched_mode), ws, st);
+        case 128: return run_prefill_d<128>(a, prefill_dynamic(a, sched_mode), ws, st);
+        default: return set_error(FMHA_ERR_UNSUPPORTED, "row-tile path: D must be 64 or 128");
     }
 }
 

@@ -300,6 +300,20 @@ __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols)
                  : "memory");
 }
 
+// Per-warpgroup register budget (every warp of the warpgroup executes the same instruction).  The
+// increases of a CTA must fit in what its decreases and the launch allocation leave free.
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc()
+{
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec()
+{
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 __device__ __forceinline__ void tmem_relinquish()
 {
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");

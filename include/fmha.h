@@ -59,7 +59,11 @@ typedef struct {
     const int32_t* seqlens_k; /* device int32[B], 0 <= seqlens_k[b] <= Skv: keys at or beyond
                                  seqlens_k[b] are never read (ragged batches); NULL = all Skv */
     int num_splits;           /* 0 = automatic split-KV; 1 = no split (each (b, kv-head) handled
-                                 by one CTA, no workspace needed for BF16/F32 output) */
+                                 by one CTA, no workspace needed for BF16/F32 output).  With 0 and
+                                 a workspace, causal or ragged problems on the 128-row path (more
+                                 than 16 query rows per key/value head) also take their work items
+                                 from a counter in the workspace (balanced across SMs); with 1, or
+                                 no workspace, in a fixed order.  0 without a workspace acts as 1 */
     void* workspace;          /* device scratch of at least fmha_workspace_size() bytes (256-B
                                  aligned); contents on entry do not matter */
     size_t workspace_bytes;
@@ -82,8 +86,9 @@ int fmha_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
              int Sq, int Skv, int D, float scale, fmha_stream_t stream);
 
 /*
- * Attention forward with options (output kind, ragged key lengths, split-KV, NVFP4).
- * opts == NULL means all defaults.  Split-KV and NVFP4 output need opts->workspace.
+ * Attention forward with options (output kind, ragged key lengths, causal mask, split-KV, NVFP4).
+ * opts == NULL means all defaults.  Split-KV, the balanced work-item order and NVFP4 output need
+ * opts->workspace; calls that share one workspace must be ordered on one stream.
  */
 int fmha_fwd_ex(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq, int Hkv,
                 int Sq, int Skv, int D, float scale, fmha_stream_t stream, const fmha_opts* opts);

@@ -60,3 +60,60 @@ def test_causal_prefill_full_size_sampled(F):
     rows = sample_rows(w, 64, seed=5)
     o_ref, l_ref = oracle_rows(w, rows, causal=True)
     check_o_lse(res["o"][rows], res["lse"][rows], o_ref, l_ref, "causal prefill full size")
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Sq,Skv,D,seq", [
+    (1, 2, 2, 1000, 1000, 64, None),      # causal, fixed item order (no workspace counter)
+    (1, 8, 2, 64, 500, 128, None),
+    (3, 2, 2, 200, 600, 64, [150, 1, 600]),
+])
+def test_causal_fixed_order(F, B, Hq, Hkv, Sq, Skv, D, seq):
+    """num_splits = 1: the row-tile kernel walks its items in the fixed strided order instead of
+    claiming them from the workspace counter; results must not depend on the order."""
+    w = inputs.Workload("t", B, Hq, Hkv, Sq, Skv, D, 1.0, "bf16", 83)
+    q, k, v, _ = w.make("cuda")
+    sl_t = None if seq is None else torch.tensor(seq, dtype=torch.int32, device="cuda")
+    res = run_attention(F, q, k, v, w.scale, seqlens=sl_t, num_splits=1, causal=True)
+    sl = None if seq is None else np.array(seq, np.int32)
+    o_ref, l_ref = oracle.attention(q.cpu(), k.cpu(), v.cpu(), w.scale, seqlens_k=sl, causal=True)
+    check_o_lse(res["o"], res["lse"], o_ref, l_ref, "causal fixed order")
+
+
+def test_ragged_prefill_balanced_order_many_units(F):
+    """Ragged non-causal prefill with the workspace counter: 48 units of very different lengths,
+    192 items for at most 152 CTAs, so CTAs claim several items of unequal size."""
+    B, H, Sq, Skv, D = 6, 8, 800, 1500, 64
+    sl = [1500, 3, 700, 1, 1280, 129]
+    w = inputs.Workload("t", B, H, H, Sq, Skv, D, 1.0, "bf16", 84)
+    q, k, v, _ = w.make("cuda")
+    for b, n in enumerate(sl):
+        k[b, :, n:] = float("nan")
+        v[b, :, n:] = float("nan")
+    sl_t = torch.tensor(sl, dtype=torch.int32, device="cuda")
+    res = run_attention(F, q, k, v, w.scale, seqlens=sl_t, num_splits=0)
+    o_ref, l_ref = oracle.attention(q.cpu(), k.cpu(), v.cpu(), w.scale, seqlens_k=np.array(sl, np.int32))
+    check_o_lse(res["o"], res["lse"], o_ref, l_ref, "ragged prefill, counter order")
+
+
+def test_causal_workspace_reuse_back_to_back(F):
+    """The work-item counter is reset on the stream before each launch: two causal calls in a row
+    on one workspace give the same (correct) result."""
+    w = inputs.Workload("t", 2, 4, 4, 600, 600, 64, 1.0, "bf16", 85)
+    q, k, v, _ = w.make("cuda")
+    B, Hq, Sq, D = q.shape
+    opts = F.make_opts(F.FMHA_OUT_BF16, None, 0, None, None, None, None, True)
+    wsb = F.fmha_workspace_size(B, Hq, w.Hkv, Sq, w.Skv, D, opts)
+    assert wsb >= 4
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    opts = F.make_opts(F.FMHA_OUT_BF16, None, 0, ws, None, None, None, True)
+    outs = []
+    for _ in range(2):
+        out = torch.full((B, Hq, Sq, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty(B, Hq, Sq, dtype=torch.float32, device="cuda")
+        F.fmha_fwd_ex(q, k, v, out, lse, w.scale, opts)
+        outs.append((out.float().cpu().numpy().reshape(-1, D), lse.cpu().numpy().reshape(-1)))
+    torch.cuda.synchronize()
+    o_ref, l_ref = oracle.attention(q.cpu(), k.cpu(), v.cpu(), w.scale, causal=True)
+    for o, l in outs:
+        check_o_lse(o, l, o_ref, l_ref, "causal back to back")
+    np.testing.assert_array_equal(outs[0][0], outs[1][0])

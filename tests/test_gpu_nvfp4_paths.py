@@ -23,7 +23,8 @@ def F():
 
 @pytest.mark.parametrize("B,Hq,Hkv,Sq,Skv,D,sigma,ragged", [
     (4, 8, 2, 1, 1500, 128, 1.0, True),     # decode path, ragged, split
-    (2, 2, 2, 300, 700, 64, 1.0, False),    # row-tile path
+    (2, 2, 2, 300, 700, 64, 1.0, False),    # row-tile path, fixed item order
+    (3, 4, 2, 300, 700, 64, 1.0, True),     # row-tile path, ragged: counter order, staging after the counter
     (2, 16, 1, 1, 300, 512, 0.5, False),    # wide-head path
 ])
 def test_staging_path_matches_fp32_path(F, B, Hq, Hkv, Sq, Skv, D, sigma, ragged):
