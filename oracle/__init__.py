@@ -55,6 +55,8 @@ def _load():
             lib.oracle_qk_f64.restype = I
             lib.oracle_nvfp4_quantize.argtypes = [P, I64, P, P, P]
             lib.oracle_nvfp4_quantize.restype = I
+            lib.oracle_nvfp4_quantize_scaled.argtypes = [P, I64, ctypes.c_float, P, P]
+            lib.oracle_nvfp4_quantize_scaled.restype = I
             lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
             lib.oracle_e4m3_decode.restype = ctypes.c_double
             lib.oracle_e4m3_round.argtypes = [ctypes.c_double]
@@ -142,6 +144,23 @@ def nvfp4_quantize(x):
     if rc != 0:
         raise ValueError("oracle_nvfp4_quantize: bad arguments (n % 16 != 0?)")
     return codes, scales, float(sg[0])
+
+
+def nvfp4_quantize_scaled(x, tensor_scale: float):
+    """NVFP4 encoding of an FP32 array (n % 16 == 0) with a given per-tensor scale s_g.
+
+    Returns (codes uint8[n/2], scales uint8[n/16])."""
+    lib = _load()
+    if not isinstance(x, np.ndarray):
+        x = x.detach().cpu().numpy()
+    xf = np.ascontiguousarray(x, dtype=np.float32).reshape(-1)
+    n = xf.shape[0]
+    codes = np.zeros(n // 2, dtype=np.uint8)
+    scales = np.zeros(n // 16, dtype=np.uint8)
+    rc = lib.oracle_nvfp4_quantize_scaled(_ptr(xf), n, float(np.float32(tensor_scale)), _ptr(codes), _ptr(scales))
+    if rc != 0:
+        raise ValueError("oracle_nvfp4_quantize_scaled: bad arguments (n % 16 != 0?)")
+    return codes, scales
 
 
 def e4m3_decode(code: int) -> float:

@@ -8,7 +8,8 @@
  * consecutive values, and an FP32 per-tensor scale s_g = amax / (6 * 448).
  *
  * Steps, written out in the order of that definition:
- *   1. amax = max |x_i| over the whole tensor; s_g = fp32_round_nearest(amax / 2688).
+ *   1. amax = max |x_i| over the whole tensor; s_g = fp32_round_nearest(amax / 2688)
+ *      (skipped by oracle_nvfp4_quantize_scaled, which takes s_g from the caller).
  *   2. per block of 16: sc = E4M3_round_nearest_even_satfinite(amax_block / (6 s_g)).
  *   3. per element: code = E2M1_round_nearest_even_satfinite(x_i / (dec(sc) * s_g)), sign kept.
  *   4. packing: element 2i in bits 3:0, element 2i+1 in bits 7:4.
@@ -82,6 +83,46 @@ uint8_t oracle_e2m1_round(double v)
     return (uint8_t)(best | (signbit(v) ? 8 : 0));
 }
 
+/* Steps 2-4 of the definition with a given per-tensor scale s_g (the single-pass form: a caller
+ * that knows s_g in advance, e.g. from an earlier step's amax, skips step 1).  Block scales above
+ * the E4M3 range and elements above 6 saturate.  An s_g that is not a positive finite number
+ * encodes every block as zero (as amax = 0 does in step 1). */
+int oracle_nvfp4_quantize_scaled(const float* x, int64_t n, float s_g, uint8_t* codes, uint8_t* scales)
+{
+    if (!x || !codes || !scales || n < 0 || n % 16 != 0)
+        return -1;
+    const int usable = s_g > 0.0f && !isinf(s_g);
+    memset(codes, 0, (size_t)(n / 2));
+    for (int64_t blk = 0; blk < n / 16; ++blk) {
+        const float* xb = x + blk * 16;
+        /* 2. block scale */
+        float amax_b = 0.0f;
+        for (int i = 0; i < 16; ++i) {
+            const float a = fabsf(xb[i]);
+            if (a > amax_b)
+                amax_b = a;
+        }
+        uint8_t sc = 0;
+        if (usable)
+            sc = oracle_e4m3_round((double)amax_b / (6.0 * (double)s_g));
+        scales[blk] = sc;
+        /* 3. element codes against den = dec(sc) * s_g (exact in FP64) */
+        const double den = usable ? oracle_e4m3_decode(sc) * (double)s_g : 0.0;
+        for (int i = 0; i < 16; ++i) {
+            uint8_t c = 0;
+            if (den > 0.0)
+                c = oracle_e2m1_round((double)xb[i] / den);
+            /* 4. packing */
+            const int64_t e = blk * 16 + i;
+            if ((e & 1) == 0)
+                codes[e / 2] |= c;
+            else
+                codes[e / 2] |= (uint8_t)(c << 4);
+        }
+    }
+    return 0;
+}
+
 int oracle_nvfp4_quantize(const float* x, int64_t n, uint8_t* codes, uint8_t* scales,
                           float* tensor_scale)
 {
@@ -97,34 +138,6 @@ int oracle_nvfp4_quantize(const float* x, int64_t n, uint8_t* codes, uint8_t* sc
     }
     const float s_g = (float)((double)amax / 2688.0);
     *tensor_scale = s_g;
-
-    memset(codes, 0, (size_t)(n / 2));
-    for (int64_t blk = 0; blk < n / 16; ++blk) {
-        const float* xb = x + blk * 16;
-        /* 2. block scale */
-        float amax_b = 0.0f;
-        for (int i = 0; i < 16; ++i) {
-            const float a = fabsf(xb[i]);
-            if (a > amax_b)
-                amax_b = a;
-        }
-        uint8_t sc = 0;
-        if (s_g > 0.0f)
-            sc = oracle_e4m3_round((double)amax_b / (6.0 * (double)s_g));
-        scales[blk] = sc;
-        /* 3. element codes against den = dec(sc) * s_g (exact in FP64) */
-        const double den = oracle_e4m3_decode(sc) * (double)s_g;
-        for (int i = 0; i < 16; ++i) {
-            uint8_t c = 0;
-            if (den > 0.0)
-                c = oracle_e2m1_round((double)xb[i] / den);
-            /* 4. packing */
-            const int64_t e = blk * 16 + i;
-            if ((e & 1) == 0)
-                codes[e / 2] |= c;
-            else
-                codes[e / 2] |= (uint8_t)(c << 4);
-        }
-    }
-    return 0;
+    /* 2.-4. */
+    return oracle_nvfp4_quantize_scaled(x, n, s_g, codes, scales);
 }

@@ -48,6 +48,10 @@ int oracle_qk_f64(const uint16_t* q, const uint16_t* k, int Sq, int Skv, int D, 
 int oracle_nvfp4_quantize(const float* x, int64_t n, uint8_t* codes, uint8_t* scales,
                           float* tensor_scale);
 
+/* The same encoding with a given per-tensor scale s_g (steps 2-4 only); s_g that is not a positive
+ * finite number gives all-zero codes and scales. */
+int oracle_nvfp4_quantize_scaled(const float* x, int64_t n, float s_g, uint8_t* codes, uint8_t* scales);
+
 /* Helpers exposed for the self-tests. */
 double oracle_e4m3_decode(uint8_t code);            /* E4M3FN bits -> value (NaN for 0x7F/0xFF) */
 uint8_t oracle_e4m3_round(double v);                /* |v| >= 0 -> nearest E4M3FN, ties even, saturating */
