@@ -48,6 +48,8 @@ class fmha_opts(ctypes.Structure):
         ("out_tensor_scale", ctypes.c_void_p),
         ("out_f32", ctypes.c_void_p),
         ("causal", ctypes.c_int),
+        ("nvfp4_scale_in", ctypes.c_void_p),
+        ("out_amax", ctypes.c_void_p),
     ]
 
 
@@ -74,6 +76,7 @@ def load(path: str | None = None):
             "fmha_fwd_ex": ([V, V, V, V, V, I, I, I, I, I, I, F, V, ctypes.POINTER(fmha_opts)], I),
             "fmha_workspace_size": ([I, I, I, I, I, I, ctypes.POINTER(fmha_opts)], S),
             "nvfp4_quantize": ([V, V, V, I64, V], I),
+            "nvfp4_quantize_scaled": ([V, V, V, I64, V, V], I),
             "nvfp4_scales_bytes": ([I64], S),
             "fmha_qk_gemm": ([V, V, V, I, I, I, V], I),
             "fmha_selftest": ([I, V, V, S, I, V], I),
@@ -134,9 +137,12 @@ def fmha_fwd(q, k, v, out, lse, scale: float, stream=None):
 
 
 def make_opts(out_kind=FMHA_OUT_BF16, seqlens_k=None, num_splits=0, workspace=None,
-              out_scales=None, out_tensor_scale=None, out_f32=None, causal=False) -> fmha_opts:
+              out_scales=None, out_tensor_scale=None, out_f32=None, causal=False,
+              nvfp4_scale_in=None, out_amax=None) -> fmha_opts:
     o = fmha_opts()
     o.causal = 1 if causal else 0
+    o.nvfp4_scale_in = None if nvfp4_scale_in is None else nvfp4_scale_in.data_ptr()
+    o.out_amax = None if out_amax is None else out_amax.data_ptr()
     o.out_kind = out_kind
     o.seqlens_k = None if seqlens_k is None else seqlens_k.data_ptr()
     o.num_splits = num_splits
@@ -172,6 +178,13 @@ def nvfp4_quantize(x, q, scales, stream=None):
     _need_cuda(x, q, scales)
     rc = load().nvfp4_quantize(_ptr(x), _ptr(q), _ptr(scales), x.numel(), _stream(stream))
     _check(rc, "nvfp4_quantize")
+
+
+def nvfp4_quantize_scaled(x, q, scales, tensor_scale, stream=None):
+    """x: FP32 [n] (n % 16 == 0), q: uint8 [n/2], scales: uint8 [n/16], tensor_scale: FP32 [1] (s_g)."""
+    _need_cuda(x, q, scales, tensor_scale)
+    rc = load().nvfp4_quantize_scaled(_ptr(x), _ptr(q), _ptr(scales), x.numel(), _ptr(tensor_scale), _stream(stream))
+    _check(rc, "nvfp4_quantize_scaled")
 
 
 def fmha_qk_gemm(q, k, s, stream=None):

@@ -219,7 +219,7 @@ static size_t workspace_bytes(const AttnArgs& a, int num_splits)
     size_t w = a.D == 512 ? wide_workspace_bytes(a)
                : use_decode_path(a.Hq, a.Hkv, a.Sq) ? decode_workspace_bytes(a, num_splits) : prefill_workspace_bytes(a, num_splits);
     w = align256(w);
-    if (a.out_kind == FMHA_OUT_NVFP4) w += 256;
+    if (a.out_kind == FMHA_OUT_NVFP4 && !a.nv_sg) w += 256;   // amax word of the two-pass NVFP4 path
     return w;
 }
 
@@ -243,6 +243,8 @@ static int validate(const void* q, const void* k, const void* v, const void* out
                 return set_error(FMHA_ERR_INVALID, "NVFP4 output needs out_scales and out_tensor_scale");
             if ((o->out_f32 && !aligned16(o->out_f32)))
                 return set_error(FMHA_ERR_INVALID, "out_f32 must be 16-byte aligned");
+            if ((reinterpret_cast<uintptr_t>(o->nvfp4_scale_in) & 3) || (reinterpret_cast<uintptr_t>(o->out_amax) & 3))
+                return set_error(FMHA_ERR_INVALID, "nvfp4_scale_in and out_amax must be 4-byte aligned");
         }
         if (o->seqlens_k && (reinterpret_cast<uintptr_t>(o->seqlens_k) & 3))
             return set_error(FMHA_ERR_INVALID, "seqlens_k must be 4-byte aligned");
@@ -272,6 +274,7 @@ static AttnArgs make_args(const void* q, const void* k, const void* v, void* out
     a.out_kind = o ? o->out_kind : FMHA_OUT_BF16;
     a.out_f32 = (o && o->out_kind == FMHA_OUT_NVFP4) ? o->out_f32 : nullptr;
     a.causal = (o && o->causal) ? 1 : 0;
+    a.nv_sg = (o && o->out_kind == FMHA_OUT_NVFP4) ? o->nvfp4_scale_in : nullptr;
     return a;
 }
 
@@ -301,11 +304,23 @@ int fmha_fwd_ex(const void* q, const void* k, const void* v, void* out, float* l
         return set_error(FMHA_ERR_WORKSPACE, "workspace missing or smaller than fmha_workspace_size()");
     if (static_cast<long long>(B) * Hq * Sq == 0) return FMHA_OK;
     const bool nvfp4 = a.out_kind == FMHA_OUT_NVFP4;
-    const size_t path_bytes = nvfp4 ? need - 256 : need;
-    unsigned* amax = nvfp4 ? reinterpret_cast<unsigned*>(static_cast<uint8_t*>(ws) + path_bytes) : nullptr;
-    if (nvfp4) {
+    const bool two_pass = nvfp4 && !a.nv_sg;
+    const size_t path_bytes = two_pass ? need - 256 : need;
+    // |O| max: the caller's out_amax when given, else (two passes) the word after the path scratch
+    unsigned* amax = nullptr;
+    if (nvfp4 && opts->out_amax)
+        amax = reinterpret_cast<unsigned*>(opts->out_amax);
+    else if (two_pass)
+        amax = reinterpret_cast<unsigned*>(static_cast<uint8_t*>(ws) + path_bytes);
+    if (amax) {
         a.amax_slot = reinterpret_cast<float*>(amax);
         FMHA_CHECK_CUDA(cudaMemsetAsync(amax, 0, sizeof(unsigned), st));
+    }
+    if (nvfp4 && a.nv_sg) {
+        // single pass: the epilogues write the codes and block scales themselves
+        a.nv_codes = static_cast<uint8_t*>(out);
+        a.nv_scales = opts->out_scales;
+        a.nv_ts = opts->out_tensor_scale;
     }
     if (D == 512)
         rc = launch_wide(a, ws, path_bytes, st);
@@ -314,7 +329,7 @@ int fmha_fwd_ex(const void* q, const void* k, const void* v, void* out, float* l
     else
         rc = launch_prefill(a, num_splits, ws, path_bytes, st);
     if (rc) return rc;
-    if (nvfp4) {
+    if (two_pass) {
         // the FP32 O the quantiser reads: caller's out_f32, else the staging area of the workspace
         const float* src = a.out_f32;
         if (!src) {
@@ -340,6 +355,18 @@ size_t nvfp4_scales_bytes(int64_t n)
 {
     if (n < 0) return 0;
     return align16(static_cast<size_t>(n / 16)) + 16;
+}
+
+int nvfp4_quantize_scaled(const float* x, uint8_t* q, uint8_t* scales, int64_t n, const float* tensor_scale,
+                          fmha_stream_t stream)
+{
+    if (!x || !q || !scales || !tensor_scale) return set_error(FMHA_ERR_INVALID, "nvfp4_quantize_scaled: NULL pointer");
+    if (n < 0 || n % 16 != 0) return set_error(FMHA_ERR_INVALID, "nvfp4_quantize_scaled: n must be a non-negative multiple of 16");
+    if (!aligned16(x) || (reinterpret_cast<uintptr_t>(q) & 7) || (reinterpret_cast<uintptr_t>(tensor_scale) & 3))
+        return set_error(FMHA_ERR_INVALID, "nvfp4_quantize_scaled: x 16-byte, q 8-byte, tensor_scale 4-byte aligned");
+    if (!device_status_ptr()) return set_error(FMHA_ERR_CUDA, "no CUDA device");
+    if (n == 0) return FMHA_OK;
+    return launch_nvfp4(x, q, scales, nullptr, nullptr, n, true, reinterpret_cast<cudaStream_t>(stream), tensor_scale);
 }
 
 int nvfp4_quantize(const float* x, uint8_t* q, uint8_t* scales, int64_t n, fmha_stream_t stream)

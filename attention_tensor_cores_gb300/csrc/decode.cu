@@ -32,6 +32,7 @@
 #include <cstdio>
 
 #include "internal.h"
+#include "nvfp4_dev.cuh"
 #include "ptx.cuh"
 
 namespace fmha {
@@ -77,6 +78,10 @@ struct DecodeParams {
     float* lse;              // [U*G] or NULL
     float* o_stage;          // FP32 [U*G][D] copy for NVFP4, else NULL
     unsigned* amax_bits;     // NVFP4: running max |O| (FP32 bits), else NULL
+    const float* nv_sg;      // single-pass NVFP4: given s_g; codes/scales written here, else NULL
+    uint8_t* nv_codes;
+    uint8_t* nv_scales;
+    float* nv_ts;
     float* part_o;           // [slots][16][D]
     float* part_lse;         // [slots][16]
     int* status;
@@ -230,6 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ float red_sum[4][kN];
 
     const int warp = threadIdx.x / 32;
+    if (blockIdx.x == 0 && threadIdx.x == 0 && p.nv_ts) *p.nv_ts = *p.nv_sg;   // single-pass NVFP4: report s_g
     const WaitCtl wc{&abort_flag, p.status, p.limit};
 
     if (threadIdx.x == 0) {
@@ -385,6 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int lane = static_cast<int>(lane_id());
         const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
         const int G = p.G;
+        const float nv_sg = p.nv_sg ? *p.nv_sg : 0.f;
         Ring sr(2), pr(2), orr(2), vr(S);
         uint32_t tile_ctr = 0;
         while (sched.next(it)) {
@@ -498,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int q = 0; q < kN; ++q) L[q] = 0.f;
             }
-            if (aborted(wc)) continue;
+            if (__any_sync(0xffffffffu, aborted(wc))) continue;   // warp-uniform (shuffles below)
             const bool empty = it.t1 <= it.t0;
             float local_amax = 0.f;
             if (tid < D) {
@@ -510,10 +517,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float lse_v = none ? -INFINITY : (m[q] + __log2f(L[q])) * kLn2;
                     const size_t row = static_cast<size_t>(it.u) * G + q;
                     if (it.whole) {
-                        if (p.o_stage) {
-                            p.o_stage[row * D + tid] = o;
-                            local_amax = fmaxf(local_amax, fabsf(o));
-                        }
+                        if (p.o_stage) p.o_stage[row * D + tid] = o;
+                        if (p.amax_bits) local_amax = fmaxf(local_amax, fabsf(o));
+                        // single-pass NVFP4: a warp holds 32 consecutive columns of the row
+                        if (p.nv_codes) nvfp4_encode_lanes(o, nv_sg, tid, p.nv_codes + row * (D / 2), p.nv_scales + row * (D / 16));
                         if (p.out) {
                             if (p.out_f32)
                                 static_cast<float*>(p.out)[row * D + tid] = o;
@@ -650,6 +657,7 @@ __global__ void combine_kernel(const __grid_constant__ DecodeParams p, int nctas
             static_cast<uint16_t*>(p.out)[r * D + d] = float_to_bf16_bits(o);
     }
     if (d == 0 && p.lse) p.lse[r] = lse_v;
+    if (p.nv_codes) nvfp4_encode_lanes(o, *p.nv_sg, d, p.nv_codes + r * (D / 2), p.nv_scales + r * (D / 16));
     if (p.amax_bits) {
         const float wm = warp_max(fabsf(o));
         if ((threadIdx.x & 31) == 0 && wm > 0.f) atomicMax(p.amax_bits, __float_as_uint(wm));
@@ -679,7 +687,7 @@ DecodeWs decode_ws_layout(const AttnArgs& a, bool split, int nsm)
     w.o_off = off;
     off += al(slots * kN * a.D * 4);
     w.stage_off = off;
-    const bool stage = (a.out_kind == FMHA_OUT_NVFP4) && !a.out_f32;
+    const bool stage = (a.out_kind == FMHA_OUT_NVFP4) && !a.out_f32 && !a.nv_sg;
     off += stage ? al(static_cast<size_t>(a.B) * a.Hq * a.Sq * a.D * 4) : 0;
     w.total = off;
     return w;
@@ -731,8 +739,12 @@ int run_decode(const AttnArgs& a, bool split, void* ws, cudaStream_t st)
     p.out = nvfp4 ? nullptr : a.out;
     p.out_f32 = a.out_kind == FMHA_OUT_F32 ? 1 : 0;
     p.lse = a.lse;
-    p.o_stage = nvfp4 ? (a.out_f32 ? a.out_f32 : reinterpret_cast<float*>(base + w.stage_off)) : nullptr;
+    p.o_stage = nvfp4 ? (a.out_f32 ? a.out_f32 : (a.nv_sg ? nullptr : reinterpret_cast<float*>(base + w.stage_off))) : nullptr;
     p.amax_bits = nvfp4 ? reinterpret_cast<unsigned*>(a.amax_slot) : nullptr;
+    p.nv_sg = a.nv_sg;
+    p.nv_codes = a.nv_codes;
+    p.nv_scales = a.nv_scales;
+    p.nv_ts = a.nv_ts;
     p.part_lse = split ? reinterpret_cast<float*>(base + w.lse_off) : nullptr;
     p.part_o = split ? reinterpret_cast<float*>(base + w.o_off) : nullptr;
     p.status = device_status_ptr();

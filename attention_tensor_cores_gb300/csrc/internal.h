@@ -59,6 +59,11 @@ struct AttnArgs {
     float* out_f32;          // FP32 O destination (NVFP4 path), else NULL
     float* amax_slot;        // NVFP4 path: |O| max accumulator (uint bits), else NULL
     int causal;              // bottom-right aligned causal mask
+    // single-pass NVFP4 (given s_g): the epilogues encode O directly, else all NULL
+    const float* nv_sg;      // device s_g
+    uint8_t* nv_codes;       // E2M1 codes [rows][D/2]
+    uint8_t* nv_scales;      // E4M3 block scales [rows][D/16]
+    float* nv_ts;            // receives s_g
 };
 
 // Decode / small-group path (query rows per key/value head <= 16): swap-AB kernels.
@@ -75,7 +80,9 @@ size_t wide_workspace_bytes(const AttnArgs& a);
 int launch_wide(const AttnArgs& a, void* ws, size_t ws_bytes, cudaStream_t st);
 
 // NVFP4
+// NVFP4 quantiser: s_g from sg_in when given (no amax pass), else from *amax_bits (computed here
+// unless amax_ready).
 int launch_nvfp4(const float* x, uint8_t* codes, uint8_t* scales, float* tensor_scale, unsigned* amax_bits,
-                 int64_t n, bool amax_ready, cudaStream_t st);
+                 int64_t n, bool amax_ready, cudaStream_t st, const float* sg_in = nullptr);
 
 }  // namespace fmha

@@ -29,6 +29,7 @@
 #include <cuda_runtime.h>
 
 #include "internal.h"
+#include "nvfp4_dev.cuh"
 #include "ptx.cuh"
 
 namespace fmha {
@@ -43,8 +44,8 @@ constexpr int kTN = 128;          // keys per tile
 // floats) and its packed P without spilling: 2*128*208 + 128*88 = 64512, and on each SM quarter
 // (warps w, w+4, w+8) the control warp frees exactly what its two softmax warps take.  The
 // fixed-order kernel keeps 10 warps at 168 registers, which measured faster for dense problems.
-template <bool DYN>
-constexpr int prefill_threads() { return DYN ? 384 : 320; }
+template <bool RING>
+constexpr int prefill_threads() { return RING ? 384 : 320; }
 constexpr uint32_t kRegsSoftmax = 208;
 constexpr uint32_t kRegsCtl = 88;
 static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsCtl <= prefill_threads<true>() * 168, "register split exceeds the launch allocation");
@@ -89,6 +90,10 @@ struct PrefillParams {
     float* lse;
     float* o_stage;
     unsigned* amax_bits;
+    const float* nv_sg;      // single-pass NVFP4: given s_g; codes/scales written here, else NULL
+    uint8_t* nv_codes;
+    uint8_t* nv_scales;
+    float* nv_ts;
     int* status;
     long long limit;
 };
@@ -156,8 +161,11 @@ struct PRing {
     }
 };
 
-template <int D, bool CAUSAL, bool DYN>
-__global__ void __launch_bounds__(prefill_threads<DYN>(), 1)
+// RING: 12 warps with the register split, work items handed out through the shared-memory ring
+// (from the workspace counter when p.sched is set, else in the fixed order), and the single-pass
+// NVFP4 epilogue.  !RING: 10 warps at 168 registers, fixed order, no NVFP4 encoder (dense problems).
+template <int D, bool CAUSAL, bool RING>
+__global__ void __launch_bounds__(prefill_threads<RING>(), 1)
     prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap, const __grid_constant__ PrefillParams p)
 {
@@ -176,6 +184,7 @@ __global__ void __launch_bounds__(prefill_threads<DYN>(), 1)
 
     const int warp = threadIdx.x / 32;
     const WaitCtl wc{&abort_flag, p.status, p.limit};
+    if (RING && blockIdx.x == 0 && threadIdx.x == 0 && p.nv_ts) *p.nv_ts = *p.nv_sg;   // single-pass NVFP4: report s_g
     if (threadIdx.x == 0) {
         abort_flag = 0;
         for (int i = 0; i < QS; ++i) {
@@ -214,7 +223,7 @@ __global__ void __launch_bounds__(prefill_threads<DYN>(), 1)
     // Each setmaxnreg dominates only its own role's code (the register budget of code after a join
     // would be the smaller one) and is executed by whole warpgroups.
     if (warp >= 8) {
-        if constexpr (DYN) setmaxnreg_dec<kRegsCtl>();
+        if constexpr (RING) setmaxnreg_dec<kRegsCtl>();
         if (warp == 8) {
             // ------------------------------------------------ TMA producer
             if (lane_id() == 0) {
@@ -226,10 +235,10 @@ __global__ void __launch_bounds__(prefill_threads<DYN>(), 1)
                 for (int i = 0; i < S; ++i) kcnt[i] = vcnt[i] = 0;
                 for (int i = 0; i < QS; ++i) qcnt[i] = 0;
                 PRing ir(kItemSlots);
-                int item = DYN ? atomicAdd(p.sched, 1) : static_cast<int>(blockIdx.x);
+                int item = (RING && p.sched) ? atomicAdd(p.sched, 1) : static_cast<int>(blockIdx.x);
                 for (;;) {
                     const bool more = item < n_items;
-                    if constexpr (DYN) {
+                    if constexpr (RING) {
                         // hand the item (or the end mark) to the MMA and softmax warps
                         if (!mbar_wait(&item_empty[ir.idx], ir.phase ^ 1, wc)) break;
                         item_q[ir.idx] = more ? item : -1;
@@ -244,9 +253,9 @@ __global__ void __launch_bounds__(prefill_threads<DYN>(), 1)
                     const int T = max(tile_count<CAUSAL>(p, pair, 0, n), tile_count<CAUSAL>(p, pair, 1, n));
                     // the next item is claimed once this one's loads are issued, so a CTA takes new
                     // work only shortly before it runs out
-                    const int next = DYN ? -1 : item + static_cast<int>(gridDim.x);
+                    const int next = item + static_cast<int>(gridDim.x);
                     if (T == 0) {
-                        item = DYN ? atomicAdd(p.sched, 1) : next;
+                        item = (RING && p.sched) ? atomicAdd(p.sched, 1) : next;
                         continue;
                     }
                     mbar_wait(&q_empty[qr.idx], qr.phase ^ 1, wc);
@@ -280,7 +289,7 @@ __global__ void __launch_bounds__(prefill_threads<DYN>(), 1)
                         }
                         vr.advance();
                     }
-                    item = DYN ? atomicAdd(p.sched, 1) : next;
+                    item = (RING && p.sched) ? atomicAdd(p.sched, 1) : next;
                 }
                 for (int i = 0; i < S; ++i) {
                     if (kcnt[i]) drain_wait_p(&k_full[i], (kcnt[i] - 1) & 1, kDrainLimit);
@@ -302,7 +311,7 @@ __global__ void __launch_bounds__(prefill_threads<DYN>(), 1)
                 int next_fixed = static_cast<int>(blockIdx.x);
                 for (;;) {
                     int item;
-                    if constexpr (DYN) {
+                    if constexpr (RING) {
                         if (!mbar_wait(&item_full[ir.idx], ir.phase, wc)) break;
                         item = item_q[ir.idx];
                         mbar_arrive(&item_empty[ir.idx]);
@@ -394,7 +403,7 @@ __global__ void __launch_bounds__(prefill_threads<DYN>(), 1)
             }
         }
     } else {
-        if constexpr (DYN) setmaxnreg_inc<kRegsSoftmax>();
+        if constexpr (RING) setmaxnreg_inc<kRegsSoftmax>();
         // ------------------------------------------------ softmax / rescale / epilogue, one row per thread
         const int q = warp / 4;
         const int wl = warp % 4;
@@ -403,13 +412,14 @@ __global__ void __launch_bounds__(prefill_threads<DYN>(), 1)
         const uint32_t tS = tmem + lane_base + q * 128;
         const uint32_t tP = tmem + lane_base + C::kColP + q * C::kPStride;
         const uint32_t tO = tmem + lane_base + C::kColO + q * D;
+        const float nv_sg = (RING && p.nv_sg) ? *p.nv_sg : 0.f;
         uint32_t gt = 0;     // tiles processed by this warpgroup over the kernel's life (S/P/O rings)
         uint32_t gring = 0;  // K/V ring position of the current item's first tile
         PRing ir(kItemSlots);
         int next_fixed = static_cast<int>(blockIdx.x);
         for (;;) {
             int item;
-            if constexpr (DYN) {
+            if constexpr (RING) {
                 // the whole warp leaves together (the TMEM accesses below are warp-collective)
                 if (!__all_sync(0xffffffffu, mbar_wait(&item_full[ir.idx], ir.phase, wc))) break;
                 item = item_q[ir.idx];
@@ -554,8 +564,22 @@ __global__ void __launch_bounds__(prefill_threads<DYN>(), 1)
                         float4* dst = reinterpret_cast<float4*>(p.o_stage + orow * D + c4 * 32);
 #pragma unroll
                         for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                    }
+                    if (p.amax_bits) {
 #pragma unroll
                         for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+                    }
+                    if constexpr (RING) {
+                        if (p.nv_codes) {
+                            // single-pass NVFP4: this thread holds the whole row, two 16-value blocks per chunk
+#pragma unroll
+                            for (int b = 0; b < 2; ++b) {
+                                uint32_t lo, hi;
+                                const uint32_t sc = nvfp4_encode16(v + 16 * b, nv_sg, lo, hi);
+                                reinterpret_cast<uint2*>(p.nv_codes + orow * (D / 2) + c4 * 16)[b] = make_uint2(lo, hi);
+                                p.nv_scales[orow * (D / 16) + c4 * 2 + b] = static_cast<uint8_t>(sc);
+                            }
+                        }
                     }
                     if (p.out) {
                         if (p.out_f32) {
@@ -588,16 +612,20 @@ constexpr size_t kSchedBytes = 256;
 // Work-item counter: causal or ragged problems (items of different sizes) when a workspace is in use.
 bool prefill_dynamic(const AttnArgs& a, int sched_mode) { return sched_mode != 1 && (a.causal || a.seqlens); }
 
+// The ring kernel: balanced (counter) order, or single-pass NVFP4 output (its epilogue encoder needs
+// the softmax warps' larger register budget; in the compact kernel it slowed dense problems).
+bool prefill_ring(const AttnArgs& a, int sched_mode) { return prefill_dynamic(a, sched_mode) || a.nv_sg; }
+
 size_t stage_bytes(const AttnArgs& a)
 {
     // NVFP4 output without a caller-provided FP32 buffer: FP32 staging of O (last in the scratch)
-    if (a.out_kind == FMHA_OUT_NVFP4 && !a.out_f32)
+    if (a.out_kind == FMHA_OUT_NVFP4 && !a.out_f32 && !a.nv_sg)
         return (static_cast<size_t>(a.B) * a.Hq * a.Sq * a.D * 4 + 255) & ~size_t(255);
     return 0;
 }
 
-template <int D, bool CAUSAL, bool DYN>
-int run_prefill(const AttnArgs& a, void* ws, cudaStream_t st)
+template <int D, bool CAUSAL, bool RING>
+int run_prefill(const AttnArgs& a, bool dynamic, void* ws, cudaStream_t st)
 {
     using C = PrefillCfg<D>;
     const int nsm = num_sms();
@@ -633,25 +661,29 @@ int run_prefill(const AttnArgs& a, void* ws, cudaStream_t st)
     const size_t unit_kv = static_cast<size_t>(a.Skv) * D * 2 * 2;
     const size_t g = (size_t(32) << 20) / (unit_kv ? unit_kv : 1);
     p.group = static_cast<int>(g < 1 ? 1 : (g > static_cast<size_t>(U) ? U : g));
-    p.sched = DYN ? static_cast<int*>(ws) : nullptr;
+    p.sched = dynamic ? static_cast<int*>(ws) : nullptr;
     p.c = a.scale * kLog2eP;
     p.seqlens = a.seqlens;
     const bool nvfp4 = a.out_kind == FMHA_OUT_NVFP4;
     p.out = nvfp4 ? nullptr : a.out;
     p.out_f32 = a.out_kind == FMHA_OUT_F32 ? 1 : 0;
     p.lse = a.lse;
-    float* stage = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + (DYN ? kSchedBytes : 0));
-    p.o_stage = nvfp4 ? (a.out_f32 ? a.out_f32 : stage) : nullptr;
+    float* stage = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + (dynamic ? kSchedBytes : 0));
+    p.o_stage = nvfp4 ? (a.out_f32 ? a.out_f32 : (a.nv_sg ? nullptr : stage)) : nullptr;
     p.amax_bits = nvfp4 ? reinterpret_cast<unsigned*>(a.amax_slot) : nullptr;
+    p.nv_sg = a.nv_sg;
+    p.nv_codes = a.nv_codes;
+    p.nv_scales = a.nv_scales;
+    p.nv_ts = a.nv_ts;
     p.status = device_status_ptr();
     p.limit = wait_limit();
     const long long items = static_cast<long long>(U) * p.pairs;
     const int grid = static_cast<int>(items < nsm ? items : nsm);
-    FMHA_CHECK_CUDA(cudaFuncSetAttribute(prefill_kernel<D, CAUSAL, DYN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes));
+    FMHA_CHECK_CUDA(cudaFuncSetAttribute(prefill_kernel<D, CAUSAL, RING>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes));
     if (grid > 0) {
-        if (DYN) FMHA_CHECK_CUDA(cudaMemsetAsync(p.sched, 0, sizeof(int), st));
+        if (dynamic) FMHA_CHECK_CUDA(cudaMemsetAsync(p.sched, 0, sizeof(int), st));
         timing_mark_begin(st);
-        prefill_kernel<D, CAUSAL, DYN><<<grid, prefill_threads<DYN>(), C::kSmemBytes, st>>>(qmap, kmap, vmap, p);
+        prefill_kernel<D, CAUSAL, RING><<<grid, prefill_threads<RING>(), C::kSmemBytes, st>>>(qmap, kmap, vmap, p);
         timing_mark_end(st);
         FMHA_CHECK_LAUNCH("prefill_kernel");
         count_launch();
@@ -660,10 +692,12 @@ int run_prefill(const AttnArgs& a, void* ws, cudaStream_t st)
 }
 
 template <int D>
-int run_prefill_d(const AttnArgs& a, bool dyn, void* ws, cudaStream_t st)
+int run_prefill_d(const AttnArgs& a, int sched_mode, void* ws, cudaStream_t st)
 {
-    if (a.causal) return dyn ? run_prefill<D, true, true>(a, ws, st) : run_prefill<D, true, false>(a, ws, st);
-    return dyn ? run_prefill<D, false, true>(a, ws, st) : run_prefill<D, false, false>(a, ws, st);
+    const bool dyn = prefill_dynamic(a, sched_mode);
+    const bool ring = prefill_ring(a, sched_mode);
+    if (a.causal) return ring ? run_prefill<D, true, true>(a, dyn, ws, st) : run_prefill<D, true, false>(a, dyn, ws, st);
+    return ring ? run_prefill<D, false, true>(a, dyn, ws, st) : run_prefill<D, false, false>(a, dyn, ws, st);
 }
 
 }  // namespace
@@ -677,8 +711,8 @@ int launch_prefill(const AttnArgs& a, int sched_mode, void* ws, size_t ws_bytes,
 {
     if (ws_bytes < prefill_workspace_bytes(a, sched_mode)) return set_error(FMHA_ERR_WORKSPACE, "row-tile path: workspace too small");
     switch (a.D) {
-        case 64: return run_prefill_d<64>(a, prefill_dynamic(a, sched_mode), ws, st);
-        case 128: return run_prefill_d<128>(a, prefill_dynamic(a, sched_mode), ws, st);
+        case 64: return run_prefill_d<64>(a, sched_mode, ws, st);
+        case 128: return run_prefill_d<128>(a, sched_mode, ws, st);
         default: return set_error(FMHA_ERR_UNSUPPORTED, "row-tile path: D must be 64 or 128");
     }
 }

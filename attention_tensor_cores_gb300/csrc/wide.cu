@@ -22,6 +22,7 @@
 #include <cuda_runtime.h>
 
 #include "internal.h"
+#include "nvfp4_dev.cuh"
 #include "ptx.cuh"
 
 namespace fmha {
@@ -64,6 +65,10 @@ struct WideParams {
     float* lse;
     float* o_stage;
     unsigned* amax_bits;
+    const float* nv_sg;      // single-pass NVFP4: given s_g; codes/scales written here, else NULL
+    uint8_t* nv_codes;
+    uint8_t* nv_scales;
+    float* nv_ts;
     float* part_o;      // [slots][128][512]
     float* part_lse;    // [slots][128]
     int* status;
@@ -165,6 +170,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
     __shared__ int abort_flag;
 
     const int warp = threadIdx.x / 32;
+    if (blockIdx.x == 0 && threadIdx.x == 0 && p.nv_ts) *p.nv_ts = *p.nv_sg;   // single-pass NVFP4: report s_g
     const int half = blockIdx.x & 1;
     const WaitCtl wc{&abort_flag, p.status, p.limit};
     if (threadIdx.x == 0) {
@@ -439,8 +445,21 @@ __global__ void __launch_bounds__(kWThreads, 1)
                             float4* dst = reinterpret_cast<float4*>(p.o_stage + orow * kWD + col);
 #pragma unroll
                             for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                        }
+                        if (p.amax_bits) {
 #pragma unroll
                             for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+                        }
+                        if (p.nv_codes) {
+                            // single-pass NVFP4: two 16-value blocks of this thread's row per chunk
+                            const float sg = *p.nv_sg;
+#pragma unroll
+                            for (int b = 0; b < 2; ++b) {
+                                uint32_t lo, hi;
+                                const uint32_t sc = nvfp4_encode16(v + 16 * b, sg, lo, hi);
+                                reinterpret_cast<uint2*>(p.nv_codes + orow * (kWD / 2) + col / 2)[b] = make_uint2(lo, hi);
+                                p.nv_scales[orow * (kWD / 16) + col / 16 + b] = static_cast<uint8_t>(sc);
+                            }
                         }
                         if (p.out) {
                             if (p.out_f32) {
@@ -604,6 +623,13 @@ __global__ void __launch_bounds__(32 * kCombRows) wide_combine_kernel(const __gr
         }
     }
     if (lane == 0 && p.lse) p.lse[orow] = lse_v;
+    if (p.nv_codes) {
+        // single-pass NVFP4: lane holds columns 16 lane .. 16 lane + 15, one block
+        uint32_t lo, hi;
+        const uint32_t sc = nvfp4_encode16(acc, *p.nv_sg, lo, hi);
+        reinterpret_cast<uint2*>(p.nv_codes + orow * (kWD / 2))[lane] = make_uint2(lo, hi);
+        p.nv_scales[orow * (kWD / 16) + lane] = static_cast<uint8_t>(sc);
+    }
     if (p.amax_bits) {
         float m = 0.f;
 #pragma unroll
@@ -633,7 +659,7 @@ WideWs wide_ws_layout(const AttnArgs& a, int npairs)
     w.o_off = off;
     off += al(slots * kWRows * kWD * 4);
     w.stage_off = off;
-    const bool stage = (a.out_kind == FMHA_OUT_NVFP4) && !a.out_f32;
+    const bool stage = (a.out_kind == FMHA_OUT_NVFP4) && !a.out_f32 && !a.nv_sg;
     off += stage ? al(static_cast<size_t>(a.B) * a.Hq * a.Sq * kWD * 4) : 0;
     w.total = off;
     return w;
@@ -692,8 +718,12 @@ int launch_wide(const AttnArgs& a, void* ws, size_t ws_bytes, cudaStream_t st)
     p.out = nvfp4 ? nullptr : a.out;
     p.out_f32 = a.out_kind == FMHA_OUT_F32 ? 1 : 0;
     p.lse = a.lse;
-    p.o_stage = nvfp4 ? (a.out_f32 ? a.out_f32 : reinterpret_cast<float*>(base + w.stage_off)) : nullptr;
+    p.o_stage = nvfp4 ? (a.out_f32 ? a.out_f32 : (a.nv_sg ? nullptr : reinterpret_cast<float*>(base + w.stage_off))) : nullptr;
     p.amax_bits = nvfp4 ? reinterpret_cast<unsigned*>(a.amax_slot) : nullptr;
+    p.nv_sg = a.nv_sg;
+    p.nv_codes = a.nv_codes;
+    p.nv_scales = a.nv_scales;
+    p.nv_ts = a.nv_ts;
     p.part_lse = reinterpret_cast<float*>(base + w.lse_off);
     p.part_o = reinterpret_cast<float*>(base + w.o_off);
     p.status = device_status_ptr();

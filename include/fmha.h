@@ -73,6 +73,16 @@ typedef struct {
     int causal;               /* 1: bottom-right aligned causal mask: with n keys, query i of Sq sees
                                  keys 0 .. i + n - Sq (a query that sees none gets O = 0,
                                  LSE = -inf); 0 = all keys */
+    const float* nvfp4_scale_in; /* NVFP4, optional: device float[1], a given per-tensor scale s_g
+                                 (e.g. an earlier step's max|O| / 2688).  Set: single pass, the
+                                 attention epilogues write codes and block scales with this s_g
+                                 directly; no amax pass, no FP32 staging, no workspace for NVFP4.
+                                 Blocks beyond 6 * 448 * s_g saturate; an s_g that is not a
+                                 positive finite number gives all-zero codes and scales;
+                                 *out_tensor_scale receives s_g.  NULL: s_g = fp32(max|O| / 2688)
+                                 of this O (two passes) */
+    float* out_amax;          /* optional, NVFP4 only: device float[1], receives max|O| (FP32) of
+                                 this call */
 } fmha_opts;
 
 /*
@@ -110,6 +120,16 @@ int nvfp4_quantize(const float* x, uint8_t* q, uint8_t* scales, int64_t n, fmha_
 
 /* Size in bytes of the `scales` buffer nvfp4_quantize needs for n values. */
 size_t nvfp4_scales_bytes(int64_t n);
+
+/*
+ * NVFP4 encoding of x[n] (n % 16 == 0) with a given per-tensor scale: tensor_scale is a device
+ * float[1] holding s_g.  q: n/2 bytes of E2M1 codes (as nvfp4_quantize); scales: n/16 bytes of
+ * E4M3 block scales (no trailing s_g).  Same roundings as nvfp4_quantize; blocks beyond
+ * 6 * 448 * s_g saturate and an s_g that is not a positive finite number gives all zeros.
+ * Errors: FMHA_ERR_INVALID for NULL pointers, n < 0, n % 16 != 0 or x, q not 16-byte aligned.
+ */
+int nvfp4_quantize_scaled(const float* x, uint8_t* q, uint8_t* scales, int64_t n, const float* tensor_scale,
+                          fmha_stream_t stream);
 
 /*
  * Test hook: raw S = Q K^T in FP32, no scale ("CURRENT_ISSUE.md" @57d67e6, "The 4x Bug":

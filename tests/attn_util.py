@@ -16,8 +16,12 @@ O_MEAN = 2e-3
 LSE_REL = 1e-3
 
 
-def run_attention(F, q, k, v, scale, out_kind="bf16", seqlens=None, num_splits=None, want_f32=False, causal=False):
-    """Calls fmha_fwd (no options) or fmha_fwd_ex; returns dict of host numpy results."""
+def run_attention(F, q, k, v, scale, out_kind="bf16", seqlens=None, num_splits=None, want_f32=False, causal=False,
+                  nvfp4_scale=None, want_amax=False):
+    """Calls fmha_fwd (no options) or fmha_fwd_ex; returns dict of host numpy results.
+
+    nvfp4_scale: a given per-tensor scale s_g (single-pass NVFP4); want_amax: also return max|O|
+    through opts.out_amax."""
     B, Hq, Sq, D = q.shape
     Hkv, Skv = k.shape[1], k.shape[2]
     lse = torch.full((B, Hq, Sq), float("nan"), dtype=torch.float32, device="cuda")
@@ -35,21 +39,27 @@ def run_attention(F, q, k, v, scale, out_kind="bf16", seqlens=None, num_splits=N
             scales = torch.zeros(n // 16, dtype=torch.uint8, device="cuda")
             ts = torch.zeros(1, dtype=torch.float32, device="cuda")
             f32 = torch.full((n,), float("nan"), dtype=torch.float32, device="cuda") if want_f32 else None
+            sg_in = None if nvfp4_scale is None else torch.tensor([nvfp4_scale], dtype=torch.float32, device="cuda")
+            amax = torch.full((1,), float("nan"), dtype=torch.float32, device="cuda") if want_amax else None
         else:
+            sg_in = amax = None
             dt = torch.bfloat16 if out_kind == "bf16" else torch.float32
             out = torch.full((B, Hq, Sq, D), float("nan"), dtype=dt, device="cuda")
             scales = ts = f32 = None
         ns = 0 if num_splits is None else num_splits
-        opts = F.make_opts(kind, seqlens, ns, None, scales, ts, f32, causal)
+        opts = F.make_opts(kind, seqlens, ns, None, scales, ts, f32, causal, sg_in, amax)
         wsb = F.fmha_workspace_size(B, Hq, Hkv, Sq, Skv, D, opts)
         ws = torch.empty(max(wsb, 1), dtype=torch.uint8, device="cuda") if wsb else None
-        opts = F.make_opts(kind, seqlens, ns, ws, scales, ts, f32, causal)
+        opts = F.make_opts(kind, seqlens, ns, ws, scales, ts, f32, causal, sg_in, amax)
+        res["workspace_bytes"] = wsb
         F.fmha_fwd_ex(q, k, v, out, lse, scale, opts)
         torch.cuda.synchronize()
         if out_kind == "nvfp4":
             res["codes"] = out.cpu().numpy()
             res["scales"] = scales.cpu().numpy()
             res["tensor_scale"] = float(ts.cpu()[0])
+            if want_amax:
+                res["amax"] = float(amax.cpu()[0])
             if want_f32:
                 res["o"] = f32.cpu().numpy().reshape(-1, D)
         else:
