@@ -507,6 +507,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (__any_sync(0xffffffffu, aborted(wc))) continue;   // warp-uniform (shuffles below)
             const bool empty = it.t1 <= it.t0;
+            // single-pass NVFP4 in split mode: whole units also go through the combine, which
+            // encodes every row in parallel (encoding here would lengthen the CTAs holding many
+            // short units)
+            const bool final_here = it.whole && !(p.split && p.nv_codes);
             float local_amax = 0.f;
             if (tid < D) {
 #pragma unroll
@@ -516,7 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float o = none ? 0.f : acc[q] / L[q];
                     const float lse_v = none ? -INFINITY : (m[q] + __log2f(L[q])) * kLn2;
                     const size_t row = static_cast<size_t>(it.u) * G + q;
-                    if (it.whole) {
+                    if (final_here) {
                         if (p.o_stage) p.o_stage[row * D + tid] = o;
                         if (p.amax_bits) local_amax = fmaxf(local_amax, fabsf(o));
                         // single-pass NVFP4: a warp holds 32 consecutive columns of the row
@@ -534,7 +538,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            if (p.amax_bits && it.whole) {
+            if (p.amax_bits && final_here) {
                 const float wm = warp_max(local_amax);
                 if (lane == 0 && wm > 0.f) atomicMax(p.amax_bits, __float_as_uint(wm));
             }
@@ -603,7 +607,7 @@ __global__ void combine_kernel(const __grid_constant__ DecodeParams p, int nctas
             const long long P = nctas;
             const int c0 = static_cast<int>(min((((Tu + 1) * P) - 1) / T, P - 1));
             const int c1 = static_cast<int>(min((((Tu + tiles) * P) - 1) / T, P - 1));
-            if (c0 == c1) {
+            if (c0 == c1 && !p.nv_codes) {
                 cnt = -1;   // one CTA held the whole unit and wrote it
             } else {
                 for (int cw = c0; cw <= c1; cw += 32) {
