@@ -7,18 +7,22 @@
 // BF16 Q tile alone is 128 KB of shared memory.  The design:
 //
 //  * CTA pairs split the value dimension: CTA h of a pair accumulates O[:, 256h : 256h + 256] (256
-//    TMEM columns).  Both CTAs of the pair compute the full S = Q K^T (M = 128 query rows, N = 32
-//    keys, K = 512), so each holds all of Q (128 KB) and each 32-key K tile (32 KB), plus its half of
-//    the V tile (16 KB); two K/V stages fit in the remaining shared memory.  The pair's K tiles are
-//    the same addresses, read once from HBM and once more from L2.
-//  * Stream-K over keys: the 32-key tiles of all units (b, kv-head, 128-row block) are laid end to
-//    end and pair p of P takes [p*T/P, (p+1)*T/P); a run that covers a whole unit writes O and LSE,
+//    TMEM columns).  Both CTAs of the pair compute the full S = Q K^T, so each holds all of Q.
+//  * 128-key tiles: the QK MMA is M = 128 query rows by N = 128 keys, so each K = 16 step reads a
+//    4 KB slice of Q for 256K MACs (with 32-key tiles the Q re-reads made the tensor core's
+//    shared-memory operand path the limiter).  A 128-key K tile (128 KB) and Q (128 KB) do not fit
+//    together, so K and V stream through one ring of 16 KB chunks: a K chunk is 64 of the 512
+//    contraction columns of the tile's 128 keys, a V chunk is 32 keys by this CTA's 256 columns.
+//    Chunks go through the ring in the order the MMAs use them: K(0); K(j), V(j-1) for each later
+//    tile j; then V of the last tile.
+//  * Tensor Memory: S (128 columns), P (64 columns of BF16 pairs), O half (256 columns).  QK(j+1)
+//    only needs the softmax to have read S(j), so it runs while the softmax of j works; PV(j) needs
+//    P(j).  The tensor pipe then alternates QK(j+1), PV(j) without waiting on the softmax.
+//  * Stream-K over keys: the tiles of all units (b, kv-head, 128-row block) are laid end to end and
+//    pair p of P takes [p*T/P, (p+1)*T/P); a run that covers a whole unit writes O and LSE,
 //    otherwise a normalised partial goes to slot unit + p and the combine kernel merges them.
 //  * Roles: warps 0-3 softmax (one query row per thread, lazy rescale as in the row-tile kernel),
-//    warp 4 loads Q and K, warp 6 loads V (so a V slot that frees late never holds back the next K
-//    tile), warp 5 issues MMAs by polling: a QK may run up to two tiles ahead of the PVs (S is
-//    double-buffered in TMEM), so the tensor pipe does not wait on the softmax.  All waits are
-//    bounded.
+//    warp 4 loads Q, K and V, warp 5 issues the MMAs in order.  All waits are bounded.
 #include <cuda_runtime.h>
 
 #include "internal.h"
@@ -31,22 +35,30 @@ namespace {
 constexpr int kWD = 512;            // head dim of Q/K/V
 constexpr int kWHalf = 256;         // value columns per CTA
 constexpr int kWRows = 128;         // query rows per unit (MMA M)
-constexpr int kWKeys = 32;          // keys per tile (QK N, PV K)
-constexpr int kWStages = 2;
-constexpr int kWThreads = 224;   // 4 softmax warps, Q/K producer, MMA issuer, V producer
+constexpr int kWKeys = 128;         // keys per tile (QK N, PV K)
+constexpr int kWKChunks = 8;        // K chunks per tile: 64 contraction columns each
+constexpr int kWVChunks = 4;        // V chunks per tile: 32 keys each
+constexpr int kWVKeys = kWKeys / kWVChunks;
+constexpr int kWChunkBytes = 16384;
+constexpr int kWSlots = 6;          // chunk ring depth
+constexpr int kWThreads = 192;      // 4 softmax warps, producer, MMA issuer
 constexpr float kLog2eW = 1.4426950408889634f;
 constexpr float kLn2W = 0.6931471805599453f;
 constexpr float kRescaleW = 8.0f;
 
 constexpr int kWQBytes = 8 * kWRows * 128;          // 8 atoms of 128 rows x 128 B = 128 KB
-constexpr int kWKBytes = 8 * kWKeys * 128;          // 8 atoms of 32 rows x 128 B = 32 KB
-constexpr int kWVBytes = 4 * kWKeys * 128;          // 4 atoms (this CTA's 256 columns) = 16 KB
 constexpr int kWOffQ = 0;
-constexpr int kWOffK = kWOffQ + kWQBytes;
-constexpr int kWOffV = kWOffK + kWStages * kWKBytes;
-constexpr int kWSmem = kWOffV + kWStages * kWVBytes + 1024;
-// TMEM columns: S[2] at 0/32, P[2] at 64/80 (16 columns = 32 BF16 keys), O half at 256..511.
-constexpr uint32_t kWColS = 0, kWColP = 64, kWColO = 256;
+constexpr int kWOffRing = kWOffQ + kWQBytes;
+constexpr int kWSmem = kWOffRing + kWSlots * kWChunkBytes + 1024;
+static_assert(kWKeys * 128 == kWChunkBytes && 4 * kWVKeys * 128 == kWChunkBytes, "chunk layouts");
+// TMEM columns: S 0..127, P 128..191 (BF16 pairs of 128 keys), O half 256..511.
+constexpr uint32_t kWColS = 0, kWColP = 128, kWColO = 256;
+
+// Position of chunk c of V(j) in an item's chunk sequence K(0); K(1), V(0); ...; K(T-1), V(T-2); V(T-1).
+__device__ __forceinline__ uint32_t wv_chunk_pos(int j, int T, int c)
+{
+    return static_cast<uint32_t>(j < T - 1 ? 12 * j + 16 + c : 12 * j + 8 + c);
+}
 
 struct WideParams {
     int U;          // units = B * Hkv * row_tiles
@@ -164,8 +176,8 @@ __global__ void __launch_bounds__(kWThreads, 1)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    __shared__ uint64_t q_full, q_empty, k_full[kWStages], k_empty[kWStages], v_full[kWStages], v_empty[kWStages];
-    __shared__ uint64_t s_full[2], s_empty[2], p_full, o_done, mma_done;
+    __shared__ uint64_t q_full, q_empty, c_full[kWSlots], c_empty[kWSlots];
+    __shared__ uint64_t s_full, s_empty, p_full, o_done, mma_done;
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
 
@@ -177,16 +189,12 @@ __global__ void __launch_bounds__(kWThreads, 1)
         abort_flag = 0;
         mbar_init(&q_full, 1);
         mbar_init(&q_empty, 1);
-        for (int i = 0; i < kWStages; ++i) {
-            mbar_init(&k_full[i], 1);
-            mbar_init(&k_empty[i], 1);
-            mbar_init(&v_full[i], 1);
-            mbar_init(&v_empty[i], 1);
+        for (int i = 0; i < kWSlots; ++i) {
+            mbar_init(&c_full[i], 1);
+            mbar_init(&c_empty[i], 1);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&s_full[i], 1);
-            mbar_init(&s_empty[i], 128);
-        }
+        mbar_init(&s_full, 1);
+        mbar_init(&s_empty, 128);
         mbar_init(&p_full, 128);
         mbar_init(&o_done, 1);
         mbar_init(&mma_done, 1);
@@ -205,13 +213,38 @@ __global__ void __launch_bounds__(kWThreads, 1)
     WItem it;
 
     if (warp == 4) {
-        // ------------------------------------------------ TMA producer
+        // ------------------------------------------------ TMA producer: Q per item, then the chunk sequence
         if (lane_id() == 0) {
             tma_prefetch_desc(&qmap);
             tma_prefetch_desc(&kmap);
             tma_prefetch_desc(&vmap);
-            WRing kr(kWStages);
-            uint32_t qn = 0, kcnt[kWStages] = {0, 0};
+            WRing cr(kWSlots);
+            uint32_t qn = 0, ccnt[kWSlots] = {0, 0, 0, 0, 0, 0};
+            auto load_k = [&](int hu, int t) {
+                for (int a = 0; a < kWKChunks; ++a) {
+                    mbar_wait(&c_empty[cr.idx], cr.phase ^ 1, wc);
+                    if (!aborted(wc)) {
+                        mbar_arrive_expect_tx(&c_full[cr.idx], kWChunkBytes);
+                        tma_load_3d(smem + kWOffRing + cr.idx * kWChunkBytes, &kmap, &c_full[cr.idx], a * 64, t * kWKeys, hu);
+                        ++ccnt[cr.idx];
+                    }
+                    cr.advance();
+                }
+            };
+            auto load_v = [&](int hu, int t) {
+                for (int c = 0; c < kWVChunks; ++c) {
+                    mbar_wait(&c_empty[cr.idx], cr.phase ^ 1, wc);
+                    if (!aborted(wc)) {
+                        uint8_t* dst = smem + kWOffRing + cr.idx * kWChunkBytes;
+                        mbar_arrive_expect_tx(&c_full[cr.idx], kWChunkBytes);
+                        for (int a = 0; a < 4; ++a)
+                            tma_load_3d(dst + a * (kWVKeys * 128), &vmap, &c_full[cr.idx], half * kWHalf + a * 64,
+                                        t * kWKeys + c * kWVKeys, hu);
+                        ++ccnt[cr.idx];
+                    }
+                    cr.advance();
+                }
+            };
             while (sched.next(it)) {
                 const int hu = wunit_head(p, it.u);
                 const int rt = it.u % p.row_tiles;
@@ -222,155 +255,120 @@ __global__ void __launch_bounds__(kWThreads, 1)
                         tma_load_3d(smem + kWOffQ + a * (kWRows * 128), &qmap, &q_full, a * 64, rt * kWRows, hu);
                 }
                 ++qn;
-                for (int t = it.t0; t < it.t1; ++t) {
-                    mbar_wait(&k_empty[kr.idx], kr.phase ^ 1, wc);
-                    if (!aborted(wc)) {
-                        uint8_t* dst = smem + kWOffK + kr.idx * kWKBytes;
-                        mbar_arrive_expect_tx(&k_full[kr.idx], kWKBytes);
-                        for (int a = 0; a < 8; ++a)
-                            tma_load_3d(dst + a * (kWKeys * 128), &kmap, &k_full[kr.idx], a * 64, t * kWKeys, hu);
-                        ++kcnt[kr.idx];
-                    }
-                    kr.advance();
+                if (it.t1 <= it.t0) continue;
+                load_k(hu, it.t0);
+                for (int t = it.t0 + 1; t < it.t1 && !aborted(wc); ++t) {
+                    load_k(hu, t);
+                    load_v(hu, t - 1);
                 }
+                load_v(hu, it.t1 - 1);
             }
-            for (int i = 0; i < kWStages; ++i)
-                if (kcnt[i]) wdrain(&k_full[i], (kcnt[i] - 1) & 1, kDrainLimit);
+            for (int i = 0; i < kWSlots; ++i)
+                if (ccnt[i]) wdrain(&c_full[i], (ccnt[i] - 1) & 1, kDrainLimit);
             if (qn) wdrain(&q_full, (qn - 1) & 1, kDrainLimit);
         }
-    } else if (warp == 6) {
-        // ------------------------------------------------ V producer (this CTA's half of the columns)
-        if (lane_id() == 0) {
-            WRing vr(kWStages);
-            uint32_t vcnt[kWStages] = {0, 0};
-            while (sched.next(it)) {
-                const int hu = wunit_head(p, it.u);
-                for (int t = it.t0; t < it.t1; ++t) {
-                    mbar_wait(&v_empty[vr.idx], vr.phase ^ 1, wc);
-                    if (!aborted(wc)) {
-                        uint8_t* dst = smem + kWOffV + vr.idx * kWVBytes;
-                        mbar_arrive_expect_tx(&v_full[vr.idx], kWVBytes);
-                        for (int a = 0; a < 4; ++a)
-                            tma_load_3d(dst + a * (kWKeys * 128), &vmap, &v_full[vr.idx], half * kWHalf + a * 64,
-                                        t * kWKeys, hu);
-                        ++vcnt[vr.idx];
-                    }
-                    vr.advance();
-                }
-            }
-            for (int i = 0; i < kWStages; ++i)
-                if (vcnt[i]) wdrain(&v_full[i], (vcnt[i] - 1) & 1, kDrainLimit);
-        }
     } else if (warp == 5) {
-        // ------------------------------------------------ MMA issuer
+        // ------------------------------------------------ MMA issuer, in the chunk order
         if (lane_id() == 0) {
             constexpr uint32_t idesc_qk = idesc_bf16_f32(kWRows, kWKeys, false, false);
             constexpr uint32_t idesc_pv = idesc_bf16_f32(kWRows, kWHalf, false, true);
-            uint32_t qn = 0;
-            uint32_t nk = 0, nv = 0, ns = 0, np = 0;   // K tiles, V tiles, QKs and PVs so far (kernel life)
+            WRing cr(kWSlots);
+            uint32_t qn = 0, ns = 0, np = 0;   // items, QKs and PVs so far (kernel life)
             const uint32_t sQ = smem_u32(smem + kWOffQ);
+            const uint64_t dq0 = sdesc_sw128(sQ, 16, 1024);
+            auto issue_qk = [&]() {
+                if (ns > 0) mbar_wait(&s_empty, (ns - 1) & 1, wc);   // the softmax has read S
+                for (int a = 0; a < kWKChunks; ++a) {
+                    mbar_wait(&c_full[cr.idx], cr.phase, wc);
+                    if (aborted(wc)) return;
+                    tc_fence_after();
+                    const uint64_t dk = sdesc_sw128(smem_u32(smem + kWOffRing + cr.idx * kWChunkBytes), 16, 1024);
+                    const uint64_t dq = dq0 + ((a * (kWRows * 128)) >> 4);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_ss(tmem + kWColS, dq + ((kk * 32) >> 4), dk + ((kk * 32) >> 4), idesc_qk, (a > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(&c_empty[cr.idx]);
+                    cr.advance();
+                }
+                mma_commit(&s_full);
+                ++ns;
+            };
+            auto issue_pv = [&](bool first) {
+                mbar_wait(&p_full, np & 1, wc);
+                for (int c = 0; c < kWVChunks; ++c) {
+                    mbar_wait(&c_full[cr.idx], cr.phase, wc);
+                    if (aborted(wc)) return;
+                    tc_fence_after();
+                    const uint32_t sV = smem_u32(smem + kWOffRing + cr.idx * kWChunkBytes);
+#pragma unroll
+                    for (int kq = 0; kq < kWVKeys / 16; ++kq) {
+                        const uint64_t db = sdesc_sw128(sV + kq * 2048, kWVKeys * 128, 1024);
+                        mma_ts(tmem + kWColO, tmem + kWColP + (c * (kWVKeys / 16) + kq) * 8, db, idesc_pv,
+                               (!first || c > 0 || kq > 0) ? 1u : 0u);
+                    }
+                    mma_commit(&c_empty[cr.idx]);
+                    cr.advance();
+                }
+                mma_commit(&o_done);
+                ++np;
+            };
             while (sched.next(it)) {
                 mbar_wait(&q_full, qn & 1, wc);
                 ++qn;
+                tc_fence_after();
                 const int T = it.t1 - it.t0;
-                int jq = 0, jp = 0;
-                long long t_idle = clock64();
-                int idle = 0;
-                while (jp < T && !aborted(wc)) {
-                    bool did = false;
-                    // QK of tile jq: its K tile landed and its S buffer was read (up to 2 ahead of PV)
-                    if (jq < T) {
-                        const uint32_t ks = nk % kWStages, sb = ns & 1;
-                        bool ok = mbar_test(&k_full[ks], (nk / kWStages) & 1);
-                        if (ok) ok = mbar_test(&s_empty[sb], ((ns >> 1) & 1) ^ 1);
-                        if (ok) {
-                            tc_fence_after();
-                            // descriptors once per tile; K steps add constant offsets to their address
-                            // fields (addr >> 4 in 14 bits covers all of shared memory: no carry leaves it)
-                            const uint64_t dq = sdesc_sw128(sQ, 16, 1024);
-                            const uint64_t dk = sdesc_sw128(smem_u32(smem + kWOffK + ks * kWKBytes), 16, 1024);
-                            const uint32_t ds = tmem + kWColS + sb * kWKeys;
-                            mma_ss(ds, dq, dk, idesc_qk, 0u);
-#pragma unroll
-                            for (int kk = 1; kk < kWD / 16; ++kk)
-                                mma_ss(ds, dq + (((kk >> 2) * (kWRows * 128) + (kk & 3) * 32) >> 4),
-                                       dk + (((kk >> 2) * (kWKeys * 128) + (kk & 3) * 32) >> 4), idesc_qk, 1u);
-                            mma_commit(&s_full[sb]);
-                            mma_commit(&k_empty[ks]);
-                            ++nk;
-                            ++ns;
-                            ++jq;
-                            did = true;
-                        }
+                if (T > 0 && !aborted(wc)) {
+                    issue_qk();
+                    for (int j = 1; j < T && !aborted(wc); ++j) {
+                        issue_qk();
+                        issue_pv(j == 1);
                     }
-                    // PV of tile jp: its P is written and its V tile landed
-                    if (jp < jq) {
-                        const uint32_t vs = nv % kWStages;
-                        bool ok = mbar_test(&p_full, np & 1);
-                        if (ok) ok = mbar_test(&v_full[vs], (nv / kWStages) & 1);
-                        if (ok) {
-                            tc_fence_after();
-                            const uint32_t sV = smem_u32(smem + kWOffV + vs * kWVBytes);
-#pragma unroll
-                            for (int kq = 0; kq < kWKeys / 16; ++kq) {
-                                const uint64_t db = sdesc_sw128(sV + kq * 2048, kWKeys * 128, 1024);
-                                mma_ts(tmem + kWColO, tmem + kWColP + kq * 8, db, idesc_pv, (jp > 0 || kq > 0) ? 1u : 0u);
-                            }
-                            mma_commit(&o_done);
-                            mma_commit(&v_empty[vs]);
-                            ++nv;
-                            ++np;
-                            ++jp;
-                            did = true;
-                        }
-                    }
-                    if (did) {
-                        t_idle = clock64();
-                        idle = 0;
-                    } else {
-                        if (++idle > 8) __nanosleep(32);
-                        if (clock64() - t_idle > p.limit) {
-                            *reinterpret_cast<volatile int*>(&abort_flag) = 1;
-                            atomicExch(p.status, kDevTimeout);
-                        }
-                    }
+                    if (!aborted(wc)) issue_pv(T == 1);
                 }
                 if (!aborted(wc)) mma_commit(&q_empty);
             }
             mma_commit(&mma_done);
             wdrain(&mma_done, 0, kDrainLimit);
         }
-    } else {
+    } else if (warp < 4) {
         // ------------------------------------------------ softmax / epilogue, one query row per thread
         const int row_in_tile = warp * 32 + static_cast<int>(lane_id());
         const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-        WRing sr(2), vr(kWStages);
-        uint32_t g = 0;   // P tiles produced = PVs issued for this CTA
+        uint32_t g = 0;       // tiles (= S reads = PVs) so far, kernel life
+        uint32_t gchunk = 0;  // chunk sequence position of the current item's first chunk
         while (sched.next(it)) {
             const int hu = wunit_head(p, it.u);
             const int row = (it.u % p.row_tiles) * kWRows + row_in_tile;
+            const int T = it.t1 - it.t0;
             // keys this row sees: 0 .. lim - 1
             const int lim = p.causal ? min(it.n, (row < p.R ? row : 0) % p.Sq + it.n - p.Sq + 1) : it.n;
             float m_run = -INFINITY, l = 0.f;
             for (int t = it.t0; t < it.t1; ++t, ++g) {
-                mbar_wait(&s_full[sr.idx], sr.phase, wc);
+                mbar_wait(&s_full, g & 1, wc);
                 tc_fence_after();
                 float s[kWKeys];
-                tmem_ld32p(tmem + lane_base + kWColS + sr.idx * kWKeys, reinterpret_cast<uint32_t*>(s));
+                uint32_t* su = reinterpret_cast<uint32_t*>(s);
+#pragma unroll
+                for (int c4 = 0; c4 < kWKeys / 32; ++c4) tmem_ld32p(tmem + lane_base + kWColS + c4 * 32, su + c4 * 32);
                 tmem_ld_wait();
                 tc_fence_before();
-                mbar_arrive(&s_empty[sr.idx]);
-                sr.advance();
-                const bool partial = (t + 1) * kWKeys > it.n;
+                mbar_arrive(&s_empty);
                 if ((t + 1) * kWKeys > lim) {
 #pragma unroll
                     for (int i = 0; i < kWKeys; ++i)
                         if (t * kWKeys + i >= lim) s[i] = -INFINITY;
                 }
-                float mx = s[0];
+                float mx[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
-                for (int i = 1; i < kWKeys; ++i) mx = fmaxf(mx, s[i]);
-                const float mt = mx * p.c;
+                for (int i = 4; i < kWKeys; i += 8) {
+                    mx[0] = fmax3(mx[0], s[i], s[i + 1]);
+                    mx[1] = fmax3(mx[1], s[i + 2], s[i + 3]);
+                    if (i + 4 < kWKeys) {
+                        mx[2] = fmax3(mx[2], s[i + 4], s[i + 5]);
+                        mx[3] = fmax3(mx[3], s[i + 6], s[i + 7]);
+                    }
+                }
+                const float mt = fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]) * p.c;
                 const bool rescale = mt > m_run + kRescaleW;
                 float alpha = 1.f;
                 if (rescale) {
@@ -378,32 +376,44 @@ __global__ void __launch_bounds__(kWThreads, 1)
                     m_run = mt;
                 }
                 const float mu = m_run == -INFINITY ? 0.f : -m_run;   // a row with no visible key yet
-                uint32_t pk[16];
-                float sum = 0.f;
+                const uint64_t cc = f32x2(p.c, p.c);
+                const uint64_t nm = f32x2(mu, mu);
+                uint32_t pk[kWKeys / 2];
+                uint64_t ls[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
                 for (int i = 0; i < kWKeys; i += 2) {
-                    const float p0 = ex2_approx(fmaf(s[i], p.c, mu));
-                    const float p1 = ex2_approx(fmaf(s[i + 1], p.c, mu));
-                    sum += p0 + p1;
+                    float x0, x1;
+                    f32x2_split(ffma2(f32x2(s[i], s[i + 1]), cc, nm), x0, x1);
+                    const float p0 = ex2_approx(x0);
+                    const float p1 = ex2_approx(x1);
+                    ls[(i >> 1) & 3] = fadd2(ls[(i >> 1) & 3], f32x2(p0, p1));
                     pk[i >> 1] = pack_bf16x2(p0, p1);
                 }
-                l = fmaf(l, alpha, sum);
+                float la, lb;
+                f32x2_split(fadd2(fadd2(ls[0], ls[1]), fadd2(ls[2], ls[3])), la, lb);
+                l = fmaf(l, alpha, la + lb);
                 // the previous PV must be done: the P buffer is reused and O must be stable
                 if (t > it.t0) mbar_wait(&o_done, (g - 1) & 1, wc);
                 tc_fence_after();
-                // ragged keys: V rows at or beyond n may hold NaN; P = 0 does not cancel it
-                if (p.seqlens && partial) {
-                    mbar_wait(&v_full[vr.idx], vr.phase, wc);
-                    const int r = row_in_tile;
-                    if (r < kWKeys && t * kWKeys + r >= it.n) {
-                        uint8_t* rowp = smem + kWOffV + vr.idx * kWVBytes + r * 128;
-                        for (int a = 0; a < 4; ++a)
-                            for (int i = 0; i < 8; ++i)
-                                reinterpret_cast<uint4*>(rowp + a * (kWKeys * 128))[i] = make_uint4(0, 0, 0, 0);
+                // ragged keys: V rows at or beyond n may hold NaN, and P = 0 does not cancel it
+                if (p.seqlens && (t + 1) * kWKeys > it.n) {
+                    const int j = t - it.t0;
+                    for (int c = 0; c < kWVChunks; ++c) {
+                        const int r0 = it.n - (t * kWKeys + c * kWVKeys);   // first row to clear in this chunk
+                        if (r0 >= kWVKeys) continue;
+                        const uint32_t pos = gchunk + wv_chunk_pos(j, T, c);
+                        const uint32_t slot = pos % kWSlots;
+                        mbar_wait(&c_full[slot], (pos / kWSlots) & 1, wc);
+                        // 128 threads clear rows max(r0, 0) .. 31: row = thread / 4, one 64-column atom each
+                        const int r = row_in_tile >> 2, a = row_in_tile & 3;
+                        if (r >= (r0 > 0 ? r0 : 0)) {
+                            uint4* rowp = reinterpret_cast<uint4*>(smem + kWOffRing + slot * kWChunkBytes + a * (kWVKeys * 128) + r * 128);
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) rowp[i] = make_uint4(0, 0, 0, 0);
+                        }
                     }
                     fence_proxy_async_smem();
                 }
-                vr.advance();
                 __syncwarp();
                 if (__any_sync(0xffffffffu, rescale) && t > it.t0) {
                     for (int c4 = 0; c4 < kWHalf / 32; ++c4) {
@@ -415,14 +425,18 @@ __global__ void __launch_bounds__(kWThreads, 1)
                         tmem_st32(tmem + lane_base + kWColO + c4 * 32, o);
                     }
                 }
-                tmem_st16(tmem + lane_base + kWColP, pk);
+                tmem_st32(tmem + lane_base + kWColP, pk);
+                tmem_st32(tmem + lane_base + kWColP + 32, pk + 32);
                 tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(&p_full);
             }
+            gchunk += static_cast<uint32_t>(12 * T);
             // ---- epilogue
-            mbar_wait(&o_done, (g - 1) & 1, wc);
-            tc_fence_after();
+            if (T > 0) {
+                mbar_wait(&o_done, (g - 1) & 1, wc);
+                tc_fence_after();
+            }
             const bool store = row < p.R && !aborted(wc);
             const int rr = row < p.R ? row : 0;
             const bool none = !(l > 0.f);   // no visible key in this range: O = 0, LSE = -inf
@@ -696,10 +710,11 @@ int launch_wide(const AttnArgs& a, void* ws, size_t ws_bytes, cudaStream_t st)
     {
         const uint64_t dims[3] = {static_cast<uint64_t>(kWD), static_cast<uint64_t>(a.Skv), static_cast<uint64_t>(heads)};
         const uint64_t strides[2] = {static_cast<uint64_t>(kWD) * 2, static_cast<uint64_t>(a.Skv) * kWD * 2};
-        const uint32_t box[3] = {64, static_cast<uint32_t>(kWKeys), 1};
-        int rc = make_tmap_bf16(&kmap, a.k, 3, dims, strides, box);
+        const uint32_t kbox[3] = {64, static_cast<uint32_t>(kWKeys), 1};    // K chunk: 64 columns x 128 keys
+        const uint32_t vbox[3] = {64, static_cast<uint32_t>(kWVKeys), 1};   // V chunk atom: 64 columns x 32 keys
+        int rc = make_tmap_bf16(&kmap, a.k, 3, dims, strides, kbox);
         if (rc) return rc;
-        rc = make_tmap_bf16(&vmap, a.v, 3, dims, strides, box);
+        rc = make_tmap_bf16(&vmap, a.v, 3, dims, strides, vbox);
         if (rc) return rc;
     }
     WideParams p{};
