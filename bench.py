@@ -36,6 +36,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 TRAFFIC = {
     # decode B8 H32 Sq1 Skv4096 D128: read 537,046,784 + written 2,968,576 bytes (profiles/decode_kernel_decode-B8-H32-Skv4096-D128.md)
     "decode_kernel<128>": {"bytes": 540015360, "source_sha": "a06d9084bc28b581"},
+    # wide-head B32 Hq128 Hkv1 Skv16384 D512: read 1,081,752,000 + written 10,413,312 bytes (profiles/wide_kernel_wide-head-B32-Hq128-Hkv1-Skv16384-D512.md)
+    "wide_kernel": {"bytes": 1092165312, "source_sha": "59bf36ffcd9cc452"},
 }
 
 
@@ -349,10 +351,11 @@ def _workload_entry(F, w, idx, steps, warmup, peaks, causal=False, given_scale=F
     else:
         gbs = w.kv_bytes() / (step_ms / 1e3) / 1e9
         ach = case.algorithmic_bytes() / (kern_ms / 1e3) / 1e9
+        traffic = traffic_for("wide_kernel", "wide.cu") if w.D == 512 else None
         e.update({"value": gbs, "unit": "GB/s", "kv_bytes": w.kv_bytes(), "flops": w.flops(),
                   "tflops": w.flops() / (step_ms / 1e3) / 1e12,
                   "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                               "frac": ach / peaks["hbm_gbs"], "traffic": None}})
+                               "frac": ach / peaks["hbm_gbs"], "traffic": traffic}})
     del case
     torch.cuda.empty_cache()
     return e
