@@ -77,6 +77,9 @@ static thread_local cudaEvent_t g_ev_end = nullptr;
 
 void count_launch(int n) { g_launches.fetch_add(n); }
 
+static std::atomic<unsigned long long> g_call_tag{0};
+unsigned long long next_call_tag() { return ((g_call_tag.fetch_add(1) + 1) & ((1ull << 48) - 1)) | (1ull << 47); }
+
 void timing_mark_begin(cudaStream_t st)
 {
     if (g_ev_begin) cudaEventRecord(g_ev_begin, st);

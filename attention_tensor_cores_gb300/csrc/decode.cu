@@ -84,6 +84,9 @@ struct DecodeParams {
     float* nv_ts;
     float* part_o;           // [slots][16][D]
     float* part_lse;         // [slots][16]
+    int fixup;               // split mode: the CTA completing a unit merges its partials (no combine kernel)
+    unsigned long long gen;  // this call's tag for the arrival counters (48 bits)
+    unsigned long long* unit_ctr;   // [U] arrival counters: (gen << 16) | arrivals
     int* status;
     long long limit;
 };
@@ -217,6 +220,50 @@ __device__ __forceinline__ float warp_sum(float v)
     return v;
 }
 
+// Stream-K: the CTAs holding partials of unit u are c0..c1 of P, skipping CTAs whose tile range is
+// empty (possible when there are fewer tiles than CTAs).  Fills slots[] (partial slots u + c, at
+// most cap) and returns how many there are; 0 for a unit without tiles.
+__device__ int unit_partial_slots(const DecodeParams& p, int u, int P, int* slots, int cap)
+{
+    int tiles;
+    long long Tu, T;
+    if (p.prefix) {
+        tiles = p.prefix[u + 1] - p.prefix[u];
+        Tu = p.prefix[u];
+        T = p.prefix[p.U];
+    } else {
+        tiles = p.tiles_uniform;
+        Tu = static_cast<long long>(u) * tiles;
+        T = static_cast<long long>(p.U) * tiles;
+    }
+    if (tiles <= 0) return 0;
+    const int c0 = static_cast<int>(min((((Tu + 1) * P) - 1) / T, static_cast<long long>(P - 1)));
+    const int c1 = static_cast<int>(min((((Tu + tiles) * P) - 1) / T, static_cast<long long>(P - 1)));
+    int n = 0;
+    for (int c = c0; c <= c1 && n < cap; ++c)
+        if ((static_cast<long long>(c) * T) / P != (static_cast<long long>(c + 1) * T) / P) slots[n++] = u + c;
+    return n;
+}
+
+// Counts one arrival at a unit's counter and returns the count of this call's arrivals so far.
+// The counter carries this call's tag in its upper 48 bits, so whatever an earlier call (or the
+// caller) left in it reads as zero arrivals: no reset between calls is needed.  The CAS loop fails
+// only when another CTA arrived in between, so it ends after at most that many retries.
+__device__ __forceinline__ int arrive_unit(unsigned long long* ctr, unsigned long long gen, int need)
+{
+    // first guess: this arrival completes the unit (one round trip for the CTA that merges)
+    unsigned long long old = (gen << 16) | static_cast<unsigned long long>(need - 1);
+    for (int i = 0; i < 4096; ++i) {
+        const unsigned long long cnt = ((old >> 16) == gen) ? (old & 0xffffull) : 0ull;
+        const unsigned long long prev = atomicCAS(ctr, old, (gen << 16) | (cnt + 1));
+        if (prev == old) return static_cast<int>(cnt + 1);
+        old = prev;
+    }
+    return -1;
+}
+
+constexpr int kMaxFixSlots = 512;
+
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
@@ -233,6 +280,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ int abort_flag;
     __shared__ float red_max[2][4][kN];
     __shared__ float red_sum[4][kN];
+    __shared__ int ep_abort, fx_last;          // softmax warps: abort snapshot, "this CTA merges"
+    __shared__ int fx_n;
+    __shared__ int fx_slot[kMaxFixSlots];
 
     const int warp = threadIdx.x / 32;
     if (blockIdx.x == 0 && threadIdx.x == 0 && p.nv_ts) *p.nv_ts = *p.nv_sg;   // single-pass NVFP4: report s_g
@@ -392,6 +442,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
         const int G = p.G;
         const float nv_sg = p.nv_sg ? *p.nv_sg : 0.f;
+        // final output of one row at column tid (tid < D); the |O| max goes to amax_acc
+        auto write_final = [&](size_t row, float o, float lse_v, float& amax_acc) {
+            if (p.o_stage) p.o_stage[row * D + tid] = o;
+            if (p.amax_bits) amax_acc = fmaxf(amax_acc, fabsf(o));
+            if (p.out) {
+                if (p.out_f32)
+                    static_cast<float*>(p.out)[row * D + tid] = o;
+                else
+                    static_cast<uint16_t*>(p.out)[row * D + tid] = float_to_bf16_bits(o);
+            }
+            if (tid == 0 && p.lse) p.lse[row] = lse_v;
+        };
         Ring sr(2), pr(2), orr(2), vr(S);
         uint32_t tile_ctr = 0;
         while (sched.next(it)) {
@@ -505,7 +567,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int q = 0; q < kN; ++q) L[q] = 0.f;
             }
-            if (__any_sync(0xffffffffu, aborted(wc))) continue;   // warp-uniform (shuffles below)
+            // one abort decision for all four warps (named barriers and shuffles below)
+            if (tid == 0) ep_abort = aborted(wc) ? 1 : 0;
+            named_bar_sync(1, 128);
+            if (ep_abort) continue;
             const bool empty = it.t1 <= it.t0;
             // single-pass NVFP4 in split mode: whole units also go through the combine, which
             // encodes every row in parallel (encoding here would lengthen the CTAs holding many
@@ -521,17 +586,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float lse_v = none ? -INFINITY : (m[q] + __log2f(L[q])) * kLn2;
                     const size_t row = static_cast<size_t>(it.u) * G + q;
                     if (final_here) {
-                        if (p.o_stage) p.o_stage[row * D + tid] = o;
-                        if (p.amax_bits) local_amax = fmaxf(local_amax, fabsf(o));
+                        write_final(row, o, lse_v, local_amax);
                         // single-pass NVFP4: a warp holds 32 consecutive columns of the row
                         if (p.nv_codes) nvfp4_encode_lanes(o, nv_sg, tid, p.nv_codes + row * (D / 2), p.nv_scales + row * (D / 16));
-                        if (p.out) {
-                            if (p.out_f32)
-                                static_cast<float*>(p.out)[row * D + tid] = o;
-                            else
-                                static_cast<uint16_t*>(p.out)[row * D + tid] = float_to_bf16_bits(o);
-                        }
-                        if (tid == 0 && p.lse) p.lse[row] = lse_v;
                     } else {
                         p.part_o[(static_cast<size_t>(it.slot) * kN + q) * D + tid] = o;
                         if (tid == 0) p.part_lse[static_cast<size_t>(it.slot) * kN + q] = lse_v;
@@ -541,6 +598,69 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (p.amax_bits && final_here) {
                 const float wm = warp_max(local_amax);
                 if (lane == 0 && wm > 0.f) atomicMax(p.amax_bits, __float_as_uint(wm));
+            }
+            if (p.fixup && !final_here) {
+                // stream-K fixup: publish this partial, count the unit's arrivals, and let the CTA
+                // that completes the unit merge it (O = sum exp(lse_i - lse) O_i, as the combine)
+                __threadfence();
+                named_bar_sync(1, 128);
+                if (tid == 0) {
+                    const int n = unit_partial_slots(p, it.u, static_cast<int>(gridDim.x), fx_slot, kMaxFixSlots);
+                    fx_n = n;
+                    fx_last = (n > 0 && arrive_unit(p.unit_ctr + it.u, p.gen, n) == n) ? 1 : 0;
+                }
+                named_bar_sync(1, 128);
+                if (fx_last) {
+                    __threadfence();
+                    const int ns = fx_n;
+                    float amax_m = 0.f;
+                    for (int q = 0; q < G; ++q) {
+                        if (ns <= 4) {
+                            // one round of independent loads (all partial LSEs and this column of each
+                            // partial O), then the weights in registers
+                            float lv[4], ov[4];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const size_t sl = static_cast<size_t>(fx_slot[i < ns ? i : 0]) * kN + q;
+                                lv[i] = i < ns ? __ldcg(p.part_lse + sl) : -INFINITY;
+                                ov[i] = (i < ns && tid < D) ? __ldcg(p.part_o + sl * D + tid) : 0.f;
+                            }
+                            const float mx = fmaxf(fmaxf(lv[0], lv[1]), fmaxf(lv[2], lv[3]));
+                            const bool any = mx > -INFINITY;
+                            float sum = 0.f;
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) sum += (any && i < ns) ? __expf(lv[i] - mx) : 0.f;
+                            const float lse_all = any ? mx + __logf(sum) : -INFINITY;
+                            float o = 0.f;
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                if (any && i < ns) o = fmaf(__expf(lv[i] - lse_all), ov[i], o);
+                            if (tid < D) write_final(static_cast<size_t>(it.u) * G + q, o, lse_all, amax_m);
+                            continue;
+                        }
+                        float mx = -INFINITY;
+                        for (int i = 0; i < ns; ++i) mx = fmaxf(mx, __ldcg(p.part_lse + static_cast<size_t>(fx_slot[i]) * kN + q));
+                        // partials without a visible key carry lse = -inf and weigh 0; all of them -> empty row
+                        const bool any = mx > -INFINITY;
+                        float sum = 0.f;
+                        if (any)
+                            for (int i = 0; i < ns; ++i) sum += __expf(__ldcg(p.part_lse + static_cast<size_t>(fx_slot[i]) * kN + q) - mx);
+                        const float lse_all = (ns > 0 && any) ? mx + __logf(sum) : -INFINITY;
+                        if (tid < D) {
+                            float o = 0.f;
+                            if (any)
+                                for (int i = 0; i < ns; ++i) {
+                                    const size_t sl = static_cast<size_t>(fx_slot[i]) * kN + q;
+                                    o = fmaf(__expf(__ldcg(p.part_lse + sl) - lse_all), __ldcg(p.part_o + sl * D + tid), o);
+                                }
+                            write_final(static_cast<size_t>(it.u) * G + q, o, lse_all, amax_m);
+                        }
+                    }
+                    if (p.amax_bits) {
+                        const float wm = warp_max(amax_m);
+                        if (lane == 0 && wm > 0.f) atomicMax(p.amax_bits, __float_as_uint(wm));
+                    }
+                }
             }
         }
     }
@@ -674,7 +794,7 @@ __global__ void combine_kernel(const __grid_constant__ DecodeParams p, int nctas
 namespace {
 
 struct DecodeWs {
-    size_t prefix_off, lse_off, o_off, stage_off, total;
+    size_t prefix_off, ctr_off, lse_off, o_off, stage_off, total;
 };
 
 DecodeWs decode_ws_layout(const AttnArgs& a, bool split, int nsm)
@@ -686,6 +806,8 @@ DecodeWs decode_ws_layout(const AttnArgs& a, bool split, int nsm)
     size_t off = 0;
     w.prefix_off = off;
     off += (split && a.seqlens) ? al((U + 1) * 4) : 0;
+    w.ctr_off = off;
+    off += split ? al(U * 8) : 0;   // fixup arrival counters
     w.lse_off = off;
     off += al(slots * kN * 4);
     w.o_off = off;
@@ -751,6 +873,13 @@ int run_decode(const AttnArgs& a, bool split, void* ws, cudaStream_t st)
     p.nv_ts = a.nv_ts;
     p.part_lse = split ? reinterpret_cast<float*>(base + w.lse_off) : nullptr;
     p.part_o = split ? reinterpret_cast<float*>(base + w.o_off) : nullptr;
+    // Split units are merged in the kernel by the CTA completing them (a unit's last partial lands
+    // at the end of a CTA's range, so the merge costs a few microseconds of tail instead of the
+    // combine launch).  Measured slower for ragged batches, which keep the combine kernel (it also
+    // writes units without keys); single-pass NVFP4 keeps it too (one block per row encodes).
+    p.fixup = (split && !a.nv_sg && !a.seqlens) ? 1 : 0;
+    p.unit_ctr = split ? reinterpret_cast<unsigned long long*>(base + w.ctr_off) : nullptr;
+    p.gen = next_call_tag();
     p.status = device_status_ptr();
     p.limit = wait_limit();
 
@@ -768,7 +897,7 @@ int run_decode(const AttnArgs& a, bool split, void* ws, cudaStream_t st)
         FMHA_CHECK_LAUNCH("decode_kernel");
         count_launch();
     }
-    if (split && U * G > 0) {
+    if (split && !p.fixup && U * G > 0) {
         combine_kernel<<<U * G, D, 0, st>>>(p, grid);
         FMHA_CHECK_LAUNCH("combine_kernel");
         count_launch();

@@ -162,3 +162,41 @@ def test_bad_arguments_return_codes(F):
     assert lib.fmha_fwd_ex(P(q), P(q), P(q), P(out), None, 1, 1, 1, 1, 1, 64, 1.0, s,
                            ctypes.byref(opts)) == F.FMHA_ERR_WORKSPACE
     assert F.fmha_check_status() == 0
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Skv,D", [
+    (1, 8, 1, 160000, 128),   # one unit over every CTA: up to one partial per SM, merged by the last arrival
+    (1, 4, 1, 1000, 64),      # fewer key tiles than CTAs: some CTAs hold no tiles
+    (3, 16, 2, 777, 128),     # several units, partial tail tiles
+])
+def test_split_merge_in_kernel(F, B, Hq, Hkv, Skv, D):
+    """Split-KV units are merged inside the decode kernel by the CTA that completes them."""
+    w = inputs.Workload("t", B, Hq, Hkv, 1, Skv, D, 1.0, "bf16", 37)
+    q, k, v, _ = w.make("cuda")
+    res = run_attention(F, q, k, v, w.scale, num_splits=0)
+    o_ref, l_ref = oracle.attention(q.cpu(), k.cpu(), v.cpu(), w.scale)
+    check_o_lse(res["o"], res["lse"], o_ref, l_ref, "in-kernel merge")
+
+
+def test_merge_counters_across_calls(F):
+    """Arrival counters are tagged per call, not reset: repeated calls on one workspace (and a
+    workspace first filled with arbitrary bytes) give identical results."""
+    w = inputs.Workload("t", 4, 8, 2, 1, 5000, 128, 1.0, "bf16", 38)
+    q, k, v, _ = w.make("cuda")
+    B, Hq, Sq, D = q.shape
+    opts = F.make_opts(F.FMHA_OUT_BF16, None, 0)
+    wsb = F.fmha_workspace_size(B, Hq, w.Hkv, Sq, w.Skv, D, opts)
+    ws = torch.randint(0, 256, (wsb,), dtype=torch.uint8, device="cuda")
+    opts = F.make_opts(F.FMHA_OUT_BF16, None, 0, ws)
+    outs = []
+    for _ in range(3):
+        out = torch.full((B, Hq, Sq, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty(B, Hq, Sq, dtype=torch.float32, device="cuda")
+        F.fmha_fwd_ex(q, k, v, out, lse, w.scale, opts)
+        outs.append(out.float().cpu().numpy())
+    torch.cuda.synchronize()
+    assert F.fmha_check_status() == 0
+    o_ref, l_ref = oracle.attention(q.cpu(), k.cpu(), v.cpu(), w.scale)
+    check_o_lse(outs[0].reshape(-1, D), None, o_ref, l_ref, "merge across calls")
+    np.testing.assert_array_equal(outs[0], outs[1])
+    np.testing.assert_array_equal(outs[0], outs[2])
