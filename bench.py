@@ -34,8 +34,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # named kernel, with the sha256 of its source file at capture time; reported only while the
 # source is unchanged.
 TRAFFIC = {
-    # decode B8 H32 Sq1 Skv4096 D128: read 537,046,784 + written 2,968,576 bytes (profiles/decode_kernel_decode-B8-H32-Skv4096-D128.md)
-    "decode_kernel<128>": {"bytes": 540015360, "source_sha": "a06d9084bc28b581"},
+    # decode B8 H32 Sq1 Skv4096 D128: read 537,082,112 + written 3,287,552 bytes (profiles/decode_kernel_decode-B8-H32-Skv4096-D128.md)
+    "decode_kernel<128>": {"bytes": 540369664, "source_sha": "0d95a88e0f8e3f9b"},
     # wide-head B32 Hq128 Hkv1 Skv16384 D512: read 1,081,752,000 + written 10,413,312 bytes (profiles/wide_kernel_wide-head-B32-Hq128-Hkv1-Skv16384-D512.md)
     "wide_kernel": {"bytes": 1092165312, "source_sha": "59bf36ffcd9cc452"},
 }
