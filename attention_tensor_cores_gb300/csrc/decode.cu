@@ -178,10 +178,6 @@ __device__ __forceinline__ uint32_t sw128_offset(int r, int k, uint32_t atom_byt
     return a * atom_bytes + r * 128 + ((((kk >> 3) ^ (r & 7)) & 7) << 4) + ((kk & 7) << 1);
 }
 
-__device__ __forceinline__ void named_bar_sync(int id, int n)
-{
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
 
 // Bounded wait that ignores the abort flag: used at teardown so nothing is still in flight.
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, long long limit)
@@ -243,23 +239,6 @@ __device__ int unit_partial_slots(const DecodeParams& p, int u, int P, int* slot
     for (int c = c0; c <= c1 && n < cap; ++c)
         if ((static_cast<long long>(c) * T) / P != (static_cast<long long>(c + 1) * T) / P) slots[n++] = u + c;
     return n;
-}
-
-// Counts one arrival at a unit's counter and returns the count of this call's arrivals so far.
-// The counter carries this call's tag in its upper 48 bits, so whatever an earlier call (or the
-// caller) left in it reads as zero arrivals: no reset between calls is needed.  The CAS loop fails
-// only when another CTA arrived in between, so it ends after at most that many retries.
-__device__ __forceinline__ int arrive_unit(unsigned long long* ctr, unsigned long long gen, int need)
-{
-    // first guess: this arrival completes the unit (one round trip for the CTA that merges)
-    unsigned long long old = (gen << 16) | static_cast<unsigned long long>(need - 1);
-    for (int i = 0; i < 4096; ++i) {
-        const unsigned long long cnt = ((old >> 16) == gen) ? (old & 0xffffull) : 0ull;
-        const unsigned long long prev = atomicCAS(ctr, old, (gen << 16) | (cnt + 1));
-        if (prev == old) return static_cast<int>(cnt + 1);
-        old = prev;
-    }
-    return -1;
 }
 
 constexpr int kMaxFixSlots = 512;
@@ -877,7 +856,7 @@ int run_decode(const AttnArgs& a, bool split, void* ws, cudaStream_t st)
     // at the end of a CTA's range, so the merge costs a few microseconds of tail instead of the
     // combine launch).  Measured slower for ragged batches, which keep the combine kernel (it also
     // writes units without keys); single-pass NVFP4 keeps it too (one block per row encodes).
-    p.fixup = (split && !a.nv_sg && !a.seqlens) ? 1 : 0;
+    p.fixup = (split && !a.nv_sg && !a.seqlens && nsm <= kMaxFixSlots) ? 1 : 0;
     p.unit_ctr = split ? reinterpret_cast<unsigned long long*>(base + w.ctr_off) : nullptr;
     p.gen = next_call_tag();
     p.status = device_status_ptr();

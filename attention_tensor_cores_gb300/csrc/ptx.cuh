@@ -143,6 +143,29 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
     }
 }
 
+// Named barrier over the first n threads' warps (id 1..15; 0 is __syncthreads).
+__device__ __forceinline__ void named_bar_sync(int id, int n)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// Counts one arrival at a unit's counter and returns the count of this call's arrivals so far.
+// The counter carries this call's tag in its upper 48 bits, so whatever an earlier call (or the
+// caller) left in it reads as zero arrivals: no reset between calls is needed.  The CAS loop fails
+// only when another CTA arrived in between, so it ends after at most that many retries.
+__device__ __forceinline__ int arrive_unit(unsigned long long* ctr, unsigned long long gen, int need)
+{
+    // first guess: this arrival completes the unit (one round trip for the CTA that merges)
+    unsigned long long old = (gen << 16) | static_cast<unsigned long long>(need - 1);
+    for (int i = 0; i < 4096; ++i) {
+        const unsigned long long cnt = ((old >> 16) == gen) ? (old & 0xffffull) : 0ull;
+        const unsigned long long prev = atomicCAS(ctr, old, (gen << 16) | (cnt + 1));
+        if (prev == old) return static_cast<int>(cnt + 1);
+        old = prev;
+    }
+    return -1;
+}
+
 // Bounded wait with cluster-scope acquire (for barriers that CTAs of the cluster arrive on).
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, const WaitCtl& w);
 
