@@ -66,7 +66,6 @@ struct DecodeParams {
     int Skv;
     int D;
     int Sq;             // query rows per head (column q of a unit is query q % Sq)
-    int causal;         // bottom-right aligned causal mask
     float c;            // scale * log2(e)
     const int32_t* seqlens;
     const int32_t* prefix;   // [U+1] tile prefix (ragged split mode), else NULL
@@ -834,7 +833,6 @@ int run_decode(const AttnArgs& a, bool split, void* ws, cudaStream_t st)
     p.Skv = a.Skv;
     p.D = D;
     p.Sq = a.Sq > 0 ? a.Sq : 1;
-    p.causal = a.causal;
     p.c = a.scale * kLog2e;
     p.seqlens = a.seqlens;
     p.tiles_uniform = (a.Skv + kTileKV - 1) / kTileKV;

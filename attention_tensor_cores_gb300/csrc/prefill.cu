@@ -80,7 +80,6 @@ struct PrefillParams {
     int Skv;
     int pairs;      // ceil(R / 256)
     int Sq;         // query rows per head: row r of a unit is query r % Sq
-    int causal;     // bottom-right aligned causal mask
     int group;      // causal item order: units per group
     int* sched;     // global work-item counter (zeroed before the launch), NULL = fixed order
     float c;        // scale * log2(e)
@@ -656,7 +655,6 @@ int run_prefill(const AttnArgs& a, bool dynamic, void* ws, cudaStream_t st)
     p.Skv = a.Skv;
     p.pairs = (R + 2 * kTM - 1) / (2 * kTM);
     p.Sq = a.Sq > 0 ? a.Sq : 1;
-    p.causal = a.causal;
     // causal item groups: as many units as keep their K and V within 32 MiB of L2
     const size_t unit_kv = static_cast<size_t>(a.Skv) * D * 2 * 2;
     const size_t g = (size_t(32) << 20) / (unit_kv ? unit_kv : 1);

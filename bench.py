@@ -503,7 +503,7 @@ def main():
             case.call()
         torch.cuda.synchronize()
         assert F.fmha_check_status() == 0
-        print(f"profile run of {case.w.name}: {args.repeat} calls ok")
+        print(f"profile run of {case.w.name} ({args.profile}): {args.repeat} calls ok")
         return
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
