@@ -43,6 +43,7 @@ constexpr int kN = 16;          // query rows per unit, padded (MMA N)
 constexpr int kThreads = 192;   // 4 softmax warps + producer + MMA
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleD = 8.0f;   // log2 units: a column's reference max moves only when exceeded by more
 
 template <int D>
 struct DecodeCfg {
@@ -257,6 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
     __shared__ float red_max[2][4][kN];
+    __shared__ uint32_t red_need[2][4];   // per warp: columns whose scores passed the reference + kRescaleD
     __shared__ float red_sum[4][kN];
     __shared__ int ep_abort, fx_last;          // softmax warps: abort snapshot, "this CTA merges"
     __shared__ int fx_n;
@@ -475,25 +477,42 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float x[kN];
 #pragma unroll
                 for (int q = 0; q < kN; ++q) x[q] = (CAUSAL ? kv < lim[q] : valid) ? __uint_as_float(sv[q]) * p.c : -INFINITY;
+                // Lazy column max (as the row-tile kernel's lazy rescale): the reference m[q] moves only
+                // when some score of column q exceeds it by more than 2^8, so P <= 256 and the final
+                // O = acc / L and LSE = m + log2 L are exact for any reference.  Usually no column
+                // moves and no max is reduced: one OR of flags across the four warps decides.
                 float(*rb)[kN] = red_max[tile_ctr & 1];
+                uint32_t need = 0;
 #pragma unroll
                 for (int q = 0; q < kN; ++q)
-                    if (q < G) {
-                        const float mx = warp_max(x[q]);
-                        if (lane == 0) rb[warp][q] = mx;
-                    }
+                    if (q < G && x[q] > m[q] + kRescaleD) need |= 1u << q;
+                need = __reduce_or_sync(0xffffffffu, need);
+                if (lane == 0) red_need[tile_ctr & 1][warp] = need;
                 named_bar_sync(1, 128);
+                need = red_need[tile_ctr & 1][0] | red_need[tile_ctr & 1][1] | red_need[tile_ctr & 1][2] | red_need[tile_ctr & 1][3];
+                if (need) {   // the same value in all four warps
+#pragma unroll
+                    for (int q = 0; q < kN; ++q)
+                        if ((need >> q) & 1u) {
+                            const float mx = warp_max(x[q]);
+                            if (lane == 0) rb[warp][q] = mx;
+                        }
+                    named_bar_sync(1, 128);
+                }
                 ++tile_ctr;
                 float alpha[kN], pv[kN];
 #pragma unroll
                 for (int q = 0; q < kN; ++q) {
                     if (q < G) {
-                        const float mt = fmaxf(fmaxf(rb[0][q], rb[1][q]), fmaxf(rb[2][q], rb[3][q]));
-                        const float mn = fmaxf(m[q], mt);
-                        // causal: a column with no visible key so far keeps m = -inf (no -inf - -inf)
-                        alpha[q] = (CAUSAL && m[q] == -INFINITY) ? 0.f : ex2_approx(m[q] - mn);
-                        m[q] = mn;
-                        pv[q] = ex2_approx(x[q] - ((CAUSAL && mn == -INFINITY) ? 0.f : mn));
+                        alpha[q] = 1.f;
+                        if ((need >> q) & 1u) {
+                            const float mt = fmaxf(fmaxf(rb[0][q], rb[1][q]), fmaxf(rb[2][q], rb[3][q]));
+                            // a column without a finite reference yet has nothing to rescale
+                            alpha[q] = m[q] == -INFINITY ? 0.f : ex2_approx(m[q] - mt);
+                            m[q] = mt;
+                        }
+                        // a column with no visible key so far keeps m = -inf (no -inf - -inf)
+                        pv[q] = m[q] == -INFINITY ? 0.f : ex2_approx(x[q] - m[q]);
                         l[q] = fmaf(l[q], alpha[q], pv[q]);
                     } else {
                         alpha[q] = 0.f;

@@ -34,8 +34,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # named kernel, with the sha256 of its source file at capture time; reported only while the
 # source is unchanged.
 TRAFFIC = {
-    # decode B8 H32 Sq1 Skv4096 D128: read 537,122,304 + written 2,827,520 bytes (profiles/decode_kernel_decode-B8-H32-Skv4096-D128.md)
-    "decode_kernel<128>": {"bytes": 539949824, "source_sha": "5c045a3d40d766f7"},
+    # decode B8 H32 Sq1 Skv4096 D128: read 537,084,928 + written 3,311,616 bytes (profiles/decode_kernel_decode-B8-H32-Skv4096-D128.md)
+    "decode_kernel<128>": {"bytes": 540396544, "source_sha": "5ae4f8c85541c707"},
     # wide-head B32 Hq128 Hkv1 Skv16384 D512: read 1,081,752,000 + written 10,413,312 bytes (profiles/wide_kernel_wide-head-B32-Hq128-Hkv1-Skv16384-D512.md)
     "wide_kernel": {"bytes": 1092165312, "source_sha": "59bf36ffcd9cc452"},
 }
@@ -127,6 +127,15 @@ def traffic_for(kernel: str, src: str, launches_per_step: int = 1):
     if not t or t.get("source_sha") != source_sha(src):
         return None
     return t["bytes"]
+
+
+def spec_decode_workload():
+    """Decode with 4 new tokens per head under the causal mask (speculative or chunked decode):
+    B8 Hq32 Hkv8 Sq4 Skv8192 D128, 16 query rows per key/value head, BF16 out (an extra line, not one
+    of the five specified configurations)."""
+    from attention_tensor_cores_gb300 import inputs
+    return inputs.Workload("speculative decode B8 Hq32 Hkv8 Sq4 Skv8192 D128 (causal, BF16 out)",
+                           8, 32, 8, 4, 8192, 128, 1.0, "bf16", 1006)
 
 
 # ------------------------------------------------------------------------------------------------
@@ -412,6 +421,10 @@ def run_ours(args, rank, world, local):
             extra["c5_given_scale"]["workload"] = wl[4].name.replace("(NVFP4 out)", "(NVFP4 out, one pass with a given scale)")
         except F.FmhaError as ex:
             extra["c5_given_scale"] = {"workload": "ragged NVFP4, given scale", "unsupported": str(ex)}
+        try:   # decode with several new tokens per head (speculative or chunked decode), causal mask
+            extra["c2_spec_causal"] = _workload_entry(F, spec_decode_workload(), 1, min(args.steps, 10), args.warmup, peaks, causal=True)
+        except F.FmhaError as ex:
+            extra["c2_spec_causal"] = {"workload": "speculative decode", "unsupported": str(ex)}
         try:   # the prefill workload with the causal mask
             extra["c3_causal"] = _workload_entry(F, wl[2], 2, min(args.steps, 10), args.warmup, peaks, causal=True)
             extra["c3_causal"]["workload"] = wl[2].name.replace("non-causal", "causal")
@@ -484,7 +497,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--only-headline", action="store_true", help="skip the other workloads")
-    ap.add_argument("--profile", choices=["c1", "c2", "c3", "c4", "c5", "c3_causal", "c5_given_scale"], default=None,
+    ap.add_argument("--profile", choices=["c1", "c2", "c3", "c4", "c5", "c3_causal", "c5_given_scale", "c2_spec_causal"], default=None,
                     help="run one workload's call --repeat times, untimed (for a profiler)")
     ap.add_argument("--repeat", type=int, default=5)
     args = ap.parse_args()
@@ -494,7 +507,8 @@ def main():
         ge.build()
         import attention_tensor_cores_gb300 as F
         from attention_tensor_cores_gb300 import inputs
-        case = Case(F, inputs.workloads()[int(args.profile[1]) - 1], num_splits=0, causal=args.profile == "c3_causal")
+        w = spec_decode_workload() if args.profile == "c2_spec_causal" else inputs.workloads()[int(args.profile[1]) - 1]
+        case = Case(F, w, num_splits=0, causal=args.profile in ("c3_causal", "c2_spec_causal"))
         if args.profile == "c5_given_scale":   # one two-pass call gives the scale the rest reuse
             case.call()
             torch.cuda.synchronize()

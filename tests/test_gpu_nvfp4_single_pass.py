@@ -115,3 +115,17 @@ def test_standalone_scaled_quantiser_ties(F):
     codes, scales = oracle.nvfp4_quantize_scaled(x, sg)
     np.testing.assert_array_equal(sc.cpu().numpy(), scales)
     np.testing.assert_array_equal(q.cpu().numpy(), codes)
+
+
+def test_two_pass_reports_amax(F):
+    """Two-pass NVFP4 with opts.out_amax: the caller's word is the |O| max the quantiser uses, so it
+    equals max |O| of the FP32 output and s_g = fp32(amax / 2688)."""
+    w = inputs.Workload("t", 2, 4, 4, 160, 520, 64, 1.0, "nvfp4", 93)
+    q, k, v, _ = w.make("cuda")
+    a = run_attention(F, q, k, v, w.scale, out_kind="nvfp4", num_splits=0, want_f32=True, want_amax=True)
+    amax = float(np.abs(a["o"]).max())
+    assert a["amax"] == amax
+    assert a["tensor_scale"] == float(np.float32(np.float64(np.float32(amax)) / 2688.0))
+    codes, scales, sg = oracle.nvfp4_quantize(a["o"].reshape(-1))
+    np.testing.assert_array_equal(a["codes"], codes)
+    np.testing.assert_array_equal(a["scales"], scales)
