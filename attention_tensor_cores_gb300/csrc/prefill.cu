@@ -36,7 +36,6 @@ namespace fmha {
 namespace {
 
 constexpr int kTM = 128;          // query rows per tile (MMA M)
-constexpr int kTN = 128;          // keys per tile
 // Threads: 2 softmax warpgroups + TMA warp + MMA warp.  The counter-order kernel adds two idle warps
 // so that its third warpgroup is whole (setmaxnreg acts on whole warpgroups) and splits registers:
 // the launch gives every thread 168 (384 x 168 = 64512 of the SM's 65536); the third warpgroup drops
@@ -57,9 +56,13 @@ constexpr int kItemSlots = 4;     // work-item ring between the TMA warp and the
 
 template <int D>
 struct PrefillCfg {
+    // Keys per tile: 128 at D = 64; 64 at D = 128, so that S (double-buffered over the two query
+    // tiles), separate P buffers and O fit the 512 Tensor Memory columns and QK(j + 1) can run
+    // while the softmax of tile j still owns its P.
+    static constexpr int kTN = (D == 64) ? 128 : 64;
     static constexpr int kAtoms = D / 64;
     static constexpr int kQStages = (D == 64) ? 2 : 1;
-    static constexpr int kStages = (D == 64) ? 4 : 2;
+    static constexpr int kStages = 4;
     static constexpr int kQTileBytes = kAtoms * kTM * 128;
     static constexpr int kQBytes = 2 * kQTileBytes;
     static constexpr int kKVBytes = kAtoms * kTN * 128;
@@ -67,10 +70,12 @@ struct PrefillCfg {
     static constexpr int kOffK = kOffQ + kQStages * kQBytes;
     static constexpr int kOffV = kOffK + kStages * kKVBytes;
     static constexpr int kSmemBytes = kOffV + kStages * kKVBytes + 1024;
-    static constexpr bool kAliasP = (D != 64);
-    static constexpr uint32_t kColP = kAliasP ? 0u : 256u;     // P_q at kColP + q * kPStride
-    static constexpr uint32_t kPStride = kAliasP ? 128u : 64u;
-    static constexpr uint32_t kColO = kAliasP ? 256u : 384u;   // O_q at kColO + q * D
+    // Tensor Memory columns: S_q at q * kTN, P_q (BF16 pairs) at kColP + q * kPStride, O_q at kColO + q * D
+    static constexpr uint32_t kColP = 2 * kTN;
+    static constexpr uint32_t kPStride = kTN / 2;
+    static constexpr uint32_t kColO = 512 - 2 * D;
+    static_assert(kColP + 2 * kPStride <= kColO, "Tensor Memory layout");
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 };
 
 struct PrefillParams {
@@ -124,7 +129,7 @@ __device__ __forceinline__ void item_coords(const PrefillParams& p, int r, int& 
 
 // Key tiles query tile q of a pair needs: none when its rows are all past R; with the causal
 // mask only those up to the last key its rows can see (row r sees keys < r % Sq + n - Sq + 1).
-template <bool CAUSAL>
+template <bool CAUSAL, int kTN>
 __device__ __forceinline__ int tile_count(const PrefillParams& p, int pair, int q, int n)
 {
     const int a = pair * 2 * kTM + q * kTM;
@@ -170,6 +175,7 @@ __global__ void __launch_bounds__(prefill_threads<RING>(), 1)
 {
     using C = PrefillCfg<D>;
     constexpr int S = C::kStages;
+    constexpr int kTN = C::kTN;
     constexpr int QS = C::kQStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -249,7 +255,7 @@ __global__ void __launch_bounds__(prefill_threads<RING>(), 1)
                     item_coords<CAUSAL>(p, item, u, pair);
                     const int r0 = pair * 2 * kTM;
                     const int n = unit_keys(p, u);
-                    const int T = max(tile_count<CAUSAL>(p, pair, 0, n), tile_count<CAUSAL>(p, pair, 1, n));
+                    const int T = max(tile_count<CAUSAL, C::kTN>(p, pair, 0, n), tile_count<CAUSAL, C::kTN>(p, pair, 1, n));
                     // the next item is claimed once this one's loads are issued, so a CTA takes new
                     // work only shortly before it runs out
                     const int next = item + static_cast<int>(gridDim.x);
@@ -324,7 +330,7 @@ __global__ void __launch_bounds__(prefill_threads<RING>(), 1)
                     int u, pair;
                     item_coords<CAUSAL>(p, item, u, pair);
                     const int n = unit_keys(p, u);
-                    const int Tq[2] = {tile_count<CAUSAL>(p, pair, 0, n), tile_count<CAUSAL>(p, pair, 1, n)};
+                    const int Tq[2] = {tile_count<CAUSAL, C::kTN>(p, pair, 0, n), tile_count<CAUSAL, C::kTN>(p, pair, 1, n)};
                     const int T = max(Tq[0], Tq[1]);
                     if (T == 0) continue;
                     mbar_wait(&q_full[qr.idx], qr.phase, wc);
@@ -341,15 +347,12 @@ __global__ void __launch_bounds__(prefill_threads<RING>(), 1)
                                 const uint32_t g = gtile + jq[q];
                                 bool ok = mbar_test(&k_full[g % S], (g / S) & 1);
                                 if (ok && nqk[q] > 0) ok = mbar_test(&s_free[q], (nqk[q] - 1) & 1);
-                                // P aliases S: the previous PV must have been issued and have finished reading P
-                                if (ok && C::kAliasP && nqk[q] > 0)
-                                    ok = npv[q] == nqk[q] && mbar_test(&o_done[q], (npv[q] - 1) & 1);
                                 if (ok) {
                                     tc_fence_after();
                                     // descriptors once; K steps add constant offsets to the address fields
                                     const uint64_t dq = sdesc_sw128(sQ + q * C::kQTileBytes, 16, 1024);
                                     const uint64_t dk = sdesc_sw128(smem_u32(smem + C::kOffK + (g % S) * C::kKVBytes), 16, 1024);
-                                    const uint32_t dS = tmem + q * 128;
+                                    const uint32_t dS = tmem + q * kTN;
     #pragma unroll
                                     for (int kk = 0; kk < D / 16; ++kk)
                                         mma_ss(dS, dq + (((kk >> 2) * (kTM * 128) + (kk & 3) * 32) >> 4),
@@ -408,7 +411,7 @@ __global__ void __launch_bounds__(prefill_threads<RING>(), 1)
         const int wl = warp % 4;
         const uint32_t lane_base = static_cast<uint32_t>(wl * 32) << 16;
         const int row_in_tile = wl * 32 + static_cast<int>(lane_id());
-        const uint32_t tS = tmem + lane_base + q * 128;
+        const uint32_t tS = tmem + lane_base + q * kTN;
         const uint32_t tP = tmem + lane_base + C::kColP + q * C::kPStride;
         const uint32_t tO = tmem + lane_base + C::kColO + q * D;
         const float nv_sg = (RING && p.nv_sg) ? *p.nv_sg : 0.f;
@@ -435,7 +438,7 @@ __global__ void __launch_bounds__(prefill_threads<RING>(), 1)
             item_coords<CAUSAL>(p, item, u, pair);
             const int row = pair * 2 * kTM + q * kTM + row_in_tile;
             const int n = unit_keys(p, u);
-            const int T = tile_count<CAUSAL>(p, pair, q, n);
+            const int T = tile_count<CAUSAL, C::kTN>(p, pair, q, n);
             // keys this row sees: 0 .. lim - 1
             const int lim = CAUSAL ? min(n, (row < p.R ? row : 0) % p.Sq + n - p.Sq + 1) : n;
             float m_run = -INFINITY, l = 0.f;
@@ -525,8 +528,8 @@ __global__ void __launch_bounds__(prefill_threads<RING>(), 1)
                     fence_proxy_async_smem();
                 }
                 __syncwarp();
-                tmem_st32(tP, pk);
-                tmem_st32(tP + 32, pk + 32);
+#pragma unroll
+                for (int c = 0; c < kTN / 64; ++c) tmem_st32(tP + c * 32, pk + c * 32);
                 tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(&p_full[q]);
@@ -538,7 +541,7 @@ __global__ void __launch_bounds__(prefill_threads<RING>(), 1)
             }
             // The TMEM loads below are warp-collective: every lane executes them; only the stores
             // are predicated on the row existing.
-            gring += max(tile_count<CAUSAL>(p, pair, 0, n), tile_count<CAUSAL>(p, pair, 1, n));
+            gring += max(tile_count<CAUSAL, C::kTN>(p, pair, 0, n), tile_count<CAUSAL, C::kTN>(p, pair, 1, n));
             const bool store = row < p.R && !aborted(wc);
             const size_t orow = static_cast<size_t>(u) * p.R + (row < p.R ? row : 0);
             const bool none = !(l > 0.f);   // no visible key: O = 0, LSE = -inf
@@ -642,7 +645,7 @@ int run_prefill(const AttnArgs& a, bool dynamic, void* ws, cudaStream_t st)
     {
         const uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(a.Skv), static_cast<uint64_t>(U)};
         const uint64_t strides[2] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(a.Skv) * D * 2};
-        const uint32_t box[3] = {64, static_cast<uint32_t>(kTN), 1};
+        const uint32_t box[3] = {64, static_cast<uint32_t>(C::kTN), 1};
         int rc = make_tmap_bf16(&kmap, a.k, 3, dims, strides, box);
         if (rc) return rc;
         rc = make_tmap_bf16(&vmap, a.v, 3, dims, strides, box);

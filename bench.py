@@ -425,6 +425,13 @@ def run_ours(args, rank, world, local):
             extra["c2_spec_causal"] = _workload_entry(F, spec_decode_workload(), 1, min(args.steps, 10), args.warmup, peaks, causal=True)
         except F.FmhaError as ex:
             extra["c2_spec_causal"] = {"workload": "speculative decode", "unsupported": str(ex)}
+        try:   # the prefill workload at head dim 128
+            from attention_tensor_cores_gb300 import inputs as _inputs
+            w128 = _inputs.Workload("prefill B4 H16 Sq8192 Skv8192 D128 (non-causal, BF16 out)", 4, 16, 16, 8192, 8192,
+                                    128, 1.0, "bf16", 1007)
+            extra["c3_d128"] = _workload_entry(F, w128, 2, min(args.steps, 10), args.warmup, peaks)
+        except F.FmhaError as ex:
+            extra["c3_d128"] = {"workload": "prefill D128", "unsupported": str(ex)}
         try:   # the prefill workload with the causal mask
             extra["c3_causal"] = _workload_entry(F, wl[2], 2, min(args.steps, 10), args.warmup, peaks, causal=True)
             extra["c3_causal"]["workload"] = wl[2].name.replace("non-causal", "causal")
