@@ -18,7 +18,8 @@
  *   - Grouped-query attention: query head hq reads key/value head hq / (Hq / Hkv).
  *   - LSE is the natural logarithm of sum_j exp(scale * q.k_j) (scale included), FP32.
  *   - A key set of size 0 (seqlens_k[b] == 0) gives O = 0 and LSE = -inf.
- *   - Pointers must be 16-byte aligned.  D must be 64, 128 or 512 (16 is also accepted by
+ *   - Tensor pointers must be 16-byte aligned (LSE, seqlens_k, nvfp4_scale_in and out_amax:
+ *     4-byte; the workspace: 256-byte).  D must be 64, 128 or 512 (16 is also accepted by
  *     fmha_qk_gemm).
  *   - Return value: FMHA_OK or an fmha_status code; nothing aborts or throws.  A failed call
  *     leaves a message for fmha_error_string(code) / fmha_last_error() of the calling thread.
@@ -82,7 +83,7 @@ typedef struct {
                                  *out_tensor_scale receives s_g.  NULL: s_g = fp32(max|O| / 2688)
                                  of this O (two passes) */
     float* out_amax;          /* optional, NVFP4 only: device float[1], receives max|O| (FP32) of
-                                 this call */
+                                 this call (with two passes it is also the max the quantiser uses) */
 } fmha_opts;
 
 /*
@@ -126,7 +127,8 @@ size_t nvfp4_scales_bytes(int64_t n);
  * float[1] holding s_g.  q: n/2 bytes of E2M1 codes (as nvfp4_quantize); scales: n/16 bytes of
  * E4M3 block scales (no trailing s_g).  Same roundings as nvfp4_quantize; blocks beyond
  * 6 * 448 * s_g saturate and an s_g that is not a positive finite number gives all zeros.
- * Errors: FMHA_ERR_INVALID for NULL pointers, n < 0, n % 16 != 0 or x, q not 16-byte aligned.
+ * Errors: FMHA_ERR_INVALID for NULL pointers, n < 0, n % 16 != 0, or x not 16-byte, q not 8-byte
+ * or tensor_scale not 4-byte aligned.
  */
 int nvfp4_quantize_scaled(const float* x, uint8_t* q, uint8_t* scales, int64_t n, const float* tensor_scale,
                           fmha_stream_t stream);
