@@ -129,6 +129,25 @@ def traffic_for(kernel: str, src: str, launches_per_step: int = 1):
     return t["bytes"]
 
 
+def causal_flops(w) -> int:
+    """FLOPs of the two contractions under the bottom-right causal mask: query i of Sq sees
+    min(n, max(0, i + n - Sq + 1)) of a sequence's n keys, 4 * D FLOPs per (query, key) pair."""
+    import numpy as np
+    sl = w.seqlens()
+    ns = [w.Skv] * w.B if sl is None else [int(x) for x in sl]
+    i = np.arange(w.Sq, dtype=np.int64)
+    pairs = sum(int(np.clip(i + n - w.Sq + 1, 0, n).sum()) for n in ns)
+    return 4 * w.D * w.Hq * pairs
+
+
+def chunked_prefill_workload():
+    """Chunked prefill over a ragged KV cache: 1024 new causal query tokens per sequence, key
+    lengths drawn from U{1..8192} (seed 1008), B8 Hq=Hkv=16 D128, BF16 out (an extra line)."""
+    from attention_tensor_cores_gb300 import inputs
+    return inputs.Workload("chunked prefill B8 H16 Sq1024 Skv<=8192 D128 (ragged, causal, BF16 out)",
+                           8, 16, 16, 1024, 8192, 128, 1.0, "bf16", 1008, ragged=True)
+
+
 def spec_decode_workload():
     """Decode with 4 new tokens per head under the causal mask (speculative or chunked decode):
     B8 Hq32 Hkv8 Sq4 Skv8192 D128, 16 query rows per key/value head, BF16 out (an extra line, not one
@@ -348,8 +367,7 @@ def _workload_entry(F, w, idx, steps, warmup, peaks, causal=False, given_scale=F
     kern_ms = statistics.mean(r["kernel_ms"])
     e = {"workload": w.name, "ms_per_step": step_ms, "kernel_ms": kern_ms, "gpu_launches_per_step": r["launches"] / steps}
     if idx == 2:   # prefill: tensor-bound
-        # causal (Sq = Skv): query i sees i + 1 keys, so the contractions do 4 D sum_i (i + 1) FLOP per head
-        flops = 4 * w.D * w.B * w.Hq * (w.Sq * (w.Sq + 1) // 2) if causal else w.flops()
+        flops = causal_flops(w) if causal else w.flops()
         tf = flops / (step_ms / 1e3) / 1e12
         ach = flops / (kern_ms / 1e3) / 1e12
         e["flops"] = flops
@@ -433,6 +451,11 @@ def run_ours(args, rank, world, local):
             extra["c3_d128"] = _workload_entry(F, w128, 2, min(args.steps, 10), args.warmup, peaks)
         except F.FmhaError as ex:
             extra["c3_d128"] = {"workload": "prefill D128", "unsupported": str(ex)}
+        try:   # chunked prefill: ragged key lengths, causal, work items from the workspace counter
+            extra["c3_chunked_varlen"] = _workload_entry(F, chunked_prefill_workload(), 2, min(args.steps, 10), args.warmup,
+                                                         peaks, causal=True)
+        except F.FmhaError as ex:
+            extra["c3_chunked_varlen"] = {"workload": "chunked prefill", "unsupported": str(ex)}
         try:   # the prefill workload with the causal mask
             extra["c3_causal"] = _workload_entry(F, wl[2], 2, min(args.steps, 10), args.warmup, peaks, causal=True)
             extra["c3_causal"]["workload"] = wl[2].name.replace("non-causal", "causal")

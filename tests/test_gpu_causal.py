@@ -117,3 +117,21 @@ def test_causal_workspace_reuse_back_to_back(F):
     for o, l in outs:
         check_o_lse(o, l, o_ref, l_ref, "causal back to back")
     np.testing.assert_array_equal(outs[0][0], outs[1][0])
+
+
+@pytest.mark.parametrize("num_splits", [0, 1])
+def test_chunked_prefill_ragged_causal_d128(F, num_splits):
+    """Chunked prefill over a ragged KV cache at D = 128: 300 new queries per sequence against
+    ragged key counts, some shorter than the query chunk (their first queries see no key), NaN in the
+    padding; counter order (workspace) and fixed order."""
+    B, H, Sq, Skv, D = 4, 2, 300, 1000, 128
+    sl = [1000, 120, 301, 777]
+    w = inputs.Workload("t", B, H, H, Sq, Skv, D, 1.0, "bf16", 86)
+    q, k, v, _ = w.make("cuda")
+    for b, n in enumerate(sl):
+        k[b, :, n:] = float("nan")
+        v[b, :, n:] = float("nan")
+    sl_t = torch.tensor(sl, dtype=torch.int32, device="cuda")
+    res = run_attention(F, q, k, v, w.scale, seqlens=sl_t, num_splits=num_splits, causal=True)
+    o_ref, l_ref = oracle.attention(q.cpu(), k.cpu(), v.cpu(), w.scale, seqlens_k=np.array(sl, np.int32), causal=True)
+    check_o_lse(res["o"], res["lse"], o_ref, l_ref, "chunked prefill")
