@@ -600,7 +600,29 @@ __global__ void __launch_bounds__(32 * kCombRows) wide_combine_kernel(const __gr
     float acc[16];
 #pragma unroll
     for (int k = 0; k < 16; ++k) acc[k] = 0.f;
-    for (int c0 = 0; c0 < ns; c0 += 32) {
+    if (ns <= 4) {
+        // the usual case: every load of the lane's 16 columns of each partial in flight at once
+        float4 x[4][4];
+        float wv[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int sl = slots[j < ns ? j : 0];
+            wv[j] = (j < ns && any) ? __expf(p.part_lse[static_cast<size_t>(sl) * kWRows + r] - lse_v) : 0.f;
+            const float4* src = reinterpret_cast<const float4*>(p.part_o + (static_cast<size_t>(sl) * kWRows + r) * kWD) + lane * 4;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) x[j][k] = j < ns ? src[k] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                acc[4 * k] = fmaf(wv[j], x[j][k].x, acc[4 * k]);
+                acc[4 * k + 1] = fmaf(wv[j], x[j][k].y, acc[4 * k + 1]);
+                acc[4 * k + 2] = fmaf(wv[j], x[j][k].z, acc[4 * k + 2]);
+                acc[4 * k + 3] = fmaf(wv[j], x[j][k].w, acc[4 * k + 3]);
+            }
+    }
+    for (int c0 = 0; c0 < ns && ns > 4; c0 += 32) {
         const int mine = c0 + lane;
         const float w = (mine < ns && any) ? __expf(p.part_lse[static_cast<size_t>(slots[mine]) * kWRows + r] - lse_v) : 0.f;
         const int cnt = min(32, ns - c0);

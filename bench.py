@@ -36,8 +36,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 TRAFFIC = {
     # decode B8 H32 Sq1 Skv4096 D128: read 537,084,928 + written 3,311,616 bytes (profiles/decode_kernel_decode-B8-H32-Skv4096-D128.md)
     "decode_kernel<128>": {"bytes": 540396544, "source_sha": "5ae4f8c85541c707"},
-    # wide-head B32 Hq128 Hkv1 Skv16384 D512: read 1,081,752,000 + written 10,413,312 bytes (profiles/wide_kernel_wide-head-B32-Hq128-Hkv1-Skv16384-D512.md)
-    "wide_kernel": {"bytes": 1092165312, "source_sha": "59bf36ffcd9cc452"},
+    # wide-head B32 Hq128 Hkv1 Skv16384 D512: read 1,081,720,320 + written 10,502,144 bytes (profiles/wide_kernel_wide-head-B32-Hq128-Hkv1-Skv16384-D512.md)
+    "wide_kernel": {"bytes": 1092222464, "source_sha": "c590196cb30ca832"},
 }
 
 
