@@ -63,6 +63,9 @@ def header_functions() -> list[str]:
 def load(path: str | None = None):
     """Load libfmha.so (built by build.py / __graft_entry__.build()); raises if absent."""
     global _lib
+    lib = _lib
+    if lib is not None:
+        return lib
     with _lock:
         if _lib is not None:
             return _lib
@@ -106,13 +109,18 @@ def _check(rc: int, what: str):
 
 
 def _stream(stream=None):
+    """Raw cudaStream_t of `stream`, else of the current stream on the current device."""
     import torch
-    s = stream if stream is not None else torch.cuda.current_stream()
-    return ctypes.c_void_p(s.cuda_stream)
+    if stream is not None:
+        return stream.cuda_stream
+    raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+    if raw is not None:
+        return raw(torch.cuda.current_device())
+    return torch.cuda.current_stream().cuda_stream
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    return None if t is None else t.data_ptr()
 
 
 def _need_cuda(*ts):

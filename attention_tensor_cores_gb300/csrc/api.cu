@@ -77,6 +77,29 @@ static thread_local cudaEvent_t g_ev_end = nullptr;
 
 void count_launch(int n) { g_launches.fetch_add(n); }
 
+cudaError_t set_smem_limit_once(const void* func, int bytes)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
+    static std::mutex mu;
+    static struct Done {
+        const void* func;
+        int dev, bytes;
+    } done[256];
+    static int n_done = 0;
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        for (int i = 0; i < n_done; ++i)
+            if (done[i].func == func && done[i].dev == dev && done[i].bytes >= bytes) return cudaSuccess;
+    }
+    const cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && dev >= 0) {
+        std::lock_guard<std::mutex> lk(mu);
+        if (n_done < 256) done[n_done++] = {func, dev, bytes};
+    }
+    return e;
+}
+
 static std::atomic<unsigned long long> g_call_tag{0};
 unsigned long long next_call_tag() { return ((g_call_tag.fetch_add(1) + 1) & ((1ull << 48) - 1)) | (1ull << 47); }
 

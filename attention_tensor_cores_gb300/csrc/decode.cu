@@ -884,7 +884,7 @@ int run_decode(const AttnArgs& a, bool split, void* ws, cudaStream_t st)
         FMHA_CHECK_LAUNCH("tile_prefix_kernel");
         count_launch();
     }
-    FMHA_CHECK_CUDA(cudaFuncSetAttribute(decode_kernel<D, CAUSAL>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes));
+    FMHA_CHECK_CUDA(set_smem_limit_once(reinterpret_cast<const void*>(decode_kernel<D, CAUSAL>), C::kSmemBytes));
     const int grid = split ? nsm : (U < nsm ? U : nsm);
     if (grid > 0) {
         timing_mark_begin(st);

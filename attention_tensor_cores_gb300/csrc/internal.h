@@ -34,6 +34,8 @@ int num_sms();              // SMs of the current device
 // ---- launch accounting and the dominant-kernel timing hook ---------------------------------------
 void count_launch(int n = 1);                 // kernels this library launched (process-wide)
 unsigned long long next_call_tag();           // unique per call (48 bits, never 0): tags arrival counters
+// cudaFuncSetAttribute(func, MaxDynamicSharedMemorySize, bytes) once per (kernel, device)
+cudaError_t set_smem_limit_once(const void* func, int bytes);
 void timing_mark_begin(cudaStream_t st);      // records the pending start event (one-shot), if any
 void timing_mark_end(cudaStream_t st);        // records the pending stop event and clears the hook
 

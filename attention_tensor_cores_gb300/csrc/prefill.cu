@@ -680,7 +680,7 @@ int run_prefill(const AttnArgs& a, bool dynamic, void* ws, cudaStream_t st)
     p.limit = wait_limit();
     const long long items = static_cast<long long>(U) * p.pairs;
     const int grid = static_cast<int>(items < nsm ? items : nsm);
-    FMHA_CHECK_CUDA(cudaFuncSetAttribute(prefill_kernel<D, CAUSAL, RING>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes));
+    FMHA_CHECK_CUDA(set_smem_limit_once(reinterpret_cast<const void*>(prefill_kernel<D, CAUSAL, RING>), C::kSmemBytes));
     if (grid > 0) {
         if (dynamic) FMHA_CHECK_CUDA(cudaMemsetAsync(p.sched, 0, sizeof(int), st));
         timing_mark_begin(st);

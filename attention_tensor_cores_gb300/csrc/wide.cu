@@ -770,7 +770,7 @@ int launch_wide(const AttnArgs& a, void* ws, size_t ws_bytes, cudaStream_t st)
         FMHA_CHECK_LAUNCH("wide_prefix_kernel");
         count_launch();
     }
-    FMHA_CHECK_CUDA(cudaFuncSetAttribute(wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kWSmem));
+    FMHA_CHECK_CUDA(set_smem_limit_once(reinterpret_cast<const void*>(wide_kernel), kWSmem));
     timing_mark_begin(st);
     wide_kernel<<<2 * npairs, kWThreads, kWSmem, st>>>(qmap, kmap, vmap, p);
     timing_mark_end(st);

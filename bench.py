@@ -34,10 +34,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # named kernel, with the sha256 of its source file at capture time; reported only while the
 # source is unchanged.
 TRAFFIC = {
-    # decode B8 H32 Sq1 Skv4096 D128: read 537,084,928 + written 3,311,616 bytes (profiles/decode_kernel_decode-B8-H32-Skv4096-D128.md)
-    "decode_kernel<128>": {"bytes": 540396544, "source_sha": "5ae4f8c85541c707"},
-    # wide-head B32 Hq128 Hkv1 Skv16384 D512: read 1,081,720,320 + written 10,502,144 bytes (profiles/wide_kernel_wide-head-B32-Hq128-Hkv1-Skv16384-D512.md)
-    "wide_kernel": {"bytes": 1092222464, "source_sha": "c590196cb30ca832"},
+    # decode B8 H32 Sq1 Skv4096 D128: read 537,082,624 + written 3,222,528 bytes (profiles/decode_kernel_decode-B8-H32-Skv4096-D128.md)
+    "decode_kernel<128>": {"bytes": 540305152, "source_sha": "5fb006d3d68f254a"},
+    # wide-head B32 Hq128 Hkv1 Skv16384 D512: read 1,081,722,112 + written 10,283,008 bytes (profiles/wide_kernel_wide-head-B32-Hq128-Hkv1-Skv16384-D512.md)
+    "wide_kernel": {"bytes": 1092005120, "source_sha": "38d96554f8046aca"},
 }
 
 
