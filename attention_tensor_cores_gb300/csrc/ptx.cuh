@@ -316,6 +316,15 @@ __device__ __forceinline__ void fence_proxy_async_smem()
 // Tensor Memory
 // ------------------------------------------------------------------------------------------
 // Whole warp: allocates `ncols` (power of two >= 32) columns, writes the base address to smem.
+// 32-byte store of eight floats to global memory; `p` must be 32-byte aligned.  One store
+// instruction then covers a whole 32-byte sector per thread.
+__device__ __forceinline__ void st_global_v8(float* p, const float* v)
+{
+    asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "f"(v[0]), "f"(v[1]), "f"(v[2]),
+                 "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7])
+                 : "memory");
+}
+
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols)
 {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),

@@ -81,11 +81,19 @@ struct WideParams {
     uint8_t* nv_codes;
     uint8_t* nv_scales;
     float* nv_ts;
-    float* part_o;      // [slots][128][512]
+    float* part_o;      // [slots][64 column groups of 8][128 rows][8], see wpart_index
     float* part_lse;    // [slots][128]
     int* status;
     long long limit;
 };
+
+// Offset of partial O element (slot, row, col).  Each 8-column group keeps its 128 rows side by
+// side, so a warp storing 8 columns of 32 consecutive rows writes 1 KB of contiguous memory, and
+// a row's 8 columns are one 32-byte sector.
+__host__ __device__ __forceinline__ size_t wpart_index(size_t slot, int row, int col)
+{
+    return ((slot * (kWD / 8) + static_cast<size_t>(col >> 3)) * kWRows + row) * 8 + (col & 7);
+}
 
 struct WItem {
     int u, t0, t1, n;
@@ -489,9 +497,10 @@ __global__ void __launch_bounds__(kWThreads, 1)
                             }
                         }
                     } else {
-                        float4* dst = reinterpret_cast<float4*>(p.part_o + (static_cast<size_t>(it.slot) * kWRows + row_in_tile) * kWD + col);
+                        // the workspace starts on a 256-byte boundary, so every 8-column group of a row is
+                        // one aligned 32-byte sector
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                        for (int i = 0; i < 4; ++i) st_global_v8(p.part_o + wpart_index(it.slot, row_in_tile, col + 8 * i), v + 8 * i);
                     }
                 }
             }
@@ -537,18 +546,20 @@ __global__ void __launch_bounds__(1024) wide_prefix_kernel(const int32_t* seqlen
 }
 
 // Merges split units (lse = log sum exp lse_i, O = sum exp(lse_i - lse) O_i) and writes units
-// without keys (O = 0, LSE = -inf).  A block serves 8 query rows of one unit: warp 0 finds the
-// pairs that hold partials of the unit once (64-bit divisions), then warp w merges row w: lane i
-// holds partial i's weight, and each lane sums 16 of the row's 512 columns over the partials.
+// without keys (O = 0, LSE = -inf).  A block serves 32 of the 512 columns of one unit's 128 query
+// rows: warp 0 finds the pairs that hold partials of the unit once (64-bit divisions), then thread
+// r merges row r, its LSE in registers and its 32 columns over the partials.  A warp's load of one
+// 8-column group covers 32 consecutive rows, 1 KB of contiguous memory in the partial layout.
 constexpr int kMaxParts = 512;
-constexpr int kCombRows = 8;
+constexpr int kCombCols = 32;
 
-__global__ void __launch_bounds__(32 * kCombRows) wide_combine_kernel(const __grid_constant__ WideParams p, int npairs)
+__global__ void __launch_bounds__(kWRows) wide_combine_kernel(const __grid_constant__ WideParams p, int npairs)
 {
     __shared__ int slots[kMaxParts];
     __shared__ int nslots;
-    const int u = blockIdx.x / (kWRows / kCombRows);
-    const int r = (blockIdx.x % (kWRows / kCombRows)) * kCombRows + static_cast<int>(threadIdx.x / 32);
+    const int u = blockIdx.x / (kWD / kCombCols);
+    const int col0 = (blockIdx.x % (kWD / kCombCols)) * kCombCols;
+    const int r = static_cast<int>(threadIdx.x);
     const int lane = static_cast<int>(threadIdx.x & 31);
     const int hu = wunit_head(p, u);
     const int tiles = wunit_tiles(p, u);
@@ -581,95 +592,73 @@ __global__ void __launch_bounds__(32 * kCombRows) wide_combine_kernel(const __gr
     }
     __syncthreads();
     const int ns = nslots;
+    if (ns < 0) return;   // the same for the whole block
+    // rows beyond R (a partial row tile) compute on in-bounds workspace rows and store nothing,
+    // so that every lane takes part in the warp reduction below
     const int row = (u % p.row_tiles) * kWRows + r;
-    if (ns < 0 || row >= p.R) return;
-    // merged LSE of this row
+    const bool live = row < p.R;
+    // merged LSE of this row; partials without a visible key carry lse = -inf and weigh 0
     float mx = -INFINITY;
-    for (int i = lane; i < ns; i += 32) mx = fmaxf(mx, p.part_lse[static_cast<size_t>(slots[i]) * kWRows + r]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    // partials without a visible key carry lse = -inf and weigh 0; all of them -> empty row
+    for (int i = 0; i < ns; ++i) mx = fmaxf(mx, p.part_lse[static_cast<size_t>(slots[i]) * kWRows + r]);
     const bool any = mx > -INFINITY;
     float sum = 0.f;
     if (any)
-        for (int i = lane; i < ns; i += 32) sum += __expf(p.part_lse[static_cast<size_t>(slots[i]) * kWRows + r] - mx);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        for (int i = 0; i < ns; ++i) sum += __expf(p.part_lse[static_cast<size_t>(slots[i]) * kWRows + r] - mx);
     const float lse_v = (ns > 0 && any) ? mx + __logf(sum) : -INFINITY;
-    // weighted sum of the partial rows, 16 columns per lane
-    float acc[16];
+    // weighted sum of this row's 32 columns over the partials
+    float acc[kCombCols];
 #pragma unroll
-    for (int k = 0; k < 16; ++k) acc[k] = 0.f;
-    if (ns <= 4) {
-        // the usual case: every load of the lane's 16 columns of each partial in flight at once
-        float4 x[4][4];
-        float wv[4];
+    for (int k = 0; k < kCombCols; ++k) acc[k] = 0.f;
+    for (int j = 0; j < ns && any; ++j) {
+        const int sl = slots[j];
+        const float w = __expf(p.part_lse[static_cast<size_t>(sl) * kWRows + r] - lse_v);
+        float4 x[kCombCols / 4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int sl = slots[j < ns ? j : 0];
-            wv[j] = (j < ns && any) ? __expf(p.part_lse[static_cast<size_t>(sl) * kWRows + r] - lse_v) : 0.f;
-            const float4* src = reinterpret_cast<const float4*>(p.part_o + (static_cast<size_t>(sl) * kWRows + r) * kWD) + lane * 4;
+        for (int k = 0; k < kCombCols / 4; ++k) x[k] = *reinterpret_cast<const float4*>(p.part_o + wpart_index(sl, r, col0 + 4 * k));
 #pragma unroll
-            for (int k = 0; k < 4; ++k) x[j][k] = j < ns ? src[k] : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                acc[4 * k] = fmaf(wv[j], x[j][k].x, acc[4 * k]);
-                acc[4 * k + 1] = fmaf(wv[j], x[j][k].y, acc[4 * k + 1]);
-                acc[4 * k + 2] = fmaf(wv[j], x[j][k].z, acc[4 * k + 2]);
-                acc[4 * k + 3] = fmaf(wv[j], x[j][k].w, acc[4 * k + 3]);
-            }
-    }
-    for (int c0 = 0; c0 < ns && ns > 4; c0 += 32) {
-        const int mine = c0 + lane;
-        const float w = (mine < ns && any) ? __expf(p.part_lse[static_cast<size_t>(slots[mine]) * kWRows + r] - lse_v) : 0.f;
-        const int cnt = min(32, ns - c0);
-        for (int j = 0; j < cnt; ++j) {
-            const float wj = __shfl_sync(0xffffffffu, w, j);
-            const float4* src = reinterpret_cast<const float4*>(p.part_o + (static_cast<size_t>(slots[c0 + j]) * kWRows + r) * kWD) + lane * 4;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const float4 v = src[k];
-                acc[4 * k] = fmaf(wj, v.x, acc[4 * k]);
-                acc[4 * k + 1] = fmaf(wj, v.y, acc[4 * k + 1]);
-                acc[4 * k + 2] = fmaf(wj, v.z, acc[4 * k + 2]);
-                acc[4 * k + 3] = fmaf(wj, v.w, acc[4 * k + 3]);
-            }
+        for (int k = 0; k < kCombCols / 4; ++k) {
+            acc[4 * k] = fmaf(w, x[k].x, acc[4 * k]);
+            acc[4 * k + 1] = fmaf(w, x[k].y, acc[4 * k + 1]);
+            acc[4 * k + 2] = fmaf(w, x[k].z, acc[4 * k + 2]);
+            acc[4 * k + 3] = fmaf(w, x[k].w, acc[4 * k + 3]);
         }
     }
-    const size_t orow = static_cast<size_t>(hu) * p.R + row;
-    if (p.o_stage) {
-        float4* dst = reinterpret_cast<float4*>(p.o_stage + orow * kWD) + lane * 4;
+    const size_t orow = static_cast<size_t>(hu) * p.R + (live ? row : 0);
+    if (live && p.o_stage) {
+        float4* dst = reinterpret_cast<float4*>(p.o_stage + orow * kWD + col0);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) dst[k] = make_float4(acc[4 * k], acc[4 * k + 1], acc[4 * k + 2], acc[4 * k + 3]);
+        for (int k = 0; k < kCombCols / 4; ++k) dst[k] = make_float4(acc[4 * k], acc[4 * k + 1], acc[4 * k + 2], acc[4 * k + 3]);
     }
-    if (p.out) {
+    if (live && p.out) {
         if (p.out_f32) {
-            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow * kWD) + lane * 4;
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow * kWD + col0);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) dst[k] = make_float4(acc[4 * k], acc[4 * k + 1], acc[4 * k + 2], acc[4 * k + 3]);
+            for (int k = 0; k < kCombCols / 4; ++k) dst[k] = make_float4(acc[4 * k], acc[4 * k + 1], acc[4 * k + 2], acc[4 * k + 3]);
         } else {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + orow * kWD) + lane * 2;
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + orow * kWD + col0);
 #pragma unroll
-            for (int k = 0; k < 2; ++k)
+            for (int k = 0; k < kCombCols / 8; ++k)
                 dst[k] = make_uint4(pack_bf16x2(acc[8 * k], acc[8 * k + 1]), pack_bf16x2(acc[8 * k + 2], acc[8 * k + 3]),
                                     pack_bf16x2(acc[8 * k + 4], acc[8 * k + 5]), pack_bf16x2(acc[8 * k + 6], acc[8 * k + 7]));
         }
     }
-    if (lane == 0 && p.lse) p.lse[orow] = lse_v;
-    if (p.nv_codes) {
-        // single-pass NVFP4: lane holds columns 16 lane .. 16 lane + 15, one block
-        uint32_t lo, hi;
-        const uint32_t sc = nvfp4_encode16(acc, *p.nv_sg, lo, hi);
-        reinterpret_cast<uint2*>(p.nv_codes + orow * (kWD / 2))[lane] = make_uint2(lo, hi);
-        p.nv_scales[orow * (kWD / 16) + lane] = static_cast<uint8_t>(sc);
+    if (live && col0 == 0 && p.lse) p.lse[orow] = lse_v;
+    if (live && p.nv_codes) {
+        // single-pass NVFP4: the thread's 32 columns are two 16-value blocks of its row
+        const float sg = *p.nv_sg;
+#pragma unroll
+        for (int b = 0; b < kCombCols / 16; ++b) {
+            uint32_t lo, hi;
+            const uint32_t sc = nvfp4_encode16(acc + 16 * b, sg, lo, hi);
+            reinterpret_cast<uint2*>(p.nv_codes + orow * (kWD / 2) + col0 / 2)[b] = make_uint2(lo, hi);
+            p.nv_scales[orow * (kWD / 16) + col0 / 16 + b] = static_cast<uint8_t>(sc);
+        }
     }
     if (p.amax_bits) {
         float m = 0.f;
+        if (live)
 #pragma unroll
-        for (int k = 0; k < 16; ++k) m = fmaxf(m, fabsf(acc[k]));
+            for (int k = 0; k < kCombCols; ++k) m = fmaxf(m, fabsf(acc[k]));
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
         if (lane == 0 && m > 0.f) atomicMax(p.amax_bits, __float_as_uint(m));
@@ -776,10 +765,11 @@ int launch_wide(const AttnArgs& a, void* ws, size_t ws_bytes, cudaStream_t st)
     timing_mark_end(st);
     FMHA_CHECK_LAUNCH("wide_kernel");
     count_launch();
-    wide_combine_kernel<<<p.U * (kWRows / kCombRows), 32 * kCombRows, 0, st>>>(p, npairs);
+    wide_combine_kernel<<<p.U * (kWD / kCombCols), kWRows, 0, st>>>(p, npairs);
     FMHA_CHECK_LAUNCH("wide_combine_kernel");
     count_launch();
     return FMHA_OK;
 }
 
 }  // namespace fmha
+
