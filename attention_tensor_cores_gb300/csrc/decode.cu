@@ -260,6 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ float red_max[2][4][kN];
     __shared__ uint32_t red_need[2][4];   // per warp: columns whose scores passed the reference + kRescaleD
     __shared__ float red_sum[4][kN];
+    __shared__ float col_inv[kN], col_lse[kN];   // per query column: 1 / L and the LSE of this range
     __shared__ int ep_abort, fx_last;          // softmax warps: abort snapshot, "this CTA merges"
     __shared__ int fx_n;
     __shared__ int fx_slot[kMaxFixSlots];
@@ -548,27 +549,45 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (it.t1 > it.t0) consume(alpha_prev);
 
-            // ---- epilogue: L = sum over the 128 key lanes, O = acc / L, lse = ln2 * (m + log2 L)
-            float L[kN];
-            if (it.t1 > it.t0) {
+            // ---- epilogue: L = sum over the 128 key lanes, O = acc · (1 / L), lse = ln2 * (m + log2 L)
+            const bool empty = it.t1 <= it.t0;
+            if (!empty) {
+                if (G == 1) {
+                    const float s = warp_sum(l[0]);
+                    if (lane == 0) red_sum[warp][0] = s;
+                } else {
+                    // all columns' butterflies interleaved: five rounds of independent shuffles
+                    float v[kN];
 #pragma unroll
-                for (int q = 0; q < kN; ++q)
-                    if (q < G) {
-                        const float s = warp_sum(l[q]);
-                        if (lane == 0) red_sum[warp][q] = s;
-                    }
-                named_bar_sync(1, 128);
+                    for (int q = 0; q < kN; ++q) v[q] = q < G ? l[q] : 0.f;
 #pragma unroll
-                for (int q = 0; q < kN; ++q) L[q] = (q < G) ? (red_sum[0][q] + red_sum[1][q]) + (red_sum[2][q] + red_sum[3][q]) : 1.f;
-            } else {
+                    for (int o = 16; o > 0; o >>= 1)
 #pragma unroll
-                for (int q = 0; q < kN; ++q) L[q] = 0.f;
+                        for (int q = 0; q < kN; ++q) v[q] += __shfl_xor_sync(0xffffffffu, v[q], o);
+                    if (lane == 0)
+#pragma unroll
+                        for (int q = 0; q < kN; ++q)
+                            if (q < G) red_sum[warp][q] = v[q];
+                }
+            }
+            // red_sum is complete, and every thread is past its reads of the previous item's
+            // col_inv / col_lse (an empty item has no tile barriers in between)
+            named_bar_sync(1, 128);
+            // one thread per column: L, then 1 / L and the LSE for every thread of the CTA
+            if (tid < G) {
+                const float Lq = empty ? 0.f : (red_sum[0][tid] + red_sum[1][tid]) + (red_sum[2][tid] + red_sum[3][tid]);
+                float mq = m[0];
+#pragma unroll
+                for (int q = 1; q < kN; ++q)
+                    if (q == tid) mq = m[q];
+                const bool none = !(Lq > 0.f);   // no visible key in this range
+                col_inv[tid] = none ? 0.f : 1.f / Lq;
+                col_lse[tid] = none ? -INFINITY : (mq + __log2f(Lq)) * kLn2;
             }
             // one abort decision for all four warps (named barriers and shuffles below)
             if (tid == 0) ep_abort = aborted(wc) ? 1 : 0;
             named_bar_sync(1, 128);
             if (ep_abort) continue;
-            const bool empty = it.t1 <= it.t0;
             // single-pass NVFP4 in split mode: whole units also go through the combine, which
             // encodes every row in parallel (encoding here would lengthen the CTAs holding many
             // short units)
@@ -578,9 +597,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int q = 0; q < kN; ++q) {
                     if (q >= G) break;
-                    const bool none = empty || !(L[q] > 0.f);   // no visible key in this range
-                    const float o = none ? 0.f : acc[q] / L[q];
-                    const float lse_v = none ? -INFINITY : (m[q] + __log2f(L[q])) * kLn2;
+                    const float o = col_inv[q] > 0.f ? acc[q] * col_inv[q] : 0.f;   // 0: no visible key in this range
+                    const float lse_v = col_lse[q];
                     const size_t row = static_cast<size_t>(it.u) * G + q;
                     if (final_here) {
                         write_final(row, o, lse_v, local_amax);
@@ -611,46 +629,57 @@ __global__ void __launch_bounds__(kThreads, 1)
                     __threadfence();
                     const int ns = fx_n;
                     float amax_m = 0.f;
-                    for (int q = 0; q < G; ++q) {
-                        if (ns <= 4) {
-                            // one round of independent loads (all partial LSEs and this column of each
-                            // partial O), then the weights in registers
-                            float lv[4], ov[4];
+                    if (ns <= 4) {
+                        // the usual case: four columns at a time, every partial LSE and this thread's
+                        // element of every partial O for them loaded in one round (a column at a
+                        // time made one dependent L2 round trip per column)
+                        for (int q0 = 0; q0 < G; q0 += 4) {
+                            float lv[4][4], ov[4][4];
 #pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                const size_t sl = static_cast<size_t>(fx_slot[i < ns ? i : 0]) * kN + q;
-                                lv[i] = i < ns ? __ldcg(p.part_lse + sl) : -INFINITY;
-                                ov[i] = (i < ns && tid < D) ? __ldcg(p.part_o + sl * D + tid) : 0.f;
+                            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    const bool use = q0 + c < G && i < ns;
+                                    const size_t sl = static_cast<size_t>(fx_slot[i < ns ? i : 0]) * kN + (use ? q0 + c : 0);
+                                    lv[c][i] = use ? __ldcg(p.part_lse + sl) : -INFINITY;
+                                    ov[c][i] = (use && tid < D) ? __ldcg(p.part_o + sl * D + tid) : 0.f;
+                                }
+#pragma unroll
+                            for (int c = 0; c < 4; ++c) {
+                                const int q = q0 + c;
+                                if (q >= G) break;
+                                const float mx = fmaxf(fmaxf(lv[c][0], lv[c][1]), fmaxf(lv[c][2], lv[c][3]));
+                                const bool any = mx > -INFINITY;
+                                float sum = 0.f;
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) sum += (any && i < ns) ? __expf(lv[c][i] - mx) : 0.f;
+                                const float lse_all = any ? mx + __logf(sum) : -INFINITY;
+                                float o = 0.f;
+#pragma unroll
+                                for (int i = 0; i < 4; ++i)
+                                    if (any && i < ns) o = fmaf(__expf(lv[c][i] - lse_all), ov[c][i], o);
+                                if (tid < D) write_final(static_cast<size_t>(it.u) * G + q, o, lse_all, amax_m);
                             }
-                            const float mx = fmaxf(fmaxf(lv[0], lv[1]), fmaxf(lv[2], lv[3]));
+                        }
+                    } else {
+                        for (int q = 0; q < G; ++q) {
+                            float mx = -INFINITY;
+                            for (int i = 0; i < ns; ++i) mx = fmaxf(mx, __ldcg(p.part_lse + static_cast<size_t>(fx_slot[i]) * kN + q));
+                            // partials without a visible key carry lse = -inf and weigh 0; all of them -> empty row
                             const bool any = mx > -INFINITY;
                             float sum = 0.f;
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) sum += (any && i < ns) ? __expf(lv[i] - mx) : 0.f;
-                            const float lse_all = any ? mx + __logf(sum) : -INFINITY;
-                            float o = 0.f;
-#pragma unroll
-                            for (int i = 0; i < 4; ++i)
-                                if (any && i < ns) o = fmaf(__expf(lv[i] - lse_all), ov[i], o);
-                            if (tid < D) write_final(static_cast<size_t>(it.u) * G + q, o, lse_all, amax_m);
-                            continue;
-                        }
-                        float mx = -INFINITY;
-                        for (int i = 0; i < ns; ++i) mx = fmaxf(mx, __ldcg(p.part_lse + static_cast<size_t>(fx_slot[i]) * kN + q));
-                        // partials without a visible key carry lse = -inf and weigh 0; all of them -> empty row
-                        const bool any = mx > -INFINITY;
-                        float sum = 0.f;
-                        if (any)
-                            for (int i = 0; i < ns; ++i) sum += __expf(__ldcg(p.part_lse + static_cast<size_t>(fx_slot[i]) * kN + q) - mx);
-                        const float lse_all = (ns > 0 && any) ? mx + __logf(sum) : -INFINITY;
-                        if (tid < D) {
-                            float o = 0.f;
                             if (any)
-                                for (int i = 0; i < ns; ++i) {
-                                    const size_t sl = static_cast<size_t>(fx_slot[i]) * kN + q;
-                                    o = fmaf(__expf(__ldcg(p.part_lse + sl) - lse_all), __ldcg(p.part_o + sl * D + tid), o);
-                                }
-                            write_final(static_cast<size_t>(it.u) * G + q, o, lse_all, amax_m);
+                                for (int i = 0; i < ns; ++i) sum += __expf(__ldcg(p.part_lse + static_cast<size_t>(fx_slot[i]) * kN + q) - mx);
+                            const float lse_all = (ns > 0 && any) ? mx + __logf(sum) : -INFINITY;
+                            if (tid < D) {
+                                float o = 0.f;
+                                if (any)
+                                    for (int i = 0; i < ns; ++i) {
+                                        const size_t sl = static_cast<size_t>(fx_slot[i]) * kN + q;
+                                        o = fmaf(__expf(__ldcg(p.part_lse + sl) - lse_all), __ldcg(p.part_o + sl * D + tid), o);
+                                    }
+                                write_final(static_cast<size_t>(it.u) * G + q, o, lse_all, amax_m);
+                            }
                         }
                     }
                     if (p.amax_bits) {
@@ -1016,3 +1045,4 @@ extern "C" int fmha_fwd_decode_noalloc(const void* q, const void* k, const void*
     if (rc) return rc;
     return launch_decode(a, 0, scratch, FMHA_NOALLOC_SCRATCH_BYTES, reinterpret_cast<cudaStream_t>(stream));
 }
+
