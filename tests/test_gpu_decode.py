@@ -200,3 +200,33 @@ def test_merge_counters_across_calls(F):
     check_o_lse(outs[0].reshape(-1, D), None, o_ref, l_ref, "merge across calls")
     np.testing.assert_array_equal(outs[0], outs[1])
     np.testing.assert_array_equal(outs[0], outs[2])
+
+
+@pytest.mark.parametrize("Hkv,Sq,causal", [(8, 4, True), (4, 1, False)])
+def test_multi_column_split_merge_repeatable(F, Hkv, Sq, causal):
+    """Several query columns per key/value head (16 = 4 heads x 4 causal tokens, and 8 heads x 1),
+    split across CTAs and merged in the kernel: every column matches the oracle, and ten calls on one
+    workspace give bit-identical O and LSE (the per-column sums, 1/L and the merged partials do not
+    depend on which CTA arrives last)."""
+    w = inputs.Workload("t", 2, 32, Hkv, Sq, 3000, 128, 1.0, "bf16", 52)
+    q, k, v, _ = w.make("cuda")
+    B, Hq, _, D = q.shape
+    opts = F.make_opts(F.FMHA_OUT_BF16, None, 0, None, None, None, None, causal)
+    wsb = F.fmha_workspace_size(B, Hq, Hkv, Sq, w.Skv, D, opts)
+    ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device="cuda")
+    opts = F.make_opts(F.FMHA_OUT_BF16, None, 0, ws, None, None, None, causal)
+    outs, lses = [], []
+    for _ in range(10):
+        out = torch.full((B, Hq, Sq, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty(B, Hq, Sq, dtype=torch.float32, device="cuda")
+        F.fmha_fwd_ex(q, k, v, out, lse, w.scale, opts)
+        outs.append(out.float().cpu().numpy())
+        lses.append(lse.cpu().numpy())
+    torch.cuda.synchronize()
+    assert F.fmha_check_status() == 0
+    o_ref, l_ref = oracle.attention(q.cpu(), k.cpu(), v.cpu(), w.scale, causal=causal)
+    check_o_lse(outs[0].reshape(-1, D), lses[0].reshape(-1), o_ref.reshape(-1, D), l_ref.reshape(-1),
+                f"G={Hq // Hkv * Sq}")
+    for o, l in zip(outs[1:], lses[1:]):
+        np.testing.assert_array_equal(o, outs[0])
+        np.testing.assert_array_equal(l, lses[0])
