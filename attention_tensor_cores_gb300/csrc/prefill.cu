@@ -56,13 +56,15 @@ constexpr int kItemSlots = 4;     // work-item ring between the TMA warp and the
 
 template <int D>
 struct PrefillCfg {
-    // Keys per tile: 128 at D = 64; 64 at D = 128, so that S (double-buffered over the two query
-    // tiles), separate P buffers and O fit the 512 Tensor Memory columns and QK(j + 1) can run
-    // while the softmax of tile j still owns its P.
-    static constexpr int kTN = (D == 64) ? 128 : 64;
+    // 128 keys per tile (a QK MMA of N = 128 runs at the full rate; N = 64 at 64 %).  At D = 64
+    // each query tile has its own S buffer.  At D = 128 the two O buffers take 256 columns, so the
+    // two query tiles take one S buffer in turns: a QK waits for the other tile's softmax to read S,
+    // never for its own PV (P has buffers of its own).
+    static constexpr bool kSharedS = (D == 128);
+    static constexpr int kTN = 128;
     static constexpr int kAtoms = D / 64;
     static constexpr int kQStages = (D == 64) ? 2 : 1;
-    static constexpr int kStages = 4;
+    static constexpr int kStages = (D == 64) ? 4 : 2;
     static constexpr int kQTileBytes = kAtoms * kTM * 128;
     static constexpr int kQBytes = 2 * kQTileBytes;
     static constexpr int kKVBytes = kAtoms * kTN * 128;
@@ -70,8 +72,9 @@ struct PrefillCfg {
     static constexpr int kOffK = kOffQ + kQStages * kQBytes;
     static constexpr int kOffV = kOffK + kStages * kKVBytes;
     static constexpr int kSmemBytes = kOffV + kStages * kKVBytes + 1024;
-    // Tensor Memory columns: S_q at q * kTN, P_q (BF16 pairs) at kColP + q * kPStride, O_q at kColO + q * D
-    static constexpr uint32_t kColP = 2 * kTN;
+    // Tensor Memory columns: S_q at col_s(q), P_q (BF16 pairs) at kColP + q * kPStride, O_q at kColO + q * D
+    static constexpr uint32_t col_s(int q) { return kSharedS ? 0u : static_cast<uint32_t>(q * kTN); }
+    static constexpr uint32_t kColP = kSharedS ? kTN : 2 * kTN;
     static constexpr uint32_t kPStride = kTN / 2;
     static constexpr uint32_t kColO = 512 - 2 * D;
     static_assert(kColP + 2 * kPStride <= kColO, "Tensor Memory layout");
@@ -311,6 +314,7 @@ __global__ void __launch_bounds__(prefill_threads<RING>(), 1)
                 PRing qr(QS);
                 uint32_t gtile = 0;          // global K/V tile counter (ring position of tile 0 of an item)
                 uint32_t nqk[2] = {0, 0};    // QKs issued per query tile over the kernel's life
+                uint32_t nqk_all = 0;        // QKs issued over the kernel's life (shared S buffer)
                 uint32_t npv[2] = {0, 0};    // PVs issued per query tile
                 PRing ir(kItemSlots);
                 int next_fixed = static_cast<int>(blockIdx.x);
@@ -346,19 +350,29 @@ __global__ void __launch_bounds__(prefill_threads<RING>(), 1)
                             if (jq[q] < Tq[q]) {
                                 const uint32_t g = gtile + jq[q];
                                 bool ok = mbar_test(&k_full[g % S], (g / S) & 1);
-                                if (ok && nqk[q] > 0) ok = mbar_test(&s_free[q], (nqk[q] - 1) & 1);
+                                if constexpr (C::kSharedS) {
+                                    // one S buffer: QKs in a fixed order (tile 0 then tile 1 at each key
+                                    // tile, then whichever tile has key tiles left), each once the
+                                    // softmax has read the previous QK's S
+                                    const int nxt = (jq[0] < Tq[0] && (jq[0] <= jq[1] || jq[1] >= Tq[1])) ? 0 : 1;
+                                    if (q != nxt) ok = false;
+                                    if (ok && nqk_all > 0) ok = mbar_test(&s_free[0], (nqk_all - 1) & 1);
+                                } else {
+                                    if (ok && nqk[q] > 0) ok = mbar_test(&s_free[q], (nqk[q] - 1) & 1);
+                                }
                                 if (ok) {
                                     tc_fence_after();
                                     // descriptors once; K steps add constant offsets to the address fields
                                     const uint64_t dq = sdesc_sw128(sQ + q * C::kQTileBytes, 16, 1024);
                                     const uint64_t dk = sdesc_sw128(smem_u32(smem + C::kOffK + (g % S) * C::kKVBytes), 16, 1024);
-                                    const uint32_t dS = tmem + q * kTN;
+                                    const uint32_t dS = tmem + C::col_s(q);
     #pragma unroll
                                     for (int kk = 0; kk < D / 16; ++kk)
                                         mma_ss(dS, dq + (((kk >> 2) * (kTM * 128) + (kk & 3) * 32) >> 4),
                                                dk + (((kk >> 2) * (kTN * 128) + (kk & 3) * 32) >> 4), idesc_qk, kk > 0 ? 1u : 0u);
                                     mma_commit(&s_full[q]);
                                     ++nqk[q];
+                                    ++nqk_all;
                                     ++jq[q];
                                     // the last of the query tiles that need K_g releases it
                                     if (Tq[q ^ 1] <= jq[q] - 1 || jq[q ^ 1] >= jq[q]) mma_commit(&k_empty[g % S]);
@@ -411,7 +425,7 @@ __global__ void __launch_bounds__(prefill_threads<RING>(), 1)
         const int wl = warp % 4;
         const uint32_t lane_base = static_cast<uint32_t>(wl * 32) << 16;
         const int row_in_tile = wl * 32 + static_cast<int>(lane_id());
-        const uint32_t tS = tmem + lane_base + q * kTN;
+        const uint32_t tS = tmem + lane_base + C::col_s(q);
         const uint32_t tP = tmem + lane_base + C::kColP + q * C::kPStride;
         const uint32_t tO = tmem + lane_base + C::kColO + q * D;
         const float nv_sg = (RING && p.nv_sg) ? *p.nv_sg : 0.f;
@@ -451,7 +465,7 @@ __global__ void __launch_bounds__(prefill_threads<RING>(), 1)
                 for (int c4 = 0; c4 < kTN / 32; ++c4) tmem_ld32p(tS + c4 * 32, su + c4 * 32);
                 tmem_ld_wait();
                 tc_fence_before();
-                mbar_arrive(&s_free[q]);
+                mbar_arrive(&s_free[C::kSharedS ? 0 : q]);
                 if ((j + 1) * kTN > lim) {
 #pragma unroll
                     for (int i = 0; i < kTN; ++i)
@@ -614,9 +628,10 @@ constexpr size_t kSchedBytes = 256;
 // Work-item counter: causal or ragged problems (items of different sizes) when a workspace is in use.
 bool prefill_dynamic(const AttnArgs& a, int sched_mode) { return sched_mode != 1 && (a.causal || a.seqlens); }
 
-// The ring kernel: balanced (counter) order, or single-pass NVFP4 output (its epilogue encoder needs
-// the softmax warps' larger register budget; in the compact kernel it slowed dense problems).
-bool prefill_ring(const AttnArgs& a, int sched_mode) { return prefill_dynamic(a, sched_mode) || a.nv_sg; }
+// The ring kernel: balanced (counter) order, single-pass NVFP4 output (its epilogue encoder needs
+// the softmax warps' larger register budget; in the compact kernel it slowed dense problems), and
+// every D = 128 problem (a row of 128 scores with P and O needs that budget too).
+bool prefill_ring(const AttnArgs& a, int sched_mode) { return prefill_dynamic(a, sched_mode) || a.nv_sg || a.D == 128; }
 
 size_t stage_bytes(const AttnArgs& a)
 {
@@ -696,9 +711,13 @@ template <int D>
 int run_prefill_d(const AttnArgs& a, int sched_mode, void* ws, cudaStream_t st)
 {
     const bool dyn = prefill_dynamic(a, sched_mode);
-    const bool ring = prefill_ring(a, sched_mode);
-    if (a.causal) return ring ? run_prefill<D, true, true>(a, dyn, ws, st) : run_prefill<D, true, false>(a, dyn, ws, st);
-    return ring ? run_prefill<D, false, true>(a, dyn, ws, st) : run_prefill<D, false, false>(a, dyn, ws, st);
+    if constexpr (PrefillCfg<D>::kSharedS) {   // always the ring kernel (prefill_ring)
+        return a.causal ? run_prefill<D, true, true>(a, dyn, ws, st) : run_prefill<D, false, true>(a, dyn, ws, st);
+    } else {
+        const bool ring = prefill_ring(a, sched_mode);
+        if (a.causal) return ring ? run_prefill<D, true, true>(a, dyn, ws, st) : run_prefill<D, true, false>(a, dyn, ws, st);
+        return ring ? run_prefill<D, false, true>(a, dyn, ws, st) : run_prefill<D, false, false>(a, dyn, ws, st);
+    }
 }
 
 }  // namespace

@@ -140,6 +140,14 @@ def causal_flops(w) -> int:
     return 4 * w.D * w.Hq * pairs
 
 
+def d128_prefill_workload():
+    """The prefill workload at head dimension 128 (an extra line): B4 H16 Sq=Skv=8192 D128, N(0,1),
+    non-causal, BF16 out (seed 1007)."""
+    from attention_tensor_cores_gb300 import inputs
+    return inputs.Workload("prefill B4 H16 Sq8192 Skv8192 D128 (non-causal, BF16 out)", 4, 16, 16, 8192, 8192,
+                           128, 1.0, "bf16", 1007)
+
+
 def chunked_prefill_workload():
     """Chunked prefill over a ragged KV cache: 1024 new causal query tokens per sequence, key
     lengths drawn from U{1..8192} (seed 1008), B8 Hq=Hkv=16 D128, BF16 out (an extra line)."""
@@ -456,10 +464,7 @@ def run_ours(args, rank, world, local):
         except F.FmhaError as ex:
             extra["c2_spec_causal"] = {"workload": "speculative decode", "unsupported": str(ex)}
         try:   # the prefill workload at head dim 128
-            from attention_tensor_cores_gb300 import inputs as _inputs
-            w128 = _inputs.Workload("prefill B4 H16 Sq8192 Skv8192 D128 (non-causal, BF16 out)", 4, 16, 16, 8192, 8192,
-                                    128, 1.0, "bf16", 1007)
-            extra["c3_d128"] = _workload_entry(F, w128, 2, min(args.steps, 10), args.warmup, peaks)
+            extra["c3_d128"] = _workload_entry(F, d128_prefill_workload(), 2, min(args.steps, 10), args.warmup, peaks)
         except F.FmhaError as ex:
             extra["c3_d128"] = {"workload": "prefill D128", "unsupported": str(ex)}
         try:   # chunked prefill: ragged key lengths, causal, work items from the workspace counter
@@ -539,7 +544,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--only-headline", action="store_true", help="skip the other workloads")
-    ap.add_argument("--profile", choices=["c1", "c2", "c3", "c4", "c5", "c3_causal", "c5_given_scale", "c2_spec_causal"], default=None,
+    ap.add_argument("--profile", choices=["c1", "c2", "c3", "c4", "c5", "c3_causal", "c3_d128", "c5_given_scale", "c2_spec_causal"], default=None,
                     help="run one workload's call --repeat times, untimed (for a profiler)")
     ap.add_argument("--repeat", type=int, default=5)
     args = ap.parse_args()
@@ -549,7 +554,12 @@ def main():
         ge.build()
         import attention_tensor_cores_gb300 as F
         from attention_tensor_cores_gb300 import inputs
-        w = spec_decode_workload() if args.profile == "c2_spec_causal" else inputs.workloads()[int(args.profile[1]) - 1]
+        if args.profile == "c2_spec_causal":
+            w = spec_decode_workload()
+        elif args.profile == "c3_d128":
+            w = d128_prefill_workload()
+        else:
+            w = inputs.workloads()[int(args.profile[1]) - 1]
         case = Case(F, w, num_splits=0, causal=args.profile in ("c3_causal", "c2_spec_causal"))
         if args.profile == "c5_given_scale":   # one two-pass call gives the scale the rest reuse
             case.call()

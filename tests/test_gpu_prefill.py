@@ -23,7 +23,7 @@ def F():
     (1, 1, 1, 300, 300, 64),     # two pairs, the second tile of the last pair entirely past the rows
     (2, 2, 2, 128, 1000, 64),    # one tile per pair, 8 key tiles with a tail of 104
     (1, 8, 2, 64, 500, 128),     # GQA: 4 heads x 64 rows = 256 rows per key/value head, D = 128
-    (1, 2, 1, 512, 384, 128),    # D = 128 (P written over S), several pairs
+    (1, 2, 1, 512, 384, 128),    # D = 128 (one S buffer shared by the two query tiles), several pairs
     (1, 1, 1, 17, 1, 64),        # one key
     (1, 1, 1, 1000, 4100, 64),   # 33 key tiles, last one with 4 keys
 ])
