@@ -79,10 +79,12 @@ def test_causal_fixed_order(F, B, Hq, Hkv, Sq, Skv, D, seq):
     check_o_lse(res["o"], res["lse"], o_ref, l_ref, "causal fixed order")
 
 
-def test_ragged_prefill_balanced_order_many_units(F):
+@pytest.mark.parametrize("D", [64, 128])
+def test_ragged_prefill_balanced_order_many_units(F, D):
     """Ragged non-causal prefill with the workspace counter: 48 units of very different lengths,
-    192 items for at most 152 CTAs, so CTAs claim several items of unequal size."""
-    B, H, Sq, Skv, D = 6, 8, 800, 1500, 64
+    192 items for at most 152 CTAs, so CTAs claim several items of unequal size (at D = 128 the two
+    query tiles of every item also take the shared S buffer in turns, across items)."""
+    B, H, Sq, Skv = 6, 8, 800, 1500
     sl = [1500, 3, 700, 1, 1280, 129]
     w = inputs.Workload("t", B, H, H, Sq, Skv, D, 1.0, "bf16", 84)
     q, k, v, _ = w.make("cuda")
@@ -92,7 +94,7 @@ def test_ragged_prefill_balanced_order_many_units(F):
     sl_t = torch.tensor(sl, dtype=torch.int32, device="cuda")
     res = run_attention(F, q, k, v, w.scale, seqlens=sl_t, num_splits=0)
     o_ref, l_ref = oracle.attention(q.cpu(), k.cpu(), v.cpu(), w.scale, seqlens_k=np.array(sl, np.int32))
-    check_o_lse(res["o"], res["lse"], o_ref, l_ref, "ragged prefill, counter order")
+    check_o_lse(res["o"], res["lse"], o_ref, l_ref, f"ragged prefill, counter order, D={D}")
 
 
 def test_causal_workspace_reuse_back_to_back(F):

@@ -84,3 +84,14 @@ def test_prefill_full_size_sampled(F):
     o_ref, l_ref = oracle_rows(w, rows)
     check_o_lse(res["o"][rows], res["lse"][rows], o_ref, l_ref, "prefill full size")
     assert np.all(np.isfinite(res["o"])) and np.all(np.isfinite(res["lse"]))
+
+
+def test_dense_d128_many_items_fixed_order(F):
+    """Dense D = 128 prefill without a workspace (fixed item order): 4 x 16 heads x 3 row-tile pairs
+    = 192 items for at most 152 CTAs, so CTAs run several items and the shared S buffer's turn order
+    continues across them."""
+    w = inputs.Workload("t", 4, 16, 16, 600, 900, 128, 1.0, "bf16", 47)
+    q, k, v, _ = w.make("cuda")
+    res = run_attention(F, q, k, v, w.scale)
+    o_ref, l_ref = oracle.attention(q.cpu(), k.cpu(), v.cpu(), w.scale)
+    check_o_lse(res["o"], res["lse"], o_ref, l_ref, "dense D=128, many items")
