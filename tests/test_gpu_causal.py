@@ -28,6 +28,7 @@ def F():
     (1, 2, 1, 700, 300, 64, 1.0),     # row-tile path, Sq > Skv: 400 queries see no key
     (1, 8, 2, 64, 500, 128, 1.0),     # row-tile path, GQA: head blocks of 64 rows interleave
     (1, 1, 1, 513, 513, 128, 1.0),    # D = 128 (shared S, query tiles with different key-tile counts), 1-row last tile
+    (1, 2, 2, 700, 300, 128, 1.0),    # D = 128, Sq > Skv: whole query tiles see no key (no QK in the shared-S order)
     (2, 16, 1, 3, 100, 512, 0.5),     # wide-head path, 3 tokens per head
 ])
 def test_causal(F, B, Hq, Hkv, Sq, Skv, D, sigma):
