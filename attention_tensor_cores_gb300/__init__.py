@@ -23,6 +23,7 @@ FMHA_ERR_UNSUPPORTED = 2
 FMHA_ERR_WORKSPACE = 3
 FMHA_ERR_CUDA = 4
 FMHA_ERR_TIMEOUT = 5
+FMHA_ERR_RACE = 6
 FMHA_OUT_BF16 = 0
 FMHA_OUT_F32 = 1
 FMHA_OUT_NVFP4 = 2

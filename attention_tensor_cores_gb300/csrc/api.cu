@@ -13,7 +13,7 @@
 
 #include "internal.h"
 
-namespace fmha {
+namespace atc_gb300 {
 
 // ---- errors ------------------------------------------------------------------------------------
 static thread_local std::string g_last_error;
@@ -33,6 +33,7 @@ int cuda_error(cudaError_t e, const char* what)
 // One int per device in this library's module: kernels write a nonzero code when a bounded wait
 // expires.  Its address is looked up once per device and passed to kernels as a pointer.
 static __device__ int g_status_word;
+static constexpr int kDevMergeLost = 6;   // the value the split-KV merge leaves (ptx.cuh)
 static constexpr int kMaxDevices = 64;
 static std::atomic<int*> g_status_addr[kMaxDevices];
 static std::atomic<int> g_num_sms[kMaxDevices];
@@ -159,9 +160,9 @@ int make_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t*
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
-}  // namespace fmha
+}  // namespace atc_gb300
 
-using namespace fmha;
+using namespace atc_gb300;
 
 // ================================================================================================
 // C ABI
@@ -177,6 +178,7 @@ const char* fmha_error_string(int code)
         case FMHA_ERR_WORKSPACE: return "FMHA_ERR_WORKSPACE: workspace missing or too small";
         case FMHA_ERR_CUDA: return "FMHA_ERR_CUDA: CUDA call or kernel launch failed";
         case FMHA_ERR_TIMEOUT: return "FMHA_ERR_TIMEOUT: a kernel's bounded wait expired";
+        case FMHA_ERR_RACE: return "FMHA_ERR_RACE: overlapping calls on one workspace left a split-KV merge unsettled";
         default: return "unknown fmha status";
     }
 }
@@ -207,6 +209,8 @@ int fmha_check_status(fmha_stream_t stream)
         const int zero = 0;
         e = cudaMemcpyToSymbol(g_status_word, &zero, sizeof(int));
         if (e != cudaSuccess) return cuda_error(e, "cudaMemcpyToSymbol(status)");
+        if (v == kDevMergeLost)
+            return set_error(FMHA_ERR_RACE, "a split-KV merge counter never settled (device status word set)");
         return set_error(FMHA_ERR_TIMEOUT, "a kernel's bounded wait expired (device status word set)");
     }
     return FMHA_OK;
@@ -242,7 +246,7 @@ static bool use_decode_path(int Hq, int Hkv, int Sq) { return static_cast<long l
 // row-tile path the work-item counter (causal or ragged) and the FP32 staging of O, last.
 static size_t workspace_bytes(const AttnArgs& a, int num_splits)
 {
-    size_t w = a.D == 512 ? wide_workspace_bytes(a)
+    size_t w = a.D == 512 ? wide_workspace_bytes(a, num_splits)
                : use_decode_path(a.Hq, a.Hkv, a.Sq) ? decode_workspace_bytes(a, num_splits) : prefill_workspace_bytes(a, num_splits);
     w = align256(w);
     if (a.out_kind == FMHA_OUT_NVFP4 && !a.nv_sg) w += 256;   // amax word of the two-pass NVFP4 path
@@ -349,7 +353,7 @@ int fmha_fwd_ex(const void* q, const void* k, const void* v, void* out, float* l
         a.nv_ts = opts->out_tensor_scale;
     }
     if (D == 512)
-        rc = launch_wide(a, ws, path_bytes, st);
+        rc = launch_wide(a, num_splits, ws, path_bytes, st);
     else if (use_decode_path(Hq, Hkv, Sq))
         rc = launch_decode(a, num_splits, ws, path_bytes, st);
     else

@@ -14,7 +14,7 @@
 #include "internal.h"
 #include "ptx.cuh"
 
-namespace fmha {
+namespace atc_gb300 {
 namespace {
 
 constexpr int kQkThreads = 128;
@@ -346,4 +346,4 @@ int launch_selftest(int which, const void* in, void* out, size_t out_bytes, int 
     return set_error(FMHA_ERR_INVALID, "selftest: unknown test id");
 }
 
-}  // namespace fmha
+}  // namespace atc_gb300

@@ -35,7 +35,7 @@
 #include "nvfp4_dev.cuh"
 #include "ptx.cuh"
 
-namespace fmha {
+namespace atc_gb300 {
 namespace {
 
 constexpr int kTileKV = 128;    // keys per tile = MMA M
@@ -622,7 +622,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (tid == 0) {
                     const int n = unit_partial_slots(p, it.u, static_cast<int>(gridDim.x), fx_slot, kMaxFixSlots);
                     fx_n = n;
-                    fx_last = (n > 0 && arrive_unit(p.unit_ctr + it.u, p.gen, n) == n) ? 1 : 0;
+                    const int arrived = n > 0 ? arrive_unit(p.unit_ctr + it.u, p.gen, n) : 0;
+                    // -1: the counter kept changing under us (another call on this workspace):
+                    // the unit may stay unmerged, so say so instead of failing silently
+                    if (arrived < 0) atomicExch(p.status, kDevMergeLost);
+                    fx_last = (arrived == n && n > 0) ? 1 : 0;
                 }
                 named_bar_sync(1, 128);
                 if (fx_last) {
@@ -952,7 +956,7 @@ int launch_decode(const AttnArgs& a, int num_splits, void* ws, size_t ws_bytes, 
     }
 }
 
-}  // namespace fmha
+}  // namespace atc_gb300
 
 // ================================================================================================
 // Split-KV decode without any device allocation by the caller or the library.
@@ -970,7 +974,7 @@ int launch_decode(const AttnArgs& a, int num_splits, void* ws, size_t ws_bytes, 
 // ================================================================================================
 static __device__ __align__(256) unsigned char g_fmha_decode_scratch[FMHA_NOALLOC_SCRATCH_BYTES];
 
-namespace fmha {
+namespace atc_gb300 {
 namespace {
 
 constexpr int kMaxScratchDevices = 64;
@@ -995,13 +999,13 @@ int decode_scratch_address(void** out)
 }
 
 }  // namespace
-}  // namespace fmha
+}  // namespace atc_gb300
 
 extern "C" int fmha_fwd_decode_noalloc(const void* q, const void* k, const void* v, void* out, float* lse, int B,
                                        int Hq, int Hkv, int Sq, int Skv, int D, float scale,
                                        const int32_t* seqlens_k, fmha_stream_t stream)
 {
-    using namespace fmha;
+    using namespace atc_gb300;
     if (!q || !k || !v || !out) return set_error(FMHA_ERR_INVALID, "fmha_fwd_decode_noalloc: NULL q/k/v/out");
     if (B < 0 || Hq <= 0 || Hkv <= 0 || Sq < 0 || Skv <= 0 || Hq % Hkv != 0)
         return set_error(FMHA_ERR_INVALID, "fmha_fwd_decode_noalloc: need B >= 0, Sq >= 0, Skv >= 1, Hq % Hkv == 0");

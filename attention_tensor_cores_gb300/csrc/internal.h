@@ -10,7 +10,7 @@
 
 #include "../../include/fmha.h"
 
-namespace fmha {
+namespace atc_gb300 {
 
 // ---- errors ------------------------------------------------------------------------------
 int set_error(int code, const std::string& msg);  // records msg for fmha_last_error(), returns code
@@ -18,12 +18,12 @@ int cuda_error(cudaError_t e, const char* what);  // FMHA_ERR_CUDA with the CUDA
 #define FMHA_CHECK_CUDA(expr)                                      \
     do {                                                           \
         cudaError_t e__ = (expr);                                  \
-        if (e__ != cudaSuccess) return ::fmha::cuda_error(e__, #expr); \
+        if (e__ != cudaSuccess) return ::atc_gb300::cuda_error(e__, #expr); \
     } while (0)
 #define FMHA_CHECK_LAUNCH(what)                                                 \
     do {                                                                        \
         cudaError_t e__ = cudaGetLastError();                                   \
-        if (e__ != cudaSuccess) return ::fmha::cuda_error(e__, what);           \
+        if (e__ != cudaSuccess) return ::atc_gb300::cuda_error(e__, what);           \
     } while (0)
 
 // ---- device status word and wait limit -------------------------------------------------------
@@ -78,9 +78,10 @@ int launch_decode(const AttnArgs& a, int num_splits, void* ws, size_t ws_bytes, 
 size_t prefill_workspace_bytes(const AttnArgs& a, int sched_mode);
 int launch_prefill(const AttnArgs& a, int sched_mode, void* ws, size_t ws_bytes, cudaStream_t st);
 
-// Wide-head path (D = 512): CTA pairs split the value columns, stream-K over 32-key tiles.
-size_t wide_workspace_bytes(const AttnArgs& a);
-int launch_wide(const AttnArgs& a, void* ws, size_t ws_bytes, cudaStream_t st);
+// Wide-head path (D = 512): CTA pairs split the value columns, stream-K over 128-key tiles, or
+// whole units per pair without a workspace when num_splits == 1.
+size_t wide_workspace_bytes(const AttnArgs& a, int num_splits);
+int launch_wide(const AttnArgs& a, int num_splits, void* ws, size_t ws_bytes, cudaStream_t st);
 
 // NVFP4
 // NVFP4 quantiser: s_g from sg_in when given (no amax pass), else from *amax_bits (computed here
@@ -88,4 +89,4 @@ int launch_wide(const AttnArgs& a, void* ws, size_t ws_bytes, cudaStream_t st);
 int launch_nvfp4(const float* x, uint8_t* codes, uint8_t* scales, float* tensor_scale, unsigned* amax_bits,
                  int64_t n, bool amax_ready, cudaStream_t st, const float* sg_in = nullptr);
 
-}  // namespace fmha
+}  // namespace atc_gb300

@@ -16,7 +16,7 @@
 #include "nvfp4_dev.cuh"
 #include "ptx.cuh"
 
-namespace fmha {
+namespace atc_gb300 {
 namespace {
 
 __global__ void amax_kernel(const float* __restrict__ x, int64_t n, unsigned* amax_bits)
@@ -86,4 +86,4 @@ int launch_nvfp4(const float* x, uint8_t* codes, uint8_t* scales, float* tensor_
     return FMHA_OK;
 }
 
-}  // namespace fmha
+}  // namespace atc_gb300

@@ -18,7 +18,7 @@
 
 #include <cstdint>
 
-namespace fmha {
+namespace atc_gb300 {
 
 // ---- FP64 route ------------------------------------------------------------------------------------
 
@@ -205,4 +205,4 @@ __device__ __forceinline__ void nvfp4_encode_lanes(float x, float sg, int col, u
     if (!(col & 15)) scales_row[col >> 4] = static_cast<uint8_t>(sc);
 }
 
-}  // namespace fmha
+}  // namespace atc_gb300

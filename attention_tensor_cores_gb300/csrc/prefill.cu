@@ -32,7 +32,7 @@
 #include "nvfp4_dev.cuh"
 #include "ptx.cuh"
 
-namespace fmha {
+namespace atc_gb300 {
 namespace {
 
 constexpr int kTM = 128;          // query rows per tile (MMA M)
@@ -737,4 +737,4 @@ int launch_prefill(const AttnArgs& a, int sched_mode, void* ws, size_t ws_bytes,
     }
 }
 
-}  // namespace fmha
+}  // namespace atc_gb300

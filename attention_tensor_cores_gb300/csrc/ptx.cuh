@@ -12,7 +12,7 @@
 #include <cstdint>
 #include <cuda.h>
 
-namespace fmha {
+namespace atc_gb300 {
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p)
 {
@@ -102,8 +102,8 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity)
 // shared memory.
 constexpr long long kDrainLimit = 4000000000LL;
 
-// Status codes a kernel can leave in the device status word.
-enum : int { kDevOk = 0, kDevTimeout = 5 };
+// Status codes a kernel can leave in the device status word (the host maps them to fmha_status).
+enum : int { kDevOk = 0, kDevTimeout = 5, kDevMergeLost = 6 };
 
 // Per-CTA abort state: once any wait of a CTA gives up, every later wait of that CTA returns
 // false at once, so all roles run their (bounded) loops to the end without blocking and meet
@@ -152,7 +152,9 @@ __device__ __forceinline__ void named_bar_sync(int id, int n)
 // Counts one arrival at a unit's counter and returns the count of this call's arrivals so far.
 // The counter carries this call's tag in its upper 48 bits, so whatever an earlier call (or the
 // caller) left in it reads as zero arrivals: no reset between calls is needed.  The CAS loop fails
-// only when another CTA arrived in between, so it ends after at most that many retries.
+// only when another CTA arrived in between, so within one call it ends after at most `need` (at
+// most a few hundred) retries.  Returns -1 after 4096 failures, which only calls that overlap on
+// one workspace can cause; the caller reports that through the status word.
 __device__ __forceinline__ int arrive_unit(unsigned long long* ctr, unsigned long long gen, int need)
 {
     // first guess: this arrival completes the unit (one round trip for the CTA that merges)
@@ -164,83 +166,6 @@ __device__ __forceinline__ int arrive_unit(unsigned long long* ctr, unsigned lon
         old = prev;
     }
     return -1;
-}
-
-// Bounded wait with cluster-scope acquire (for barriers that CTAs of the cluster arrive on).
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, const WaitCtl& w);
-
-// ------------------------------------------------------------------------------------------
-// Thread-block clusters / distributed shared memory
-// ------------------------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t cluster_ctarank()
-{
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-// shared::cta address -> shared::cluster address of the same location in CTA `rank`
-__device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank)
-{
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
-    return r;
-}
-
-__device__ __forceinline__ void st_cluster_v4(uint32_t caddr, uint4 v)
-{
-    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(caddr), "r"(v.x), "r"(v.y), "r"(v.z),
-                 "r"(v.w)
-                 : "memory");
-}
-
-// Arrive on an mbarrier of another CTA of the cluster (address from mapa_shared), releasing this
-// thread's earlier shared::cluster stores at cluster scope.
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t caddr)
-{
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
-}
-
-// Non-blocking test with cluster-scope acquire: remote arrivals may not wake a suspended try_wait
-// promptly, so cluster-scope waits poll.
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n"
-        ".reg .pred P;\n"
-        "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 P, [%1], %2;\n"
-        "selp.u32 %0, 1, 0, P;\n"
-        "}\n"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, const WaitCtl& w)
-{
-    const uint32_t a = smem_u32(bar);
-    if (mbar_try_wait_cluster(a, parity))
-        return true;
-    const long long t0 = clock64();
-    for (;;) {
-        if (aborted(w))
-            return false;
-        if (clock64() - t0 > w.limit) {
-            *reinterpret_cast<volatile int*>(w.abort_flag) = 1;
-            atomicExch(w.status, kDevTimeout);
-            return false;
-        }
-        if (mbar_try_wait_cluster(a, parity))
-            return true;
-    }
-}
-
-__device__ __forceinline__ void cluster_sync_all()
-{
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // ------------------------------------------------------------------------------------------
@@ -280,29 +205,10 @@ __device__ __forceinline__ void tma_load_3d_hint(void* dst, const CUtensorMap* m
         : "memory");
 }
 
-// Tiled load multicast to the CTAs of the cluster in `mask`: the box lands at the same shared
-// memory offset in each, and each one's mbarrier at the same offset gets the complete_tx.
-__device__ __forceinline__ void tma_load_3d_mc(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y, int z,
-                                               uint16_t mask)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "h"(mask)
-        : "memory");
-}
-
 __device__ __forceinline__ uint64_t policy_evict_first()
 {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-
-__device__ __forceinline__ uint64_t policy_evict_last()
-{
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
     return p;
 }
 
@@ -392,17 +298,6 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar)
 {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                  : "memory");
-}
-
-// Arrive (once) on the mbarrier at the same offset in every CTA of `mask` when all previously
-// issued tcgen05 operations of this thread finish.
-__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t mask)
-{
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            smem_u32(bar)),
-        "h"(mask)
-        : "memory");
 }
 
 // 32 lanes x 16 consecutive 32-bit columns; thread i of the warp gets lane (base lane + i).
@@ -573,4 +468,4 @@ __device__ __forceinline__ uint16_t float_to_bf16_bits(float f)
     return static_cast<uint16_t>(r & 0xFFFF);
 }
 
-}  // namespace fmha
+}  // namespace atc_gb300

@@ -21,6 +21,8 @@
 //  * Stream-K over keys: the tiles of all units (b, kv-head, 128-row block) are laid end to end and
 //    pair p of P takes [p*T/P, (p+1)*T/P); a run that covers a whole unit writes O and LSE,
 //    otherwise a normalised partial goes to slot unit + p and the combine kernel merges them.
+//    Without a workspace (no split), pair p takes whole units p, p + P, ... and writes them itself:
+//    no partials, no combine launch.
 //  * Roles: warps 0-3 softmax (one query row per thread, lazy rescale as in the row-tile kernel),
 //    warp 4 loads Q, K and V, warp 5 issues the MMAs in order.  All waits are bounded.
 #include <cuda_runtime.h>
@@ -29,7 +31,7 @@
 #include "nvfp4_dev.cuh"
 #include "ptx.cuh"
 
-namespace fmha {
+namespace atc_gb300 {
 namespace {
 
 constexpr int kWD = 512;            // head dim of Q/K/V
@@ -72,6 +74,7 @@ struct WideParams {
     const int32_t* seqlens;
     const int32_t* prefix;   // [U+1] tile prefix (ragged), else NULL
     int tiles_uniform;
+    int whole_units;    // 1: no split, pair p handles units p, p + P, ... whole (no workspace)
     void* out;
     int out_f32;
     float* lse;
@@ -120,11 +123,17 @@ __device__ __forceinline__ long long wunit_start(const WideParams& p, int u)
 struct WSched {
     const WideParams* p;
     long long g, g1;
-    int pair;
+    int pair, step;
     __device__ void init(const WideParams* pp, int pr, int npairs)
     {
         p = pp;
         pair = pr;
+        step = npairs;
+        if (p->whole_units) {
+            g = pr;
+            g1 = p->U;
+            return;
+        }
         const long long T = p->prefix ? p->prefix[p->U] : static_cast<long long>(p->U) * p->tiles_uniform;
         g = (static_cast<long long>(pr) * T) / npairs;
         g1 = (static_cast<long long>(pr + 1) * T) / npairs;
@@ -132,6 +141,17 @@ struct WSched {
     __device__ bool next(WItem& it)
     {
         if (g >= g1) return false;
+        if (p->whole_units) {
+            const int uu = static_cast<int>(g);
+            it.u = uu;
+            it.t0 = 0;
+            it.t1 = wunit_tiles(*p, uu);
+            it.n = wunit_keys(*p, uu);
+            it.whole = true;
+            it.slot = 0;
+            g += step;
+            return true;
+        }
         int uu;
         if (p->prefix) {
             int lo = 0, hi = p->U - 1;
@@ -454,8 +474,13 @@ __global__ void __launch_bounds__(kWThreads, 1)
             __syncwarp();
             for (int c4 = 0; c4 < kWHalf / 32; ++c4) {
                 uint32_t o[32];
-                tmem_ld32p(tmem + lane_base + kWColO + c4 * 32, o);
-                tmem_ld_wait();
+                if (T > 0) {   // uniform over the CTA; a unit without keys (whole-unit order) gives O = 0
+                    tmem_ld32p(tmem + lane_base + kWColO + c4 * 32, o);
+                    tmem_ld_wait();
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = 0u;
+                }
                 if (store) {
                     const int col = half * kWHalf + c4 * 32;
                     float v[32];
@@ -669,16 +694,17 @@ struct WideWs {
     size_t prefix_off, lse_off, o_off, stage_off, total;
 };
 
-WideWs wide_ws_layout(const AttnArgs& a, int npairs)
+// whole: no split (whole units per pair), which needs no prefix and no partials
+WideWs wide_ws_layout(const AttnArgs& a, int npairs, bool whole)
 {
     auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
     const int R = (a.Hq / a.Hkv) * a.Sq;
     const size_t U = static_cast<size_t>(a.B) * a.Hkv * ((R + kWRows - 1) / kWRows);
-    const size_t slots = U + npairs;
+    const size_t slots = whole ? 0 : U + npairs;
     WideWs w{};
     size_t off = 0;
     w.prefix_off = off;
-    off += a.seqlens ? al((U + 1) * 4) : 0;
+    off += (a.seqlens && !whole) ? al((U + 1) * 4) : 0;
     w.lse_off = off;
     off += al(slots * kWRows * 4);
     w.o_off = off;
@@ -692,24 +718,26 @@ WideWs wide_ws_layout(const AttnArgs& a, int npairs)
 
 }  // namespace
 
-size_t wide_workspace_bytes(const AttnArgs& a)
+size_t wide_workspace_bytes(const AttnArgs& a, int num_splits)
 {
     const int nsm = num_sms() > 0 ? num_sms() : 256;
-    return wide_ws_layout(a, nsm / 2).total;
+    return wide_ws_layout(a, nsm / 2, num_splits == 1).total;
 }
 
-int launch_wide(const AttnArgs& a, void* ws, size_t ws_bytes, cudaStream_t st)
+int launch_wide(const AttnArgs& a, int num_splits, void* ws, size_t ws_bytes, cudaStream_t st)
 {
     const int nsm = num_sms();
     if (nsm < 2) return set_error(FMHA_ERR_CUDA, "cannot query the SM count");
-    const int npairs = nsm / 2;
-    const WideWs w = wide_ws_layout(a, npairs);
-    if (!ws || ws_bytes < w.total) return set_error(FMHA_ERR_WORKSPACE, "wide-head path: workspace too small");
+    const bool whole = num_splits == 1;
+    const WideWs w = wide_ws_layout(a, nsm / 2, whole);
+    if (w.total > 0 && (!ws || ws_bytes < w.total)) return set_error(FMHA_ERR_WORKSPACE, "wide-head path: workspace too small");
     uint8_t* base = static_cast<uint8_t*>(ws);
     const int Hq_per = a.Hq / a.Hkv;
     const int R = Hq_per * a.Sq;
     const int row_tiles = (R + kWRows - 1) / kWRows;
     const int heads = a.B * a.Hkv;
+    // whole units: no more pairs than units (each pair takes units p, p + P, ...)
+    const int npairs = whole ? min(nsm / 2, heads * row_tiles) : nsm / 2;
     CUtensorMap qmap, kmap, vmap;
     {
         const uint64_t dims[3] = {static_cast<uint64_t>(kWD), static_cast<uint64_t>(R), static_cast<uint64_t>(heads)};
@@ -738,8 +766,9 @@ int launch_wide(const AttnArgs& a, void* ws, size_t ws_bytes, cudaStream_t st)
     p.Sq = a.Sq > 0 ? a.Sq : 1;
     p.causal = a.causal;
     p.seqlens = a.seqlens;
-    p.prefix = a.seqlens ? reinterpret_cast<const int32_t*>(base + w.prefix_off) : nullptr;
+    p.prefix = (a.seqlens && !whole) ? reinterpret_cast<const int32_t*>(base + w.prefix_off) : nullptr;
     p.tiles_uniform = (a.Skv + kWKeys - 1) / kWKeys;
+    p.whole_units = whole ? 1 : 0;
     const bool nvfp4 = a.out_kind == FMHA_OUT_NVFP4;
     p.out = nvfp4 ? nullptr : a.out;
     p.out_f32 = a.out_kind == FMHA_OUT_F32 ? 1 : 0;
@@ -750,8 +779,8 @@ int launch_wide(const AttnArgs& a, void* ws, size_t ws_bytes, cudaStream_t st)
     p.nv_codes = a.nv_codes;
     p.nv_scales = a.nv_scales;
     p.nv_ts = a.nv_ts;
-    p.part_lse = reinterpret_cast<float*>(base + w.lse_off);
-    p.part_o = reinterpret_cast<float*>(base + w.o_off);
+    p.part_lse = whole ? nullptr : reinterpret_cast<float*>(base + w.lse_off);
+    p.part_o = whole ? nullptr : reinterpret_cast<float*>(base + w.o_off);
     p.status = device_status_ptr();
     p.limit = wait_limit();
     if (p.prefix) {
@@ -765,11 +794,12 @@ int launch_wide(const AttnArgs& a, void* ws, size_t ws_bytes, cudaStream_t st)
     timing_mark_end(st);
     FMHA_CHECK_LAUNCH("wide_kernel");
     count_launch();
+    if (whole) return FMHA_OK;   // every unit was written by its pair
     wide_combine_kernel<<<p.U * (kWD / kCombCols), kWRows, 0, st>>>(p, npairs);
     FMHA_CHECK_LAUNCH("wide_combine_kernel");
     count_launch();
     return FMHA_OK;
 }
 
-}  // namespace fmha
+}  // namespace atc_gb300
 

@@ -45,7 +45,10 @@ typedef enum {
     FMHA_ERR_UNSUPPORTED = 2, /* valid request that this library does not implement */
     FMHA_ERR_WORKSPACE = 3,   /* workspace missing or smaller than fmha_workspace_size() */
     FMHA_ERR_CUDA = 4,        /* a CUDA runtime/driver call or kernel launch failed */
-    FMHA_ERR_TIMEOUT = 5      /* a kernel's bounded wait expired (see fmha_check_status) */
+    FMHA_ERR_TIMEOUT = 5,     /* a kernel's bounded wait expired (see fmha_check_status) */
+    FMHA_ERR_RACE = 6         /* a split-KV merge counter never settled: calls sharing one
+                                 workspace (or the allocation-free scratch) overlapped on the
+                                 GPU, so some output rows may be unmerged (see fmha_check_status) */
 } fmha_status;
 
 typedef enum {
@@ -60,7 +63,8 @@ typedef struct {
     const int32_t* seqlens_k; /* device int32[B], 0 <= seqlens_k[b] <= Skv: keys at or beyond
                                  seqlens_k[b] are never read (ragged batches); NULL = all Skv */
     int num_splits;           /* 0 = automatic split-KV; 1 = no split (each (b, kv-head) handled
-                                 by one CTA, no workspace needed for BF16/F32 output).  With 0 and
+                                 by one CTA, or by one CTA pair for D = 512; no workspace needed
+                                 for BF16/F32 output).  With 0 and
                                  a workspace, causal or ragged problems on the 128-row path (more
                                  than 16 query rows per key/value head) also take their work items
                                  from a counter in the workspace (balanced across SMs); with 1, or
@@ -87,11 +91,13 @@ typedef struct {
 } fmha_opts;
 
 /*
- * Attention forward with default options (BF16 output, dense keys, no workspace).
+ * Attention forward with default options (BF16 output, dense keys, no workspace, no split).
  *   q: BF16 [B,Hq,Sq,D]; k, v: BF16 [B,Hkv,Skv,D]; out: BF16 [B,Hq,Sq,D];
  *   lse: FP32 [B,Hq,Sq] or NULL; scale: multiplies Q K^T before the softmax.
- * Same as fmha_fwd_ex(..., opts = NULL).  D = 512 always needs a workspace (its value columns are
- * split over CTA pairs whose partial results are merged), so it goes through fmha_fwd_ex.
+ * Same as fmha_fwd_ex(..., opts = NULL): every (b, kv-head) unit is handled whole by one CTA (for
+ * D = 512 by one CTA pair, each CTA writing its half of the value columns), so nothing needs a
+ * workspace.  Decode shapes with few units leave SMs idle this way; fmha_fwd_ex with a workspace
+ * splits the keys over every SM instead.
  */
 int fmha_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq, int Hkv,
              int Sq, int Skv, int D, float scale, fmha_stream_t stream);
@@ -151,8 +157,9 @@ int fmha_selftest(int which, const void* in, void* out, size_t out_bytes, int pa
 
 /*
  * Waits for `stream`, then returns FMHA_ERR_TIMEOUT if any kernel of this library timed out
- * in a bounded wait since the last call (and clears that state), FMHA_ERR_CUDA if the stream
- * reports an error, else FMHA_OK.
+ * in a bounded wait since the last call, FMHA_ERR_RACE if a split-KV merge found its arrival
+ * counter changing under it (overlapping calls on one workspace), clearing that state in both
+ * cases; FMHA_ERR_CUDA if the stream reports an error; else FMHA_OK.
  */
 int fmha_check_status(fmha_stream_t stream);
 
