@@ -83,9 +83,17 @@ def check_o_lse(o, lse, o_ref, lse_ref, what=""):
     return float(err.max()), float(err.mean())
 
 
-def oracle_rows(w: inputs.Workload, rows, causal: bool = False):
-    """FP64 oracle for flat query rows of workload `w`, from regenerated slices only."""
+def oracle_rows(w: inputs.Workload, rows, causal: bool = False, tensors=None):
+    """FP64 oracle for flat query rows of workload `w`.
+
+    tensors: the (q, k, v) torch tensors the GPU call used (any device): they are copied to the host
+    and the oracle computes every requested row in one call.  Without them the oracle regenerates
+    just the slices it needs from the seeded generator (slow for long key sets)."""
     sl = w.seqlens()
+    rows = np.asarray(rows, dtype=np.int64)
+    if tensors is not None:
+        q, k, v = (t.cpu() for t in tensors)
+        return oracle.attention(q, k, v, w.scale, seqlens_k=sl, rows=rows, causal=causal)
     g = w.Hq // w.Hkv
     o = np.zeros((len(rows), w.D))
     lse = np.zeros(len(rows))
@@ -120,9 +128,50 @@ def oracle_rows(w: inputs.Workload, rows, causal: bool = False):
     return o, lse
 
 
-def sample_rows(w: inputs.Workload, count: int, seed: int = 0):
-    """Sorted sample of flat query rows covering first/last rows and a seeded random spread."""
-    total = w.B * w.Hq * w.Sq
+def unit_rows(w: inputs.Workload, u: int) -> tuple[int, int]:
+    """Flat row range [first, end) of (b, kv-head) unit u = b * Hkv + kvh: the query rows of its
+    Hq / Hkv heads, which are contiguous in the [B, Hq, Sq] order."""
+    g = w.Hq // w.Hkv
+    b, kvh = divmod(u, w.Hkv)
+    first = (b * w.Hq + kvh * g) * w.Sq
+    return first, first + g * w.Sq
+
+
+def split_boundary_units(tiles_per_unit, parts: int) -> list[int]:
+    """Units whose key tiles a stream-K split cuts: the tiles of all units laid end to end, part c
+    of `parts` taking [c*T/parts, (c+1)*T/parts) (integer division), as the split decode and
+    wide-head kernels partition them over CTAs or CTA pairs."""
+    pre = np.concatenate([[0], np.cumsum(np.asarray(tiles_per_unit, dtype=np.int64))])
+    T = int(pre[-1])
+    cut = set()
+    for c in range(1, parts):
+        b = c * T // parts
+        u = int(np.searchsorted(pre, b, side="right")) - 1
+        if 0 <= u < len(tiles_per_unit) and pre[u] < b < pre[u + 1]:
+            cut.add(u)
+    return sorted(cut)
+
+
+def stratified_rows(w: inputs.Workload, all_units: bool = True, edge_units=None, tile: int = 128,
+                    extra: int = 16, seed: int = 0):
+    """Flat query rows spread over the problem's structure rather than uniformly:
+      * one seeded row of every (b, kv-head) unit (all_units);
+      * for each unit in `edge_units`: the first and last row of every `tile`-row query tile and
+        the unit's last row (every query tile boundary of those units);
+      * `extra` seeded random rows."""
     rng = np.random.default_rng(seed)
-    rows = set([0, total - 1]) | set(rng.choice(total, size=min(count, total), replace=False).tolist())
+    U = w.B * w.Hkv
+    rows = set()
+    if all_units:
+        for u in range(U):
+            a, e = unit_rows(w, u)
+            rows.add(int(rng.integers(a, e)))
+    for u in (edge_units or []):
+        a, e = unit_rows(w, int(u))
+        for t0 in range(a, e, tile):
+            rows.add(t0)
+            rows.add(min(t0 + tile, e) - 1)
+    total = w.B * w.Hq * w.Sq
+    rows |= set(rng.choice(total, size=min(extra, total), replace=False).tolist())
+    rows |= {0, total - 1}
     return np.array(sorted(rows), dtype=np.int64)

@@ -6,7 +6,7 @@ import torch
 
 import oracle
 from attention_tensor_cores_gb300 import inputs
-from attn_util import check_o_lse, oracle_rows, run_attention, sample_rows
+from attn_util import check_o_lse, oracle_rows, run_attention, stratified_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -53,13 +53,15 @@ def test_causal_ragged_nan_padding(F):
     check_o_lse(res["o"], res["lse"], o_ref, l_ref, "causal ragged")
 
 
-def test_causal_prefill_full_size_sampled(F):
-    """B4 H16 Sq=Skv=8192 D64 causal, BF16 O: 64 sampled rows against the oracle."""
+def test_causal_prefill_full_size_stratified(F):
+    """B4 H16 Sq=Skv=8192 D64 causal, BF16 O: one row of every unit, the first and last row of every
+    128-row query tile of six seeded units (the diagonal tiles included), and random rows."""
     w = inputs.workloads()[2]
     q, k, v, _ = w.make("cuda")
     res = run_attention(F, q, k, v, w.scale, num_splits=0, causal=True)
-    rows = sample_rows(w, 64, seed=5)
-    o_ref, l_ref = oracle_rows(w, rows, causal=True)
+    edge = np.random.default_rng(5).choice(w.B * w.Hkv, 6, replace=False)
+    rows = stratified_rows(w, all_units=True, edge_units=edge, tile=128, extra=32, seed=5)
+    o_ref, l_ref = oracle_rows(w, rows, causal=True, tensors=(q, k, v))
     check_o_lse(res["o"][rows], res["lse"][rows], o_ref, l_ref, "causal prefill full size")
 
 

@@ -10,7 +10,7 @@ import torch
 
 import oracle
 from attention_tensor_cores_gb300 import inputs
-from attn_util import check_o_lse, oracle_rows, run_attention, sample_rows
+from attn_util import check_o_lse, oracle_rows, run_attention, split_boundary_units, stratified_rows, unit_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -85,27 +85,31 @@ def test_split_and_whole_agree(F):
     assert np.abs(res0["o"] - res1["o"]).max() <= 2 * 2 ** -8 * np.abs(o_ref).max() + 1e-6
 
 
-def test_decode_full_size_sampled(F):
-    """B8 H32 Sq1 Skv4096 D128 (split-KV, BF16 O + LSE), 48 sampled rows against the oracle."""
+def test_decode_full_size_every_row(F):
+    """B8 H32 Sq1 Skv4096 D128 (split-KV, BF16 O + LSE): every one of the 256 query rows, one per
+    (b, kv-head) unit, so every unit and every stream-K split boundary is checked."""
     w = inputs.workloads()[1]
     q, k, v, _ = w.make("cuda")
     res = run_attention(F, q, k, v, w.scale, num_splits=0)
-    rows = sample_rows(w, 48, seed=1)
-    o_ref, l_ref = oracle_rows(w, rows)
-    check_o_lse(res["o"][rows], res["lse"][rows], o_ref, l_ref, "decode full size")
-    # properties over every row: finite, |O| bounded by max|V|, LSE >= max score lower bound ln(1)
-    assert np.all(np.isfinite(res["o"])) and np.all(np.isfinite(res["lse"]))
+    rows = np.arange(w.B * w.Hq * w.Sq, dtype=np.int64)
+    o_ref, l_ref = oracle_rows(w, rows, tensors=(q, k, v))
+    check_o_lse(res["o"], res["lse"], o_ref, l_ref, "decode full size, every row")
     assert np.abs(res["o"]).max() <= float(v.abs().max()) + 1e-3
 
 
 def test_ragged_gqa_nvfp4_full_size(F):
-    """B64 Hq32 Hkv8 Sq1 ragged Skv<=32768 D128 with NVFP4 output: FP32 O on sampled rows against
-    the oracle; NVFP4 codes/scales bit-exact against the oracle quantiser on the same FP32 O."""
+    """B64 Hq32 Hkv8 Sq1 ragged Skv<=32768 D128 with NVFP4 output.  FP32 O against the oracle on
+    one row of every (b, kv-head) unit plus every row of each unit that the stream-K split cuts
+    across CTAs; NVFP4 codes/scales bit-exact against the oracle quantiser on the same FP32 O."""
     w = inputs.workloads()[4]
     q, k, v, sl = w.make("cuda", pad_fill=float("nan"))
     res = run_attention(F, q, k, v, w.scale, out_kind="nvfp4", seqlens=sl, num_splits=0, want_f32=True)
-    rows = sample_rows(w, 40, seed=2)
-    o_ref, l_ref = oracle_rows(w, rows)
+    lens = w.seqlens().astype(np.int64)
+    tiles = [int((lens[u // w.Hkv] + 127) // 128) for u in range(w.B * w.Hkv)]
+    cut = split_boundary_units(tiles, F.fmha_num_sms())
+    assert len(cut) > 50, len(cut)
+    rows = stratified_rows(w, all_units=True, edge_units=cut, tile=1, extra=16, seed=2)
+    o_ref, l_ref = oracle_rows(w, rows, tensors=(q, k, v))
     check_o_lse(res["o"][rows], res["lse"][rows], o_ref, l_ref, "ragged nvfp4 (fp32 O)")
     codes, scales, sg = oracle.nvfp4_quantize(res["o"].reshape(-1))
     assert sg == res["tensor_scale"]

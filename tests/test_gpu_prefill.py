@@ -5,7 +5,7 @@ import torch
 
 import oracle
 from attention_tensor_cores_gb300 import inputs
-from attn_util import check_o_lse, oracle_rows, run_attention, sample_rows
+from attn_util import check_o_lse, oracle_rows, run_attention, stratified_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -75,13 +75,15 @@ def test_nvfp4_output_bit_exact(F):
     np.testing.assert_array_equal(res["codes"], codes)
 
 
-def test_prefill_full_size_sampled(F):
-    """B4 H16 Sq=Skv=8192 D64 non-causal, BF16 O: 64 sampled rows against the oracle."""
+def test_prefill_full_size_stratified(F):
+    """B4 H16 Sq=Skv=8192 D64 non-causal, BF16 O: one row of every (b, head) unit, the first and
+    last row of every 128-row query tile of six seeded units, and random rows, against the oracle."""
     w = inputs.workloads()[2]
     q, k, v, _ = w.make("cuda")
     res = run_attention(F, q, k, v, w.scale)
-    rows = sample_rows(w, 64, seed=3)
-    o_ref, l_ref = oracle_rows(w, rows)
+    edge = np.random.default_rng(3).choice(w.B * w.Hkv, 6, replace=False)
+    rows = stratified_rows(w, all_units=True, edge_units=edge, tile=128, extra=32, seed=3)
+    o_ref, l_ref = oracle_rows(w, rows, tensors=(q, k, v))
     check_o_lse(res["o"][rows], res["lse"][rows], o_ref, l_ref, "prefill full size")
     assert np.all(np.isfinite(res["o"])) and np.all(np.isfinite(res["lse"]))
 

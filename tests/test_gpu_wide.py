@@ -5,7 +5,7 @@ import torch
 
 import oracle
 from attention_tensor_cores_gb300 import inputs
-from attn_util import check_o_lse, oracle_rows, run_attention
+from attn_util import check_o_lse, oracle_rows, run_attention, stratified_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -25,13 +25,19 @@ def F():
     (1, 64, 1, 3, 200),      # 192 rows per key/value head: two 128-row blocks
     (3, 16, 2, 1, 33),       # GQA 8, two key tiles, the second with one key
 ])
-@pytest.mark.parametrize("out_kind", ["bf16", "f32"])
-def test_shapes(F, B, Hq, Hkv, Sq, Skv, out_kind):
+@pytest.mark.parametrize("mode", ["fwd", "bf16", "f32", "f32_whole"])
+def test_shapes(F, B, Hq, Hkv, Sq, Skv, mode):
+    """fwd: fmha_fwd without options (whole units per CTA pair, no workspace); bf16/f32: split over
+    every SM pair with a workspace; f32_whole: whole units with FP32 output."""
     w = inputs.Workload("t", B, Hq, Hkv, Sq, Skv, 512, 0.5, "bf16", 51)
     q, k, v, _ = w.make("cuda")
-    res = run_attention(F, q, k, v, w.scale, out_kind=out_kind, num_splits=0)
+    kw = {"fwd": {}, "bf16": {"num_splits": 0}, "f32": {"out_kind": "f32", "num_splits": 0},
+          "f32_whole": {"out_kind": "f32", "num_splits": 1}}[mode]
+    res = run_attention(F, q, k, v, w.scale, **kw)
+    if mode in ("fwd", "f32_whole"):
+        assert res.get("workspace_bytes", 0) == 0
     o_ref, l_ref = oracle.attention(q.cpu(), k.cpu(), v.cpu(), w.scale)
-    check_o_lse(res["o"], res["lse"], o_ref, l_ref, out_kind)
+    check_o_lse(res["o"], res["lse"], o_ref, l_ref, mode)
 
 
 def test_ragged_nan_padding_and_empty(F):
@@ -43,10 +49,11 @@ def test_ragged_nan_padding_and_empty(F):
         k[b, :, n:] = float("nan")
         v[b, :, n:] = float("nan")
     sl_t = torch.tensor(sl, dtype=torch.int32, device="cuda")
-    res = run_attention(F, q, k, v, w.scale, seqlens=sl_t, num_splits=0)
     o_ref, l_ref = oracle.attention(q.cpu(), k.cpu(), v.cpu(), w.scale, seqlens_k=np.array(sl, np.int32))
-    check_o_lse(res["o"], res["lse"], o_ref, l_ref, "ragged wide")
-    assert np.all(res["o"][:Hq] == 0.0) and np.all(np.isneginf(res["lse"][:Hq]))
+    for ns in (0, 1):   # split with a workspace, and whole units (no workspace; the empty unit too)
+        res = run_attention(F, q, k, v, w.scale, seqlens=sl_t, num_splits=ns)
+        check_o_lse(res["o"], res["lse"], o_ref, l_ref, f"ragged wide, num_splits={ns}")
+        assert np.all(res["o"][:Hq] == 0.0) and np.all(np.isneginf(res["lse"][:Hq]))
 
 
 def test_nvfp4_output_bit_exact(F):
@@ -61,16 +68,17 @@ def test_nvfp4_output_bit_exact(F):
     np.testing.assert_array_equal(res["codes"], codes)
 
 
-def test_wide_full_size_sampled(F):
-    """B32 Hq128 Hkv1 Sq1 Skv16384 D512, N(0, 0.5), BF16 O + LSE: 40 rows from 8 batch entries."""
+@pytest.mark.parametrize("mode", ["split", "fwd"])
+def test_wide_full_size_stratified(F, mode):
+    """B32 Hq128 Hkv1 Sq1 Skv16384 D512, N(0, 0.5), BF16 O + LSE: the first and last row of every
+    unit (each unit is one 128-row tile, cut by the stream-K split into about two pieces) and random
+    rows.  split: fmha_fwd_ex with a workspace; fwd: fmha_fwd (whole units, no workspace)."""
     w = inputs.workloads()[3]
     q, k, v, _ = w.make("cuda")
-    res = run_attention(F, q, k, v, w.scale, num_splits=0)
-    rng = np.random.default_rng(4)
-    bs = sorted(rng.choice(w.B, 8, replace=False).tolist())
-    rows = np.array(sorted(b * w.Hq + h for b in bs for h in rng.choice(w.Hq, 5, replace=False)), dtype=np.int64)
-    o_ref, l_ref = oracle_rows(w, rows)
-    check_o_lse(res["o"][rows], res["lse"][rows], o_ref, l_ref, "wide full size")
+    res = run_attention(F, q, k, v, w.scale, **({"num_splits": 0} if mode == "split" else {}))
+    rows = stratified_rows(w, all_units=True, edge_units=range(w.B * w.Hkv), tile=128, extra=32, seed=4)
+    o_ref, l_ref = oracle_rows(w, rows, tensors=(q, k, v))
+    check_o_lse(res["o"][rows], res["lse"][rows], o_ref, l_ref, f"wide full size ({mode})")
     assert np.all(np.isfinite(res["o"])) and np.all(np.isfinite(res["lse"]))
     del q, k, v
     torch.cuda.empty_cache()

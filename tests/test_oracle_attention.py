@@ -110,6 +110,37 @@ def test_zero_query_gives_mean_and_log_n():
     assert abs(lse[0] - math.log(n)) < 1e-14
 
 
+@pytest.mark.parametrize("sigma,causal,ragged", [(1.0, False, False), (4.0, False, False), (1.0, True, False),
+                                                  (2.0, True, True)])
+def test_softmax_rows_sum_to_one_constant_values(sigma, causal, ragged):
+    """Softmax rows sum to 1, so a constant value matrix V = c gives O = c for every visible row,
+    whatever the scores (large sigma: very skewed weights), the mask or the key lengths."""
+    B, H, Sq, Skv, D = 2, 2, 5, 300, 16
+    q, k = _bf16((B, H, Sq, D), 60, sigma), _bf16((B, H, Skv, D), 61, sigma)
+    sl = np.array([300, 7], dtype=np.int32) if ragged else None
+    for c in (1.0, -2.5):
+        v = torch.full((B, H, Skv, D), c, dtype=torch.bfloat16)
+        o, lse = oracle.attention(q, k, v, 0.3, seqlens_k=sl, causal=causal)
+        vis = np.isfinite(lse)
+        assert vis.all()   # every query of these shapes sees at least one key
+        # FP64 summation of n terms: relative error at most about n * 2^-52
+        np.testing.assert_allclose(o, c, rtol=Skv * 2.0 ** -52, atol=0)
+
+
+def test_softmax_rows_sum_to_one_identity_values():
+    """With V = I (value row j is the j-th unit vector), O is the softmax row itself: its entries
+    must equal exp(s_j - max) / sum_j exp(s_j - max) computed directly, and each row sums to 1."""
+    Skv = D = 48
+    q, k = _bf16((1, 3, 4, D), 62, 2.0), _bf16((1, 3, Skv, D), 63, 2.0)
+    v = torch.eye(Skv, dtype=torch.bfloat16).expand(1, 3, Skv, D).contiguous()
+    scale = 0.25
+    o, _ = oracle.attention(q, k, v, scale)
+    s = scale * (q.double() @ k.double().transpose(-1, -2)).reshape(-1, Skv).numpy()
+    e = np.exp(s - s.max(axis=1, keepdims=True))
+    np.testing.assert_allclose(o, e / e.sum(axis=1, keepdims=True), rtol=0, atol=1e-15)
+    np.testing.assert_allclose(o.sum(axis=1), 1.0, rtol=0, atol=Skv * 2.0 ** -52)
+
+
 def test_joint_permutation_invariance():
     q, k, v = _bf16((1, 2, 4, 32), 21), _bf16((1, 2, 64, 32), 22), _bf16((1, 2, 64, 32), 23)
     perm = torch.randperm(64, generator=torch.Generator().manual_seed(0))

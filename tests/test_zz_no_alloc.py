@@ -3,8 +3,8 @@
 fmha_fwd_decode_noalloc serves callers that cannot give the library a workspace (plug-ins and
 bindings that only see tensor pointers, loops that may not call cudaMalloc): its split-KV scratch
 is a fixed array inside the library.  Two calls in a row, with different shapes, must match the
-workspace-based entry point (fmha_fwd_ex) within the parity tolerances, and a problem too large
-for the fixed array must be refused with FMHA_ERR_WORKSPACE.
+FP64 oracle and the workspace-based entry point (fmha_fwd_ex) within the parity tolerances, and a
+problem too large for the fixed array must be refused with FMHA_ERR_WORKSPACE.
 
 Named to be collected last, so a run that stops at the first failure has run every other test."""
 import ctypes
@@ -13,8 +13,9 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from attention_tensor_cores_gb300 import inputs
-from attn_util import check_o_lse, run_attention
+from attn_util import check_o_lse, oracle_rows, run_attention
 
 pytestmark = pytest.mark.gpu
 
@@ -38,21 +39,28 @@ def _noalloc(F, q, k, v, scale, seqlens=None):
     return out.float().cpu().numpy().reshape(-1, D), lse.cpu().numpy().reshape(-1)
 
 
-def test_two_calls_match_workspace_entry_point(F):
-    # call 1: the decode workload (B8 H32 Sq1 Skv4096 D128)
+def test_two_calls_match_workspace_entry_point_and_oracle(F):
+    """Two calls in a row on the shared scratch, each checked element by element against the FP64
+    oracle and against the workspace-based entry point, within the parity tolerances."""
+    # call 1: the decode workload (B8 H32 Sq1 Skv4096 D128), every row
     w = inputs.workloads()[1]
     q, k, v, _ = w.make("cuda")
     o1, l1 = _noalloc(F, q, k, v, w.scale)
+    o_ref, l_ref = oracle_rows(w, np.arange(w.B * w.Hq * w.Sq), tensors=(q, k, v))
+    check_o_lse(o1, l1, o_ref, l_ref, "noalloc call 1 vs oracle")
     ref = run_attention(F, q, k, v, w.scale, num_splits=0)
-    check_o_lse(o1, l1, ref["o"].astype(np.float64), ref["lse"].astype(np.float64), "noalloc call 1")
+    check_o_lse(o1, l1, ref["o"].astype(np.float64), ref["lse"].astype(np.float64), "noalloc call 1 vs fmha_fwd_ex")
     del q, k, v
     # call 2: another shape on the same scratch (GQA, Sq = 2, ragged keys including an empty set)
     w2 = inputs.Workload("t", 5, 8, 2, 2, 900, 64, 1.0, "bf16", 31)
     q, k, v, _ = w2.make("cuda")
-    sl = torch.tensor([0, 1, 900, 129, 513], dtype=torch.int32, device="cuda")
+    lens = [0, 1, 900, 129, 513]
+    sl = torch.tensor(lens, dtype=torch.int32, device="cuda")
     o2, l2 = _noalloc(F, q, k, v, w2.scale, sl)
+    o_ref2, l_ref2 = oracle.attention(q.cpu(), k.cpu(), v.cpu(), w2.scale, seqlens_k=np.array(lens, np.int32))
+    check_o_lse(o2, l2, o_ref2, l_ref2, "noalloc call 2 vs oracle")
     ref2 = run_attention(F, q, k, v, w2.scale, seqlens=sl, num_splits=0)
-    check_o_lse(o2, l2, ref2["o"].astype(np.float64), ref2["lse"].astype(np.float64), "noalloc call 2")
+    check_o_lse(o2, l2, ref2["o"].astype(np.float64), ref2["lse"].astype(np.float64), "noalloc call 2 vs fmha_fwd_ex")
     assert np.all(o2[:16] == 0.0) and np.all(np.isneginf(l2[:16]))
 
 
