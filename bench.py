@@ -323,9 +323,14 @@ def oracle_sample(w, rows_per_step: int, step: int):
     return run, kv_bytes, flops, f"{len(rows)} query rows from row {r0}"
 
 
-def cpu_baseline(w, metric_unit: str, budget_s: float = 8.0, rows_per_step: int = 64):
+def cpu_baseline(w, metric_unit: str, budget_s: float = 6.0, rows_per_step: int = 64):
+    """The oracle as it stands, timed on this host's cores on a bounded sample of workload `w`:
+    `rows_per_step` consecutive query rows (the whole workload when it has fewer), repeated until
+    `budget_s` of CPU time.  metric_unit: "GB/s" (K/V bytes of the sample's heads), "TFLOP/s"
+    (its 4*D FLOPs per query-key pair) or "us" (time per pass over the whole workload)."""
     import oracle
-    run, kvb, fl, desc = oracle_sample(w, rows_per_step, 0)
+    rows = min(rows_per_step, w.B * w.Hq * w.Sq)
+    run, kvb, fl, desc = oracle_sample(w, rows, 0)
     run()   # builds/loads the library, touches memory
     t0 = time.perf_counter()
     reps = 0
@@ -333,12 +338,12 @@ def cpu_baseline(w, metric_unit: str, budget_s: float = 8.0, rows_per_step: int 
         run()
         reps += 1
         el = time.perf_counter() - t0
-        if el >= budget_s or reps >= 50:
+        if el >= budget_s or reps >= 200:
             break
     per = el / reps
-    val = (kvb / per / 1e9) if metric_unit == "GB/s" else (fl / per / 1e12)
+    val = {"GB/s": lambda: kvb / per / 1e9, "TFLOP/s": lambda: fl / per / 1e12, "us": lambda: per * 1e6}[metric_unit]()
     return {"value": val, "unit": metric_unit, "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"{desc} of {w.name}, {reps} repetitions, {per * 1e3:.1f} ms each"}
+            "sample": f"{desc} of {w.name}, {reps} repetitions, {per * 1e3:.2f} ms each"}
 
 
 # ------------------------------------------------------------------------------------------------
@@ -360,6 +365,40 @@ def aggregate_rate(units_per_rank_per_step: float, steps: int, world: int, regio
     return world * steps * units_per_rank_per_step / (region_ms_max / 1e3)
 
 
+def read_only_peak_gbs(gib: float = 4.0, reps: int = 10) -> float:
+    """A read-only stream rate for the KV-bound rows: torch.sum over `gib` GiB of FP32 (one pass,
+    nothing written back but the scalar), best of `reps`, CUDA events.  The decode kernels mostly
+    read, so they can exceed a copy benchmark (read + write) figure; this probe says by how much."""
+    import torch
+    n = int(gib * 2 ** 30) // 4
+    x = torch.ones(n, dtype=torch.float32, device="cuda")
+    best = float("inf")
+    for _ in range(reps + 2):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        x.sum()
+        b.record()
+        torch.cuda.synchronize()
+        best = min(best, a.elapsed_time(b))
+    del x
+    torch.cuda.empty_cache()
+    return n * 4 / (best / 1e3) / 1e9
+
+
+def hbm_roofline(achieved: float, peaks: dict, read_peak: float | None) -> dict:
+    """HBM roofline entry against the measured copy bandwidth, with the read-only probe beside it;
+    a fraction above 1 of the copy figure is flagged (read-mostly traffic, not a timing error, as
+    long as the read-only fraction stays at or below 1)."""
+    r = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+         "frac": achieved / peaks["hbm_gbs"]}
+    if read_peak:
+        r["read_only_peak"] = read_peak
+        r["frac_of_read_only"] = achieved / read_peak
+    if r["frac"] > 1.0:
+        r["flag"] = "above the copy-bandwidth peak: the kernel reads far more than it writes"
+    return r
+
+
 def l2_note(in_bytes: int) -> str:
     """How the timed steps avoid measuring from a warm L2: inputs larger than L2, else say it fits."""
     import torch
@@ -369,10 +408,10 @@ def l2_note(in_bytes: int) -> str:
     return f"inputs fit in L2 ({in_bytes / 2**10:.0f} KiB, L2 {l2 / 2**20:.1f} MiB): latency figure, no roofline claim"
 
 
-def _workload_entry(F, w, idx, steps, warmup, peaks, causal=False, given_scale=False):
+def _workload_entry(F, w, idx, steps, warmup, peaks, causal=False, given_scale=False, read_peak=None, cpu=False):
     """Timing + roofline of one extra workload (rank 0 only).  given_scale: NVFP4 in one pass with the
     per-tensor scale of an earlier (two-pass) call on the same inputs, as a caller reusing the
-    previous step's scale would."""
+    previous step's scale would.  cpu: also time the oracle on a bounded sample of it."""
     import torch
     case = Case(F, w, num_splits=0, causal=causal)
     if given_scale:
@@ -384,6 +423,7 @@ def _workload_entry(F, w, idx, steps, warmup, peaks, causal=False, given_scale=F
     kern_ms = statistics.mean(r["kernel_ms"])
     e = {"workload": w.name, "ms_per_step": step_ms, "kernel_ms": kern_ms, "gpu_launches_per_step": r["launches"] / steps,
          "l2": l2_note(w.kv_bytes() + case.q.numel() * 2)}
+    unit = "us"
     if idx == 2:   # prefill: tensor-bound
         flops = causal_flops(w) if causal else w.flops()
         tf = flops / (step_ms / 1e3) / 1e12
@@ -392,19 +432,50 @@ def _workload_entry(F, w, idx, steps, warmup, peaks, causal=False, given_scale=F
         e.update({"value": tf, "unit": "TFLOP/s",
                   "roofline": {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                                "frac": ach / peaks["bf16_tflops"], "traffic": None}})
+        unit = "TFLOP/s"
     elif idx == 0:
         e.update({"value": step_ms * 1e3, "unit": "us", "note": "latency-bound, fits in L2: no roofline claim"})
     else:
         gbs = w.kv_bytes() / (step_ms / 1e3) / 1e9
         ach = case.algorithmic_bytes() / (kern_ms / 1e3) / 1e9
-        traffic = traffic_for("wide_kernel", "wide.cu") if w.D == 512 else None
+        if w.D == 512:
+            traffic = traffic_for("wide_kernel", "wide.cu")
+        elif w.ragged and not causal:
+            traffic = traffic_for("decode_kernel<128>/ragged", "decode.cu")
+        else:
+            traffic = None
+        roof = hbm_roofline(ach, peaks, read_peak)
+        roof["traffic"] = traffic
         e.update({"value": gbs, "unit": "GB/s", "kv_bytes": w.kv_bytes(), "flops": w.flops(),
-                  "tflops": w.flops() / (step_ms / 1e3) / 1e12,
-                  "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                               "frac": ach / peaks["hbm_gbs"], "traffic": traffic}})
+                  "tflops": w.flops() / (step_ms / 1e3) / 1e12, "roofline": roof})
+        unit = "GB/s"
     del case
     torch.cuda.empty_cache()
+    if cpu:
+        e["cpu_baseline"] = cpu_baseline(w, unit)
     return e
+
+
+def _summary(head: dict, extra: dict) -> dict:
+    """Compact per-configuration figures (step value, dominant kernel's roofline fraction, the
+    oracle's rate on this host) printed last on the line, so that a reader of its tail sees all five."""
+    def r4(x):
+        return None if x is None else float(f"{x:.4g}")
+
+    out = {"c2": {"value": r4(head["value"]), "unit": "GB/s", "ms": r4(head["ms_per_step"]),
+                  "kernel_frac": r4(head["roofline"]["frac"]),
+                  "cpu": r4(head["cpu"]["value"]) if head.get("cpu") else None}}
+    for key in ("c1", "c3", "c4", "c5", "c5_given_scale", "c2_spec_causal", "c3_d128", "c3_causal", "c3_chunked_varlen"):
+        e = extra.get(key)
+        if not e or "value" not in e:
+            continue
+        d = {"value": r4(e["value"]), "unit": e["unit"], "ms": r4(e["ms_per_step"])}
+        if "roofline" in e:
+            d["kernel_frac"] = r4(e["roofline"]["frac"])
+        if "cpu_baseline" in e:
+            d["cpu"] = r4(e["cpu_baseline"]["value"])
+        out[key] = d
+    return out
 
 
 def run_ours(args, rank, world, local):
@@ -426,6 +497,7 @@ def run_ours(args, rank, world, local):
     from attention_tensor_cores_gb300 import inputs
     F.load()
     peaks, peaks_src = load_peaks()
+    read_peak = read_only_peak_gbs() if rank == 0 else None
     wl = inputs.workloads()
     w = wl[1]
     head = Case(F, w, num_splits=0)
@@ -436,10 +508,10 @@ def run_ours(args, rank, world, local):
     value = aggregate_rate(w.kv_bytes(), args.steps, world, region_ms) / 1e9
     kern_ms = statistics.mean(r["kernel_ms"])
     achieved = head.algorithmic_bytes() / (kern_ms / 1e3) / 1e9
-    roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-            "frac": achieved / peaks["hbm_gbs"], "traffic": traffic_for("decode_kernel<128>", "decode.cu"),
-            "kernel": "decode_kernel<128>", "kernel_ms": kern_ms, "algorithmic_bytes": head.algorithmic_bytes(),
-            "peak_source": f"{peaks_src} HBM copy bandwidth (burst)"}
+    roof = hbm_roofline(achieved, peaks, read_peak)
+    roof.update({"traffic": traffic_for("decode_kernel<128>", "decode.cu"),
+                 "kernel": "decode_kernel<128>", "kernel_ms": kern_ms, "algorithmic_bytes": head.algorithmic_bytes(),
+                 "peak_source": f"{peaks_src} HBM copy bandwidth (burst); read_only_peak: torch.sum over 4 GiB in this run"})
     e2e_ms, h2d, d2h = time_e2e(F, head, args.steps, min(args.warmup, 3))
     e2e_ms = _max_over_ranks(e2e_ms, dist)
     e2e = {"value": world * w.kv_bytes() / (e2e_ms / 1e3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
@@ -451,16 +523,17 @@ def run_ours(args, rank, world, local):
     if rank == 0 and not args.only_headline:
         for idx in (0, 2, 3, 4):
             try:
-                extra[f"c{idx + 1}"] = _workload_entry(F, wl[idx], idx, min(args.steps, 10), args.warmup, peaks)
+                extra[f"c{idx + 1}"] = _workload_entry(F, wl[idx], idx, min(args.steps, 10), args.warmup, peaks,
+                                                       read_peak=read_peak, cpu=(world == 1 and not args.no_cpu))
             except F.FmhaError as ex:
                 extra[f"c{idx + 1}"] = {"workload": wl[idx].name, "unsupported": str(ex)}
         try:   # the ragged NVFP4 workload in one pass, with a given per-tensor scale
-            extra["c5_given_scale"] = _workload_entry(F, wl[4], 4, min(args.steps, 10), args.warmup, peaks, given_scale=True)
+            extra["c5_given_scale"] = _workload_entry(F, wl[4], 4, min(args.steps, 10), args.warmup, peaks, given_scale=True, read_peak=read_peak)
             extra["c5_given_scale"]["workload"] = wl[4].name.replace("(NVFP4 out)", "(NVFP4 out, one pass with a given scale)")
         except F.FmhaError as ex:
             extra["c5_given_scale"] = {"workload": "ragged NVFP4, given scale", "unsupported": str(ex)}
         try:   # decode with several new tokens per head (speculative or chunked decode), causal mask
-            extra["c2_spec_causal"] = _workload_entry(F, spec_decode_workload(), 1, min(args.steps, 10), args.warmup, peaks, causal=True)
+            extra["c2_spec_causal"] = _workload_entry(F, spec_decode_workload(), 1, min(args.steps, 10), args.warmup, peaks, causal=True, read_peak=read_peak)
         except F.FmhaError as ex:
             extra["c2_spec_causal"] = {"workload": "speculative decode", "unsupported": str(ex)}
         try:   # the prefill workload at head dim 128
@@ -477,7 +550,7 @@ def run_ours(args, rank, world, local):
             extra["c3_causal"]["workload"] = wl[2].name.replace("non-causal", "causal")
         except F.FmhaError as ex:
             extra["c3_causal"] = {"workload": "causal prefill", "unsupported": str(ex)}
-    cpu = cpu_baseline(w, "GB/s") if (rank == 0 and world == 1) else None
+    cpu = cpu_baseline(w, "GB/s") if (rank == 0 and world == 1 and not args.no_cpu) else None
     if dist is not None:
         dist.barrier()
     if rank != 0:
@@ -493,6 +566,7 @@ def run_ours(args, rank, world, local):
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": r["launches"],
         "clocks": r["clocks"], "workloads": extra,
     }
+    line["summary"] = _summary({"value": value, "ms_per_step": step_ms, "roofline": roof, "cpu": cpu}, extra)
     print(json.dumps(line), flush=True)
 
 
@@ -544,6 +618,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--only-headline", action="store_true", help="skip the other workloads")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the oracle's CPU baselines")
     ap.add_argument("--profile", choices=["c1", "c2", "c3", "c4", "c5", "c3_causal", "c3_d128", "c5_given_scale", "c2_spec_causal"], default=None,
                     help="run one workload's call --repeat times, untimed (for a profiler)")
     ap.add_argument("--repeat", type=int, default=5)
