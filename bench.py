@@ -165,6 +165,14 @@ def spec_decode_workload():
                            8, 32, 8, 4, 8192, 128, 1.0, "bf16", 1006)
 
 
+def ragged_nvfp4_small_workload():
+    """A quarter of the ragged GQA NVFP4 workload (B16 instead of B64, same heads, key lengths from
+    U{1..32768}, seed 1004): small enough for a multi-pass profiler capture (about 2 GiB of K/V)."""
+    from attention_tensor_cores_gb300 import inputs
+    return inputs.Workload("ragged GQA decode B16 Hq32 Hkv8 Sq1 Skv<=32768 D128 (NVFP4 out)", 16, 32, 8, 1, 32768,
+                           128, 1.0, "nvfp4", 1004, ragged=True)
+
+
 # ------------------------------------------------------------------------------------------------
 # one workload on the GPU
 # ------------------------------------------------------------------------------------------------
@@ -619,7 +627,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--only-headline", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle's CPU baselines")
-    ap.add_argument("--profile", choices=["c1", "c2", "c3", "c4", "c5", "c3_causal", "c3_d128", "c5_given_scale", "c2_spec_causal"], default=None,
+    ap.add_argument("--profile", choices=["c1", "c2", "c3", "c4", "c5", "c3_causal", "c3_d128", "c5_given_scale", "c2_spec_causal",
+                                          "c5_small"], default=None,
                     help="run one workload's call --repeat times, untimed (for a profiler)")
     ap.add_argument("--repeat", type=int, default=5)
     args = ap.parse_args()
@@ -633,6 +642,8 @@ def main():
             w = spec_decode_workload()
         elif args.profile == "c3_d128":
             w = d128_prefill_workload()
+        elif args.profile == "c5_small":
+            w = ragged_nvfp4_small_workload()
         else:
             w = inputs.workloads()[int(args.profile[1]) - 1]
         case = Case(F, w, num_splits=0, causal=args.profile in ("c3_causal", "c2_spec_causal"))
