@@ -166,7 +166,7 @@ def stratified_rows(w: inputs.Workload, all_units: bool = True, edge_units=None,
         for u in range(U):
             a, e = unit_rows(w, u)
             rows.add(int(rng.integers(a, e)))
-    for u in (edge_units or []):
+    for u in ([] if edge_units is None else edge_units):
         a, e = unit_rows(w, int(u))
         for t0 in range(a, e, tile):
             rows.add(t0)
