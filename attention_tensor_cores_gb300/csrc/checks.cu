@@ -9,6 +9,10 @@
 //     threads with the 128-byte swizzle (the decode kernel's PV product).
 //   * selftest 3: O = P V with P in Tensor Memory (TS form) and V MN-major in shared memory (the
 //     row-tile kernel's PV product).
+//   * selftest 4: the CTA-pair MMA (tcgen05 cta_group::2, M = 256) in both operand forms: which rows of
+//     A and D, and which half of B's columns, live in which CTA of the pair, and the two ways a pair
+//     can signal across its CTAs (a commit or a TMA completion aimed at the other CTA's mbarrier, or
+//     a relay through an ordinary cluster-scope arrive).
 #include <cuda_runtime.h>
 
 #include "internal.h"
@@ -284,6 +288,137 @@ __global__ void __launch_bounds__(128) pv_ts_kernel(const __grid_constant__ CUte
     if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
+// ---- selftest 4: CTA-pair MMA -----------------------------------------------------------------
+// flags bit 0 = 0 (SS): D[256][128] = A[256][64] B[128][64]^T, both K-major; CTA r of the pair loads A
+//   rows 128r.. and B rows 64r.. into its own shared memory.
+// flags bit 0 = 1 (TS): D[256][256] = A[256][32] V[32][256]; each CTA writes its 128 rows of A into its
+//   own Tensor Memory; V is MN-major and CTA r loads its columns 128r..128r+127.
+// flags bit 1: the leader's commit also arrives on the odd CTA's barrier directly (else the leader
+//   relays the completion with a cluster-scope arrive).  bit 2: the odd CTA's TMA counts its bytes
+//   on the leader's barrier (else the odd CTA waits for its own copy and relays an arrive).
+// out: [2][128][N] FP32 (CTA rank, TMEM lane, column), then 2 floats: 1 where a CTA's wait gave up.
+constexpr int kPairRegion = 32768;
+constexpr int kPairSmem = 2 * kPairRegion + 1024;
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(128)
+    pair_mma_kernel(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUtensorMap bmap, const uint16_t* A,
+                    float* out, int flags, int* status, long long limit)
+{
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sA = smem;                  // SS: 128 rows x 128 B
+    uint8_t* sB = smem + kPairRegion;    // SS: 64 rows x 128 B; TS: two atoms of 32 rows x 128 B
+    __shared__ uint64_t full_local, full_pair, done;
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_flag;
+    const int warp = threadIdx.x / 32;
+    const uint32_t rank = cluster_ctarank();
+    const int ts = flags & 1;
+    const bool direct_commit = (flags & 2) != 0, direct_tma = (flags & 4) != 0;
+    const int N = ts ? 256 : 128;
+    WaitCtl wc{&abort_flag, status, limit};
+    // both regions zeroed, so a read outside what the copies wrote shows up as zeros
+    for (int i = threadIdx.x; i < 2 * kPairRegion / 16; i += 128) reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        mbar_init(&full_local, 1);
+        mbar_init(&full_pair, direct_tma ? 1 : 2);
+        mbar_init(&done, 1);
+        fence_barrier_init();
+    }
+    if (warp == 0) {
+        tmem_alloc_pair(&tmem_slot, 512);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();   // the other CTA's barriers are initialised before anything arrives on them
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+    const uint32_t leader_full = mapa_shared(smem_u32(&full_pair), 0);
+    const uint32_t other_done = mapa_shared(smem_u32(&done), rank ^ 1u);
+    if (ts) {
+        // this CTA's rows of A as packed BF16 pairs at Tensor Memory column 256 (element 2c in bits 15:0)
+        const int row = 128 * static_cast<int>(rank) + static_cast<int>(threadIdx.x);
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            w[i] = static_cast<uint32_t>(A[row * 32 + 2 * i]) | (static_cast<uint32_t>(A[row * 32 + 2 * i + 1]) << 16);
+        tmem_st16(tmem_addr(tmem, warp * 32, 256), w);
+        tmem_st_wait();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();   // both CTAs' Tensor Memory operands are written
+    tc_fence_after();
+    const uint32_t own = ts ? 8192u : 16384u + 8192u;   // bytes this CTA loads
+    if (threadIdx.x == 0) {
+        if (rank == 0) {
+            mbar_arrive_expect_tx(&full_pair, direct_tma ? 2 * own : own);
+            if (!ts) tma_load_3d(sA, &amap, &full_pair, 0, 0, 0);
+            if (!ts) tma_load_3d(sB, &bmap, &full_pair, 0, 0, 0);
+            else {
+                tma_load_3d(sB, &bmap, &full_pair, 0, 0, 0);
+                tma_load_3d(sB + 4096, &bmap, &full_pair, 64, 0, 0);
+            }
+        } else if (direct_tma) {
+            if (!ts) tma_load_3d_pair(sA, &amap, leader_full, 0, 128, 0);
+            if (!ts) tma_load_3d_pair(sB, &bmap, leader_full, 0, 64, 0);
+            else {
+                tma_load_3d_pair(sB, &bmap, leader_full, 128, 0, 0);
+                tma_load_3d_pair(sB + 4096, &bmap, leader_full, 192, 0, 0);
+            }
+        } else {
+            mbar_arrive_expect_tx(&full_local, own);
+            if (!ts) tma_load_3d(sA, &amap, &full_local, 0, 128, 0);
+            if (!ts) tma_load_3d(sB, &bmap, &full_local, 0, 64, 0);
+            else {
+                tma_load_3d(sB, &bmap, &full_local, 128, 0, 0);
+                tma_load_3d(sB + 4096, &bmap, &full_local, 192, 0, 0);
+            }
+            if (mbar_wait(&full_local, 0, wc)) mbar_arrive_cluster(leader_full);
+        }
+        if (rank == 0) {
+            if (mbar_wait_cluster(&full_pair, 0, wc)) {
+                tc_fence_after();
+                if (!ts) {
+                    constexpr uint32_t idesc = idesc_bf16_f32(256, 128, false, false);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_ss_pair(tmem, sdesc_sw128(smem_u32(sA) + kk * 32, 16, 1024),
+                                    sdesc_sw128(smem_u32(sB) + kk * 32, 16, 1024), idesc, kk > 0 ? 1u : 0u);
+                } else {
+                    constexpr uint32_t idesc = idesc_bf16_f32(256, 256, false, true);
+#pragma unroll
+                    for (int ks = 0; ks < 2; ++ks)
+                        mma_ts_pair(tmem, tmem + 256 + ks * 8, sdesc_sw128(smem_u32(sB) + ks * 2048, 4096, 1024), idesc,
+                                    ks > 0 ? 1u : 0u);
+                }
+                mma_commit_pair(smem_u32(&done));
+                if (direct_commit) mma_commit_pair(other_done);
+                if (!direct_commit && mbar_wait(&done, 0, wc)) mbar_arrive_cluster(other_done);
+            }
+        }
+    }
+    __syncwarp();
+    const bool ok = mbar_wait_cluster(&done, 0, wc);
+    tc_fence_after();
+    for (int c = 0; c < N; c += 32) {
+        uint32_t r[32];
+        tmem_ld32p(tmem_addr(tmem, warp * 32, c), r);
+        tmem_ld_wait();
+        float* o = out + (static_cast<size_t>(rank) * 128 + threadIdx.x) * N + c;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(r[i]);
+    }
+    if (threadIdx.x == 0) out[2 * 128 * N + rank] = (ok && !aborted(wc)) ? 0.f : 1.f;
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();   // no CTA frees Tensor Memory or exits while the other may still use its barriers
+    if (warp == 0) tmem_dealloc_pair(tmem, 512);
+}
+
 }  // namespace
 
 int launch_qk_gemm(const void* q, const void* k, float* s, int Sq, int Skv, int D, cudaStream_t st)
@@ -341,6 +476,34 @@ int launch_selftest(int which, const void* in, void* out, size_t out_bytes, int 
                                                wait_limit());
             FMHA_CHECK_LAUNCH("pv_ts_kernel");
         }
+        return FMHA_OK;
+    }
+    if (which == 4) {
+        // in: A (SS: [256][64], TS: [256][32]) then B (SS: [128][64], TS: V [32][256]), BF16 row-major
+        const int ts = param & 1;
+        const int N = ts ? 256 : 128;
+        if (out_bytes < (static_cast<size_t>(2) * 128 * N + 2) * 4) return set_error(FMHA_ERR_INVALID, "selftest 4: out too small");
+        const uint16_t* A = static_cast<const uint16_t*>(in);
+        const uint16_t* B = A + (ts ? 256 * 32 : 256 * 64);
+        CUtensorMap amap, bmap;
+        {
+            const uint64_t dims[3] = {64, 256, 1};
+            const uint64_t strides[2] = {128, 256 * 128};
+            const uint32_t box[3] = {64, 128, 1};
+            int rc = make_tmap_bf16(&amap, A, 3, dims, strides, box);
+            if (rc) return rc;
+        }
+        {
+            const uint64_t dims[3] = {ts ? 256u : 64u, ts ? 32u : 128u, 1};
+            const uint64_t strides[2] = {ts ? 512u : 128u, ts ? 32u * 512u : 128u * 128u};
+            const uint32_t box[3] = {64, ts ? 32u : 64u, 1};
+            int rc = make_tmap_bf16(&bmap, B, 3, dims, strides, box);
+            if (rc) return rc;
+        }
+        FMHA_CHECK_CUDA(cudaFuncSetAttribute(pair_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmem));
+        pair_mma_kernel<<<2, 128, kPairSmem, st>>>(amap, bmap, A, static_cast<float*>(out), param, device_status_ptr(),
+                                                   wait_limit());
+        FMHA_CHECK_LAUNCH("pair_mma_kernel");
         return FMHA_OK;
     }
     return set_error(FMHA_ERR_INVALID, "selftest: unknown test id");

@@ -84,3 +84,27 @@ def test_pv_p_in_tensor_memory(F, D):
     F.fmha_selftest(3, inp, out, D)
     got = out.cpu().double().numpy().reshape(128, D)
     np.testing.assert_array_equal(got, (P.double() @ V.double()).numpy())
+
+
+@pytest.mark.parametrize("flags", [0, 1, 2, 3, 4, 5, 6, 7])
+def test_pair_mma_layout(F, flags):
+    """The CTA-pair MMA (cta_group::2, M = 256) on integer inputs, bit-exact: the even CTA's Tensor
+    Memory holds rows 0..127 of D and the odd CTA's rows 128..255 (each from its own rows of A), and
+    B's columns come half from each CTA's shared memory, the first half from the even CTA.
+    flags bit 0: A from Tensor Memory (TS form, B = V MN-major) instead of shared memory (SS form);
+    bit 1: the completion reaches the odd CTA by a commit aimed at its barrier (else a relayed arrive);
+    bit 2: the odd CTA's copy counts its bytes on the even CTA's barrier (else a relayed arrive)."""
+    ts = flags & 1
+    N, K = (256, 32) if ts else (128, 64)
+    A = _ints((256, K), 10 + flags)
+    B = _ints((K, N), 20 + flags) if ts else _ints((N, K), 20 + flags)
+    inp = torch.cat([A.reshape(-1), B.reshape(-1)]).cuda()
+    out = torch.full((2 * 128 * N + 2,), float("nan"), dtype=torch.float32, device="cuda")
+    F.fmha_selftest(4, inp, out, flags)
+    torch.cuda.synchronize()
+    assert F.fmha_check_status() == 0
+    got = out.cpu().double().numpy()
+    assert got[-2] == 0.0 and got[-1] == 0.0, "a wait gave up"
+    D = got[: 2 * 128 * N].reshape(256, N)
+    ref = (A.double() @ (B.double() if ts else B.double().T)).numpy()
+    np.testing.assert_array_equal(D, ref)
