@@ -27,6 +27,9 @@ FMHA_ERR_RACE = 6
 FMHA_OUT_BF16 = 0
 FMHA_OUT_F32 = 1
 FMHA_OUT_NVFP4 = 2
+FMHA_WIDE_AUTO = 0
+FMHA_WIDE_INDEPENDENT = 1
+FMHA_WIDE_PAIR = 2
 
 _lock = threading.Lock()
 _lib = None
@@ -51,6 +54,7 @@ class fmha_opts(ctypes.Structure):
         ("causal", ctypes.c_int),
         ("nvfp4_scale_in", ctypes.c_void_p),
         ("out_amax", ctypes.c_void_p),
+        ("wide_variant", ctypes.c_int),
     ]
 
 
@@ -147,8 +151,9 @@ def fmha_fwd(q, k, v, out, lse, scale: float, stream=None):
 
 def make_opts(out_kind=FMHA_OUT_BF16, seqlens_k=None, num_splits=0, workspace=None,
               out_scales=None, out_tensor_scale=None, out_f32=None, causal=False,
-              nvfp4_scale_in=None, out_amax=None) -> fmha_opts:
+              nvfp4_scale_in=None, out_amax=None, wide_variant=FMHA_WIDE_AUTO) -> fmha_opts:
     o = fmha_opts()
+    o.wide_variant = wide_variant
     o.causal = 1 if causal else 0
     o.nvfp4_scale_in = None if nvfp4_scale_in is None else nvfp4_scale_in.data_ptr()
     o.out_amax = None if out_amax is None else out_amax.data_ptr()

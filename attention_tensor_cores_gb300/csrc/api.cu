@@ -268,6 +268,8 @@ static int validate(const void* q, const void* k, const void* v, const void* out
     if (o) {
         if (o->out_kind < FMHA_OUT_BF16 || o->out_kind > FMHA_OUT_NVFP4) return set_error(FMHA_ERR_INVALID, "bad out_kind");
         if (o->num_splits < 0) return set_error(FMHA_ERR_INVALID, "num_splits must be >= 0");
+        if (o->wide_variant < FMHA_WIDE_AUTO || o->wide_variant > FMHA_WIDE_PAIR)
+            return set_error(FMHA_ERR_INVALID, "bad wide_variant");
         if (o->out_kind == FMHA_OUT_NVFP4) {
             if (!o->out_scales || !o->out_tensor_scale)
                 return set_error(FMHA_ERR_INVALID, "NVFP4 output needs out_scales and out_tensor_scale");
@@ -305,6 +307,7 @@ static AttnArgs make_args(const void* q, const void* k, const void* v, void* out
     a.out_f32 = (o && o->out_kind == FMHA_OUT_NVFP4) ? o->out_f32 : nullptr;
     a.causal = (o && o->causal) ? 1 : 0;
     a.nv_sg = (o && o->out_kind == FMHA_OUT_NVFP4) ? o->nvfp4_scale_in : nullptr;
+    a.wide_variant = o ? o->wide_variant : FMHA_WIDE_AUTO;
     return a;
 }
 

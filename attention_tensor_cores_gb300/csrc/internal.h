@@ -67,6 +67,7 @@ struct AttnArgs {
     uint8_t* nv_codes;       // E2M1 codes [rows][D/2]
     uint8_t* nv_scales;      // E4M3 block scales [rows][D/16]
     float* nv_ts;            // receives s_g
+    int wide_variant;        // D = 512: FMHA_WIDE_* (fmha_opts.wide_variant)
 };
 
 // Decode / small-group path (query rows per key/value head <= 16): swap-AB kernels.

@@ -27,6 +27,8 @@
 //    warp 4 loads Q, K and V, warp 5 issues the MMAs in order.  All waits are bounded.
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "internal.h"
 #include "nvfp4_dev.cuh"
 #include "ptx.cuh"
@@ -39,10 +41,7 @@ constexpr int kWHalf = 256;         // value columns per CTA
 constexpr int kWRows = 128;         // query rows per unit (MMA M)
 constexpr int kWKeys = 128;         // keys per tile (QK N, PV K)
 constexpr int kWKChunks = 8;        // K chunks per tile: 64 contraction columns each
-constexpr int kWVChunks = 4;        // V chunks per tile: 32 keys each
-constexpr int kWVKeys = kWKeys / kWVChunks;
-constexpr int kWChunkBytes = 16384;
-constexpr int kWSlots = 6;          // chunk ring depth
+constexpr int kWVKeys = 32;         // keys per V chunk
 constexpr int kWThreads = 192;      // 4 softmax warps, producer, MMA issuer
 constexpr float kLog2eW = 1.4426950408889634f;
 constexpr float kLn2W = 0.6931471805599453f;
@@ -51,15 +50,35 @@ constexpr float kRescaleW = 8.0f;
 constexpr int kWQBytes = 8 * kWRows * 128;          // 8 atoms of 128 rows x 128 B = 128 KB
 constexpr int kWOffQ = 0;
 constexpr int kWOffRing = kWOffQ + kWQBytes;
-constexpr int kWSmem = kWOffRing + kWSlots * kWChunkBytes + 1024;
-static_assert(kWKeys * 128 == kWChunkBytes && 4 * kWVKeys * 128 == kWChunkBytes, "chunk layouts");
-// TMEM columns: S 0..127, P 128..191 (BF16 pairs of 128 keys), O half 256..511.
+
+// Chunk geometry of the two variants.
+//  * Independent CTAs (PAIR = false): a K chunk is 64 contraction columns of the tile's 128 keys
+//    (16 KB), a V chunk 32 keys by this CTA's 256 value columns (4 atoms, 16 KB); 6 ring slots.
+//  * CTA-pair MMA (PAIR = true): a K chunk is 64 columns of this CTA's 64 keys of the tile (8 KB), a
+//    V chunk 32 keys by 128 value columns (2 atoms, 8 KB), the lower part (value columns 128h..) and
+//    then the upper part (256 + 128h..) of CTA h; 12 ring slots.
+template <bool PAIR>
+struct WCfg {
+    static constexpr int kKRows = PAIR ? 64 : 128;          // keys of one K chunk held by this CTA
+    static constexpr int kVAtoms = PAIR ? 2 : 4;            // 64-column atoms of a V chunk
+    static constexpr int kVChunks = PAIR ? 8 : 4;           // V chunks per tile
+    static constexpr int kChunkBytes = PAIR ? 8192 : 16384;
+    static constexpr int kSlots = PAIR ? 12 : 6;
+    static constexpr int kPeriod = kWKChunks + kVChunks;    // chunks per tile
+    static constexpr int kSmem = kWOffRing + kSlots * kChunkBytes + 1024;
+    static_assert(kKRows * 128 == kChunkBytes && kVAtoms * kWVKeys * 128 == kChunkBytes, "chunk layouts");
+    static_assert(kSmem <= 227 * 1024, "shared memory");
+};
+// TMEM columns: S 0..127, P 128..191 (BF16 pairs of 128 keys; the pair variant uses 128..255, see the
+// kernel), O half 256..511.
 constexpr uint32_t kWColS = 0, kWColP = 128, kWColO = 256;
 
 // Position of chunk c of V(j) in an item's chunk sequence K(0); K(1), V(0); ...; K(T-1), V(T-2); V(T-1).
+template <bool PAIR>
 __device__ __forceinline__ uint32_t wv_chunk_pos(int j, int T, int c)
 {
-    return static_cast<uint32_t>(j < T - 1 ? 12 * j + 16 + c : 12 * j + 8 + c);
+    constexpr int P = WCfg<PAIR>::kPeriod;
+    return static_cast<uint32_t>(j < T - 1 ? P * j + 2 * kWKChunks + c : P * j + kWKChunks + c);
 }
 
 struct WideParams {
@@ -198,44 +217,74 @@ struct WRing {
     }
 };
 
+// PAIR = false: the two CTAs of a pair run independently (each loads every K chunk, each computes
+// the full S).  PAIR = true: the pair is a cluster of two CTAs and both products are pair MMAs
+// (tcgen05 cta_group::2, issued by the even CTA): CTA h loads only keys 64h..64h+63 of each K tile,
+// and the QK MMA (M = 256 with Q in both CTAs, N = the tile's 128 keys, half from each CTA's shared
+// memory) leaves the full S in both CTAs' Tensor Memory.  The PV MMA then has to produce different
+// value columns in the two CTAs from one shared B operand, so it runs over a doubled contraction:
+// CTA h's A operand is [P, 0] (h = 0) or [0, P] (h = 1), 256 BF16 columns of Tensor Memory, and B
+// stacks the lower and upper value halves, B[k][n] = V[k][n] for k < 128 and V[k - 128][256 + n]
+// above, its 256 columns split 128/128 between the CTAs.  D = P V[:, 256h : 256h + 256] in CTA h, the
+// same output split as the independent variant.  Half of the PV work multiplies zeros; in exchange
+// every K and V byte is read into shared memory once per pair.  Dense keys only (the ragged tail
+// clears V rows in the CTA's own ring, which needs the CTA's own copy-completion barrier).
+template <bool PAIR>
 __global__ void __launch_bounds__(kWThreads, 1)
     wide_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                 const __grid_constant__ CUtensorMap vmap, const __grid_constant__ WideParams p)
 {
+    using C = WCfg<PAIR>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    __shared__ uint64_t q_full, q_empty, c_full[kWSlots], c_empty[kWSlots];
+    __shared__ uint64_t q_full, q_empty, c_full[C::kSlots], c_empty[C::kSlots];
     __shared__ uint64_t s_full, s_empty, p_full, o_done, mma_done;
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
 
     const int warp = threadIdx.x / 32;
     if (blockIdx.x == 0 && threadIdx.x == 0 && p.nv_ts) *p.nv_ts = *p.nv_sg;   // single-pass NVFP4: report s_g
-    const int half = blockIdx.x & 1;
+    // this CTA's half of the value columns (PAIR: its rank in the cluster); the even CTA leads a pair
+    const int half = PAIR ? static_cast<int>(cluster_ctarank()) : static_cast<int>(blockIdx.x & 1);
+    const bool leader = !PAIR || half == 0;
     const WaitCtl wc{&abort_flag, p.status, p.limit};
     if (threadIdx.x == 0) {
         abort_flag = 0;
         mbar_init(&q_full, 1);
         mbar_init(&q_empty, 1);
-        for (int i = 0; i < kWSlots; ++i) {
+        for (int i = 0; i < C::kSlots; ++i) {
             mbar_init(&c_full[i], 1);
             mbar_init(&c_empty[i], 1);
         }
         mbar_init(&s_full, 1);
-        mbar_init(&s_empty, 128);
-        mbar_init(&p_full, 128);
+        mbar_init(&s_empty, PAIR ? 256 : 128);   // PAIR: the softmax threads of both CTAs arrive
+        mbar_init(&p_full, PAIR ? 256 : 128);
         mbar_init(&o_done, 1);
         mbar_init(&mma_done, 1);
         fence_barrier_init();
     }
     if (warp == 5) {
-        tmem_alloc(&tmem_slot, 512);
-        tmem_relinquish();
+        if constexpr (PAIR) {
+            tmem_alloc_pair(&tmem_slot, 512);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(&tmem_slot, 512);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
     __syncthreads();
+    if constexpr (PAIR) cluster_sync();   // both CTAs' barriers exist before either signals the other
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
+    // waits on barriers that the other CTA of a pair (or its commits) may complete
+    auto wait_x = [&](uint64_t* b, uint32_t parity) -> bool {
+        if constexpr (PAIR) return mbar_wait_cluster(b, parity, wc);
+        return mbar_wait(b, parity, wc);
+    };
+    // shared::cluster address of barrier b in the leading CTA / in the other CTA of the pair
+    auto lead_bar = [&](uint64_t* b) -> uint32_t { return mapa_shared(smem_u32(b), 0); };
+    auto other_bar = [&](uint64_t* b) -> uint32_t { return mapa_shared(smem_u32(b), static_cast<uint32_t>(half ^ 1)); };
     WSched sched;
     sched.init(&p, blockIdx.x >> 1, gridDim.x >> 1);
     WItem it;
@@ -246,29 +295,44 @@ __global__ void __launch_bounds__(kWThreads, 1)
             tma_prefetch_desc(&qmap);
             tma_prefetch_desc(&kmap);
             tma_prefetch_desc(&vmap);
-            WRing cr(kWSlots);
-            uint32_t qn = 0, ccnt[kWSlots] = {0, 0, 0, 0, 0, 0};
+            WRing cr(C::kSlots);
+            uint32_t qn = 0, ccnt[C::kSlots];
+            for (int i = 0; i < C::kSlots; ++i) ccnt[i] = 0;
+            // a copy into this CTA's shared memory, completing on the current slot's barrier; with PAIR
+            // the leader's barrier counts both CTAs' bytes
+            auto load = [&](uint8_t* dst, const CUtensorMap* m, uint64_t* bar, int x, int y, int z) {
+                if constexpr (PAIR) {
+                    if (!leader) {
+                        tma_load_3d_pair(dst, m, lead_bar(bar), x, y, z);
+                        return;
+                    }
+                }
+                tma_load_3d(dst, m, bar, x, y, z);
+            };
+            // wait until this CTA's copy of the slot is free (the leader's MMA thread releases both)
+            auto begin_chunk = [&]() -> bool {
+                wait_x(&c_empty[cr.idx], cr.phase ^ 1);
+                if (aborted(wc)) return false;
+                if (leader) mbar_arrive_expect_tx(&c_full[cr.idx], PAIR ? 2 * C::kChunkBytes : C::kChunkBytes);
+                ++ccnt[cr.idx];
+                return true;
+            };
             auto load_k = [&](int hu, int t) {
                 for (int a = 0; a < kWKChunks; ++a) {
-                    mbar_wait(&c_empty[cr.idx], cr.phase ^ 1, wc);
-                    if (!aborted(wc)) {
-                        mbar_arrive_expect_tx(&c_full[cr.idx], kWChunkBytes);
-                        tma_load_3d(smem + kWOffRing + cr.idx * kWChunkBytes, &kmap, &c_full[cr.idx], a * 64, t * kWKeys, hu);
-                        ++ccnt[cr.idx];
-                    }
+                    if (begin_chunk())
+                        load(smem + kWOffRing + cr.idx * C::kChunkBytes, &kmap, &c_full[cr.idx], a * 64,
+                             t * kWKeys + (PAIR ? 64 * half : 0), hu);
                     cr.advance();
                 }
             };
             auto load_v = [&](int hu, int t) {
-                for (int c = 0; c < kWVChunks; ++c) {
-                    mbar_wait(&c_empty[cr.idx], cr.phase ^ 1, wc);
-                    if (!aborted(wc)) {
-                        uint8_t* dst = smem + kWOffRing + cr.idx * kWChunkBytes;
-                        mbar_arrive_expect_tx(&c_full[cr.idx], kWChunkBytes);
-                        for (int a = 0; a < 4; ++a)
-                            tma_load_3d(dst + a * (kWVKeys * 128), &vmap, &c_full[cr.idx], half * kWHalf + a * 64,
-                                        t * kWKeys + c * kWVKeys, hu);
-                        ++ccnt[cr.idx];
+                for (int c = 0; c < C::kVChunks; ++c) {
+                    if (begin_chunk()) {
+                        uint8_t* dst = smem + kWOffRing + cr.idx * C::kChunkBytes;
+                        const int part = PAIR ? c / 4 : 0, cc = PAIR ? c % 4 : c;
+                        const int x0 = PAIR ? part * 256 + half * 128 : half * kWHalf;
+                        for (int a = 0; a < C::kVAtoms; ++a)
+                            load(dst + a * (kWVKeys * 128), &vmap, &c_full[cr.idx], x0 + a * 64, t * kWKeys + cc * kWVKeys, hu);
                     }
                     cr.advance();
                 }
@@ -276,11 +340,10 @@ __global__ void __launch_bounds__(kWThreads, 1)
             while (sched.next(it)) {
                 const int hu = wunit_head(p, it.u);
                 const int rt = it.u % p.row_tiles;
-                mbar_wait(&q_empty, (qn & 1) ^ 1, wc);
+                wait_x(&q_empty, (qn & 1) ^ 1);
                 if (!aborted(wc)) {
-                    mbar_arrive_expect_tx(&q_full, kWQBytes);
-                    for (int a = 0; a < 8; ++a)
-                        tma_load_3d(smem + kWOffQ + a * (kWRows * 128), &qmap, &q_full, a * 64, rt * kWRows, hu);
+                    if (leader) mbar_arrive_expect_tx(&q_full, PAIR ? 2 * kWQBytes : kWQBytes);
+                    for (int a = 0; a < 8; ++a) load(smem + kWOffQ + a * (kWRows * 128), &qmap, &q_full, a * 64, rt * kWRows, hu);
                 }
                 ++qn;
                 if (it.t1 <= it.t0) continue;
@@ -291,57 +354,85 @@ __global__ void __launch_bounds__(kWThreads, 1)
                 }
                 load_v(hu, it.t1 - 1);
             }
-            for (int i = 0; i < kWSlots; ++i)
-                if (ccnt[i]) wdrain(&c_full[i], (ccnt[i] - 1) & 1, kDrainLimit);
-            if (qn) wdrain(&q_full, (qn - 1) & 1, kDrainLimit);
+            // nothing may still be landing in shared memory when the CTA exits: the leader's barriers
+            // count every copy of the pair; the other CTA waits for the release of its last chunks
+            if (leader) {
+                for (int i = 0; i < C::kSlots; ++i)
+                    if (ccnt[i]) wdrain(&c_full[i], (ccnt[i] - 1) & 1, kDrainLimit);
+                if (qn) wdrain(&q_full, (qn - 1) & 1, kDrainLimit);
+            } else {
+                for (int i = 0; i < C::kSlots; ++i)
+                    if (ccnt[i]) wdrain(&c_empty[i], (ccnt[i] - 1) & 1, kDrainLimit);
+                if (qn) wdrain(&q_empty, (qn - 1) & 1, kDrainLimit);
+            }
         }
     } else if (warp == 5) {
-        // ------------------------------------------------ MMA issuer, in the chunk order
-        if (lane_id() == 0) {
-            constexpr uint32_t idesc_qk = idesc_bf16_f32(kWRows, kWKeys, false, false);
-            constexpr uint32_t idesc_pv = idesc_bf16_f32(kWRows, kWHalf, false, true);
-            WRing cr(kWSlots);
+        // ------------------------------------------------ MMA issuer (PAIR: the leading CTA only), in the chunk order
+        if (leader && lane_id() == 0) {
+            constexpr uint32_t idesc_qk = idesc_bf16_f32(PAIR ? 256 : kWRows, kWKeys, false, false);
+            constexpr uint32_t idesc_pv = idesc_bf16_f32(PAIR ? 256 : kWRows, kWHalf, false, true);
+            // a barrier of this CTA that the other CTA of a pair has a copy of: signal both
+            auto commit_both = [&](uint64_t* b) {
+                if constexpr (PAIR) {
+                    mma_commit_pair(smem_u32(b));
+                    mma_commit_pair(other_bar(b));
+                } else {
+                    mma_commit(b);
+                }
+            };
+            WRing cr(C::kSlots);
             uint32_t qn = 0, ns = 0, np = 0;   // items, QKs and PVs so far (kernel life)
             const uint32_t sQ = smem_u32(smem + kWOffQ);
             const uint64_t dq0 = sdesc_sw128(sQ, 16, 1024);
             auto issue_qk = [&]() {
-                if (ns > 0) mbar_wait(&s_empty, (ns - 1) & 1, wc);   // the softmax has read S
+                if (ns > 0) wait_x(&s_empty, (ns - 1) & 1);   // the softmax has read S
                 for (int a = 0; a < kWKChunks; ++a) {
-                    mbar_wait(&c_full[cr.idx], cr.phase, wc);
+                    wait_x(&c_full[cr.idx], cr.phase);
                     if (aborted(wc)) return;
                     tc_fence_after();
-                    const uint64_t dk = sdesc_sw128(smem_u32(smem + kWOffRing + cr.idx * kWChunkBytes), 16, 1024);
+                    const uint64_t dk = sdesc_sw128(smem_u32(smem + kWOffRing + cr.idx * C::kChunkBytes), 16, 1024);
                     const uint64_t dq = dq0 + ((a * (kWRows * 128)) >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_ss(tmem + kWColS, dq + ((kk * 32) >> 4), dk + ((kk * 32) >> 4), idesc_qk, (a > 0 || kk > 0) ? 1u : 0u);
-                    mma_commit(&c_empty[cr.idx]);
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint32_t acc = (a > 0 || kk > 0) ? 1u : 0u;
+                        if constexpr (PAIR)
+                            mma_ss_pair(tmem + kWColS, dq + ((kk * 32) >> 4), dk + ((kk * 32) >> 4), idesc_qk, acc);
+                        else
+                            mma_ss(tmem + kWColS, dq + ((kk * 32) >> 4), dk + ((kk * 32) >> 4), idesc_qk, acc);
+                    }
+                    commit_both(&c_empty[cr.idx]);
                     cr.advance();
                 }
-                mma_commit(&s_full);
+                commit_both(&s_full);
                 ++ns;
             };
             auto issue_pv = [&](bool first) {
-                mbar_wait(&p_full, np & 1, wc);
-                for (int c = 0; c < kWVChunks; ++c) {
-                    mbar_wait(&c_full[cr.idx], cr.phase, wc);
+                wait_x(&p_full, np & 1);
+                for (int c = 0; c < C::kVChunks; ++c) {
+                    wait_x(&c_full[cr.idx], cr.phase);
                     if (aborted(wc)) return;
                     tc_fence_after();
-                    const uint32_t sV = smem_u32(smem + kWOffRing + cr.idx * kWChunkBytes);
+                    const uint32_t sV = smem_u32(smem + kWOffRing + cr.idx * C::kChunkBytes);
 #pragma unroll
                     for (int kq = 0; kq < kWVKeys / 16; ++kq) {
                         const uint64_t db = sdesc_sw128(sV + kq * 2048, kWVKeys * 128, 1024);
-                        mma_ts(tmem + kWColO, tmem + kWColP + (c * (kWVKeys / 16) + kq) * 8, db, idesc_pv,
-                               (!first || c > 0 || kq > 0) ? 1u : 0u);
+                        const uint32_t acc = (!first || c > 0 || kq > 0) ? 1u : 0u;
+                        if constexpr (PAIR) {
+                            // contraction index: key 32 (c % 4) + 16 kq of the lower (c < 4) or upper half
+                            const uint32_t a_col = kWColP + (c / 4) * 64 + (c % 4) * 16 + kq * 8;
+                            mma_ts_pair(tmem + kWColO, tmem + a_col, db, idesc_pv, acc);
+                        } else {
+                            mma_ts(tmem + kWColO, tmem + kWColP + (c * (kWVKeys / 16) + kq) * 8, db, idesc_pv, acc);
+                        }
                     }
-                    mma_commit(&c_empty[cr.idx]);
+                    commit_both(&c_empty[cr.idx]);
                     cr.advance();
                 }
-                mma_commit(&o_done);
+                commit_both(&o_done);
                 ++np;
             };
             while (sched.next(it)) {
-                mbar_wait(&q_full, qn & 1, wc);
+                wait_x(&q_full, qn & 1);
                 ++qn;
                 tc_fence_after();
                 const int T = it.t1 - it.t0;
@@ -353,15 +444,39 @@ __global__ void __launch_bounds__(kWThreads, 1)
                     }
                     if (!aborted(wc)) issue_pv(T == 1);
                 }
-                if (!aborted(wc)) mma_commit(&q_empty);
+                if (!aborted(wc)) commit_both(&q_empty);
             }
-            mma_commit(&mma_done);
+            if constexpr (PAIR)
+                mma_commit_pair(smem_u32(&mma_done));
+            else
+                mma_commit(&mma_done);
             wdrain(&mma_done, 0, kDrainLimit);
         }
     } else if (warp < 4) {
         // ------------------------------------------------ softmax / epilogue, one query row per thread
         const int row_in_tile = warp * 32 + static_cast<int>(lane_id());
         const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+        // P columns of this CTA; with PAIR the other CTA's 64 columns of the doubled contraction stay zero
+        const uint32_t col_p = kWColP + (PAIR ? 64u * static_cast<uint32_t>(half) : 0u);
+        if constexpr (PAIR) {
+            uint32_t z[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) z[i] = 0u;
+            const uint32_t col_z = kWColP + 64u * static_cast<uint32_t>(half ^ 1);
+            tmem_st32(tmem + lane_base + col_z, z);
+            tmem_st32(tmem + lane_base + col_z + 32, z);
+            tmem_st_wait();
+        }
+        // arrive on a barrier of the leading CTA
+        auto arrive_lead = [&](uint64_t* b) {
+            if constexpr (PAIR) {
+                if (!leader) {
+                    mbar_arrive_cluster(lead_bar(b));
+                    return;
+                }
+            }
+            mbar_arrive(b);
+        };
         uint32_t g = 0;       // tiles (= S reads = PVs) so far, kernel life
         uint32_t gchunk = 0;  // chunk sequence position of the current item's first chunk
         while (sched.next(it)) {
@@ -372,7 +487,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
             const int lim = p.causal ? min(it.n, (row < p.R ? row : 0) % p.Sq + it.n - p.Sq + 1) : it.n;
             float m_run = -INFINITY, l = 0.f;
             for (int t = it.t0; t < it.t1; ++t, ++g) {
-                mbar_wait(&s_full, g & 1, wc);
+                wait_x(&s_full, g & 1);
                 tc_fence_after();
                 float s[kWKeys];
                 uint32_t* su = reinterpret_cast<uint32_t*>(s);
@@ -380,7 +495,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
                 for (int c4 = 0; c4 < kWKeys / 32; ++c4) tmem_ld32p(tmem + lane_base + kWColS + c4 * 32, su + c4 * 32);
                 tmem_ld_wait();
                 tc_fence_before();
-                mbar_arrive(&s_empty);
+                arrive_lead(&s_empty);
                 if ((t + 1) * kWKeys > lim) {
 #pragma unroll
                     for (int i = 0; i < kWKeys; ++i)
@@ -421,21 +536,21 @@ __global__ void __launch_bounds__(kWThreads, 1)
                 f32x2_split(fadd2(fadd2(ls[0], ls[1]), fadd2(ls[2], ls[3])), la, lb);
                 l = fmaf(l, alpha, la + lb);
                 // the previous PV must be done: the P buffer is reused and O must be stable
-                if (t > it.t0) mbar_wait(&o_done, (g - 1) & 1, wc);
+                if (t > it.t0) wait_x(&o_done, (g - 1) & 1);
                 tc_fence_after();
                 // ragged keys: V rows at or beyond n may hold NaN, and P = 0 does not cancel it
-                if (p.seqlens && (t + 1) * kWKeys > it.n) {
+                if (!PAIR && p.seqlens && (t + 1) * kWKeys > it.n) {
                     const int j = t - it.t0;
-                    for (int c = 0; c < kWVChunks; ++c) {
+                    for (int c = 0; c < C::kVChunks; ++c) {
                         const int r0 = it.n - (t * kWKeys + c * kWVKeys);   // first row to clear in this chunk
                         if (r0 >= kWVKeys) continue;
-                        const uint32_t pos = gchunk + wv_chunk_pos(j, T, c);
-                        const uint32_t slot = pos % kWSlots;
-                        mbar_wait(&c_full[slot], (pos / kWSlots) & 1, wc);
+                        const uint32_t pos = gchunk + wv_chunk_pos<PAIR>(j, T, c);
+                        const uint32_t slot = pos % C::kSlots;
+                        mbar_wait(&c_full[slot], (pos / C::kSlots) & 1, wc);
                         // 128 threads clear rows max(r0, 0) .. 31: row = thread / 4, one 64-column atom each
                         const int r = row_in_tile >> 2, a = row_in_tile & 3;
                         if (r >= (r0 > 0 ? r0 : 0)) {
-                            uint4* rowp = reinterpret_cast<uint4*>(smem + kWOffRing + slot * kWChunkBytes + a * (kWVKeys * 128) + r * 128);
+                            uint4* rowp = reinterpret_cast<uint4*>(smem + kWOffRing + slot * C::kChunkBytes + a * (kWVKeys * 128) + r * 128);
 #pragma unroll
                             for (int i = 0; i < 8; ++i) rowp[i] = make_uint4(0, 0, 0, 0);
                         }
@@ -453,16 +568,16 @@ __global__ void __launch_bounds__(kWThreads, 1)
                         tmem_st32(tmem + lane_base + kWColO + c4 * 32, o);
                     }
                 }
-                tmem_st32(tmem + lane_base + kWColP, pk);
-                tmem_st32(tmem + lane_base + kWColP + 32, pk + 32);
+                tmem_st32(tmem + lane_base + col_p, pk);
+                tmem_st32(tmem + lane_base + col_p + 32, pk + 32);
                 tmem_st_wait();
                 tc_fence_before();
-                mbar_arrive(&p_full);
+                arrive_lead(&p_full);
             }
-            gchunk += static_cast<uint32_t>(12 * T);
+            gchunk += static_cast<uint32_t>(C::kPeriod * T);
             // ---- epilogue
             if (T > 0) {
-                mbar_wait(&o_done, (g - 1) & 1, wc);
+                wait_x(&o_done, (g - 1) & 1);
                 tc_fence_after();
             }
             const bool store = row < p.R && !aborted(wc);
@@ -541,8 +656,14 @@ __global__ void __launch_bounds__(kWThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) tmem_dealloc(tmem, 512);
+    if constexpr (PAIR) {
+        cluster_sync();   // neither CTA frees Tensor Memory or exits while the other may still signal it
+        if (warp == 5) tmem_dealloc_pair(tmem, 512);
+    } else {
+        if (warp == 5) tmem_dealloc(tmem, 512);
+    }
 }
+
 
 // Exclusive prefix of per-unit 32-key tile counts (ragged keys), one block.
 __global__ void __launch_bounds__(1024) wide_prefix_kernel(const int32_t* seqlens, int Hkv, int row_tiles, int U,
@@ -724,6 +845,40 @@ size_t wide_workspace_bytes(const AttnArgs& a, int num_splits)
     return wide_ws_layout(a, nsm / 2, num_splits == 1).total;
 }
 
+namespace {
+
+constexpr int kMaxWideDevices = 64;
+std::atomic<int> g_pair_clusters[kMaxWideDevices];
+
+// How many CTA pairs (clusters of two, one CTA per SM) the device runs at once; cached per device.
+int pair_clusters(int nsm)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxWideDevices) return nsm / 2;
+    int n = g_pair_clusters[dev].load();
+    if (n > 0) return n;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(nsm & ~1), 1, 1);
+    cfg.blockDim = dim3(kWThreads, 1, 1);
+    cfg.dynamicSmemBytes = WCfg<true>::kSmem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, wide_kernel<true>, &cfg) != cudaSuccess || n <= 0) {
+        cudaGetLastError();
+        n = nsm / 2;
+    }
+    n = min(n, nsm / 2);
+    g_pair_clusters[dev].store(n);
+    return n;
+}
+
+}  // namespace
+
 int launch_wide(const AttnArgs& a, int num_splits, void* ws, size_t ws_bytes, cudaStream_t st)
 {
     const int nsm = num_sms();
@@ -736,8 +891,13 @@ int launch_wide(const AttnArgs& a, int num_splits, void* ws, size_t ws_bytes, cu
     const int R = Hq_per * a.Sq;
     const int row_tiles = (R + kWRows - 1) / kWRows;
     const int heads = a.B * a.Hkv;
+    // CTA-pair MMA variant: dense keys (the ragged tail's V rows are cleared by each CTA in its own
+    // ring), unless the caller asks for the independent CTAs
+    const bool pair = !a.seqlens && a.wide_variant != FMHA_WIDE_INDEPENDENT;
+    if (pair) FMHA_CHECK_CUDA(set_smem_limit_once(reinterpret_cast<const void*>(wide_kernel<true>), WCfg<true>::kSmem));
+    const int max_pairs = pair ? pair_clusters(nsm) : nsm / 2;
     // whole units: no more pairs than units (each pair takes units p, p + P, ...)
-    const int npairs = whole ? min(nsm / 2, heads * row_tiles) : nsm / 2;
+    const int npairs = whole ? min(max_pairs, heads * row_tiles) : max_pairs;
     CUtensorMap qmap, kmap, vmap;
     {
         const uint64_t dims[3] = {static_cast<uint64_t>(kWD), static_cast<uint64_t>(R), static_cast<uint64_t>(heads)};
@@ -749,7 +909,8 @@ int launch_wide(const AttnArgs& a, int num_splits, void* ws, size_t ws_bytes, cu
     {
         const uint64_t dims[3] = {static_cast<uint64_t>(kWD), static_cast<uint64_t>(a.Skv), static_cast<uint64_t>(heads)};
         const uint64_t strides[2] = {static_cast<uint64_t>(kWD) * 2, static_cast<uint64_t>(a.Skv) * kWD * 2};
-        const uint32_t kbox[3] = {64, static_cast<uint32_t>(kWKeys), 1};    // K chunk: 64 columns x 128 keys
+        // K chunk: 64 columns x the tile's 128 keys, or x this CTA's 64 keys of the tile (pair MMA)
+        const uint32_t kbox[3] = {64, static_cast<uint32_t>(pair ? WCfg<true>::kKRows : WCfg<false>::kKRows), 1};
         const uint32_t vbox[3] = {64, static_cast<uint32_t>(kWVKeys), 1};   // V chunk atom: 64 columns x 32 keys
         int rc = make_tmap_bf16(&kmap, a.k, 3, dims, strides, kbox);
         if (rc) return rc;
@@ -788,10 +949,29 @@ int launch_wide(const AttnArgs& a, int num_splits, void* ws, size_t ws_bytes, cu
         FMHA_CHECK_LAUNCH("wide_prefix_kernel");
         count_launch();
     }
-    FMHA_CHECK_CUDA(set_smem_limit_once(reinterpret_cast<const void*>(wide_kernel), kWSmem));
-    timing_mark_begin(st);
-    wide_kernel<<<2 * npairs, kWThreads, kWSmem, st>>>(qmap, kmap, vmap, p);
-    timing_mark_end(st);
+    if (pair) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(2 * npairs), 1, 1);
+        cfg.blockDim = dim3(kWThreads, 1, 1);
+        cfg.dynamicSmemBytes = WCfg<true>::kSmem;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        timing_mark_begin(st);
+        const cudaError_t e = cudaLaunchKernelEx(&cfg, wide_kernel<true>, qmap, kmap, vmap, p);
+        timing_mark_end(st);
+        if (e != cudaSuccess) return cuda_error(e, "wide_kernel<pair>");
+    } else {
+        FMHA_CHECK_CUDA(set_smem_limit_once(reinterpret_cast<const void*>(wide_kernel<false>), WCfg<false>::kSmem));
+        timing_mark_begin(st);
+        wide_kernel<false><<<2 * npairs, kWThreads, WCfg<false>::kSmem, st>>>(qmap, kmap, vmap, p);
+        timing_mark_end(st);
+    }
     FMHA_CHECK_LAUNCH("wide_kernel");
     count_launch();
     if (whole) return FMHA_OK;   // every unit was written by its pair

@@ -179,10 +179,11 @@ def ragged_nvfp4_small_workload():
 class Case:
     """Device inputs/outputs of one workload and the library call that processes them."""
 
-    def __init__(self, F, w, num_splits=0, pad_fill=None, causal=False):
+    def __init__(self, F, w, num_splits=0, pad_fill=None, causal=False, wide_variant=0):
         import torch
         self.F, self.w = F, w
         self.causal = causal
+        self.wv = wide_variant
         self.q, self.k, self.v, self.sl = w.make("cuda", pad_fill=pad_fill)
         B, Hq, Sq, D = self.q.shape
         self.n_out = B * Hq * Sq * D
@@ -196,10 +197,11 @@ class Case:
             dt = torch.bfloat16 if w.out_kind == "bf16" else torch.float32
             self.out = torch.empty(B, Hq, Sq, D, dtype=dt, device="cuda")
         self.lse = torch.empty(B, Hq, Sq, dtype=torch.float32, device="cuda")
-        opts = F.make_opts(kind, self.sl, num_splits, None, self.scales, self.ts, None, causal)
+        opts = F.make_opts(kind, self.sl, num_splits, None, self.scales, self.ts, None, causal, wide_variant=self.wv)
         wsb = F.fmha_workspace_size(B, Hq, w.Hkv, Sq, w.Skv, D, opts)
         self.ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device="cuda") if wsb else None
-        self.opts = F.make_opts(kind, self.sl, num_splits, self.ws, self.scales, self.ts, None, causal)
+        self.opts = F.make_opts(kind, self.sl, num_splits, self.ws, self.scales, self.ts, None, causal,
+                                wide_variant=self.wv)
         self.kind, self.num_splits = kind, num_splits
 
     def use_given_scale(self, sg: float):
@@ -208,11 +210,12 @@ class Case:
         F, w = self.F, self.w
         B, Hq, Sq, D = self.q.shape
         self.sg_in = torch.tensor([sg], dtype=torch.float32, device="cuda")
-        opts = F.make_opts(self.kind, self.sl, self.num_splits, None, self.scales, self.ts, None, self.causal, self.sg_in)
+        opts = F.make_opts(self.kind, self.sl, self.num_splits, None, self.scales, self.ts, None, self.causal, self.sg_in,
+                           wide_variant=self.wv)
         wsb = F.fmha_workspace_size(B, Hq, w.Hkv, Sq, w.Skv, D, opts)
         self.ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device="cuda") if wsb else None
         self.opts = F.make_opts(self.kind, self.sl, self.num_splits, self.ws, self.scales, self.ts, None, self.causal,
-                                self.sg_in)
+                                self.sg_in, wide_variant=self.wv)
 
     def call(self, q=None, k=None, v=None):
         self.F.fmha_fwd_ex(self.q if q is None else q, self.k if k is None else k, self.v if v is None else v,
@@ -416,12 +419,13 @@ def l2_note(in_bytes: int) -> str:
     return f"inputs fit in L2 ({in_bytes / 2**10:.0f} KiB, L2 {l2 / 2**20:.1f} MiB): latency figure, no roofline claim"
 
 
-def _workload_entry(F, w, idx, steps, warmup, peaks, causal=False, given_scale=False, read_peak=None, cpu=False):
+def _workload_entry(F, w, idx, steps, warmup, peaks, causal=False, given_scale=False, read_peak=None, cpu=False,
+                    wide_variant=0):
     """Timing + roofline of one extra workload (rank 0 only).  given_scale: NVFP4 in one pass with the
     per-tensor scale of an earlier (two-pass) call on the same inputs, as a caller reusing the
     previous step's scale would.  cpu: also time the oracle on a bounded sample of it."""
     import torch
-    case = Case(F, w, num_splits=0, causal=causal)
+    case = Case(F, w, num_splits=0, causal=causal, wide_variant=wide_variant)
     if given_scale:
         case.call()
         torch.cuda.synchronize()
@@ -447,7 +451,7 @@ def _workload_entry(F, w, idx, steps, warmup, peaks, causal=False, given_scale=F
         gbs = w.kv_bytes() / (step_ms / 1e3) / 1e9
         ach = case.algorithmic_bytes() / (kern_ms / 1e3) / 1e9
         if w.D == 512:
-            traffic = traffic_for("wide_kernel", "wide.cu")
+            traffic = traffic_for("wide_kernel<pair>" if wide_variant != 1 else "wide_kernel<independent>", "wide.cu")
         elif w.ragged and not causal:
             traffic = traffic_for("decode_kernel<128>/ragged", "decode.cu")
         else:
@@ -473,7 +477,8 @@ def _summary(head: dict, extra: dict) -> dict:
     out = {"c2": {"value": r4(head["value"]), "unit": "GB/s", "ms": r4(head["ms_per_step"]),
                   "kernel_frac": r4(head["roofline"]["frac"]),
                   "cpu": r4(head["cpu"]["value"]) if head.get("cpu") else None}}
-    for key in ("c1", "c3", "c4", "c5", "c5_given_scale", "c2_spec_causal", "c3_d128", "c3_causal", "c3_chunked_varlen"):
+    for key in ("c1", "c3", "c4", "c5", "c4_independent", "c5_given_scale", "c2_spec_causal", "c3_d128", "c3_causal",
+                "c3_chunked_varlen"):
         e = extra.get(key)
         if not e or "value" not in e:
             continue
@@ -540,6 +545,12 @@ def run_ours(args, rank, world, local):
             extra["c5_given_scale"]["workload"] = wl[4].name.replace("(NVFP4 out)", "(NVFP4 out, one pass with a given scale)")
         except F.FmhaError as ex:
             extra["c5_given_scale"] = {"workload": "ragged NVFP4, given scale", "unsupported": str(ex)}
+        try:   # the wide-head workload on the kernel whose two CTAs of a pair run independently
+            extra["c4_independent"] = _workload_entry(F, wl[3], 3, min(args.steps, 10), args.warmup, peaks,
+                                                      read_peak=read_peak, wide_variant=F.FMHA_WIDE_INDEPENDENT)
+            extra["c4_independent"]["workload"] = wl[3].name.replace("(BF16 out)", "(BF16 out, independent CTAs)")
+        except F.FmhaError as ex:
+            extra["c4_independent"] = {"workload": "wide-head, independent CTAs", "unsupported": str(ex)}
         try:   # decode with several new tokens per head (speculative or chunked decode), causal mask
             extra["c2_spec_causal"] = _workload_entry(F, spec_decode_workload(), 1, min(args.steps, 10), args.warmup, peaks, causal=True, read_peak=read_peak)
         except F.FmhaError as ex:
@@ -628,7 +639,7 @@ def main():
     ap.add_argument("--only-headline", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle's CPU baselines")
     ap.add_argument("--profile", choices=["c1", "c2", "c3", "c4", "c5", "c3_causal", "c3_d128", "c5_given_scale", "c2_spec_causal",
-                                          "c5_small"], default=None,
+                                          "c5_small", "c4_independent"], default=None,
                     help="run one workload's call --repeat times, untimed (for a profiler)")
     ap.add_argument("--repeat", type=int, default=5)
     args = ap.parse_args()
@@ -646,7 +657,8 @@ def main():
             w = ragged_nvfp4_small_workload()
         else:
             w = inputs.workloads()[int(args.profile[1]) - 1]
-        case = Case(F, w, num_splits=0, causal=args.profile in ("c3_causal", "c2_spec_causal"))
+        case = Case(F, w, num_splits=0, causal=args.profile in ("c3_causal", "c2_spec_causal"),
+                    wide_variant=F.FMHA_WIDE_INDEPENDENT if args.profile == "c4_independent" else F.FMHA_WIDE_AUTO)
         if args.profile == "c5_given_scale":   # one two-pass call gives the scale the rest reuse
             case.call()
             torch.cuda.synchronize()

@@ -88,7 +88,17 @@ typedef struct {
                                  of this O (two passes) */
     float* out_amax;          /* optional, NVFP4 only: device float[1], receives max|O| (FP32) of
                                  this call (with two passes it is also the max the quantiser uses) */
+    int wide_variant;         /* D = 512 kernel (fmha_wide_variant); results agree within rounding */
 } fmha_opts;
+
+/* Kernel variants for D = 512 (the value columns are split over a pair of CTAs either way). */
+typedef enum {
+    FMHA_WIDE_AUTO = 0,        /* FMHA_WIDE_PAIR for dense keys, FMHA_WIDE_INDEPENDENT with seqlens_k */
+    FMHA_WIDE_INDEPENDENT = 1, /* two independent CTAs: each loads every K tile, computes the full S */
+    FMHA_WIDE_PAIR = 2         /* a cluster of two CTAs running pair MMAs (tcgen05 cta_group::2): each
+                                  CTA loads half of every K tile; dense keys only (with seqlens_k the
+                                  independent CTAs run) */
+} fmha_wide_variant;
 
 /*
  * Attention forward with default options (BF16 output, dense keys, no workspace, no split).

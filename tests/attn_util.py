@@ -17,16 +17,16 @@ LSE_REL = 1e-3
 
 
 def run_attention(F, q, k, v, scale, out_kind="bf16", seqlens=None, num_splits=None, want_f32=False, causal=False,
-                  nvfp4_scale=None, want_amax=False):
+                  nvfp4_scale=None, want_amax=False, wide_variant=None):
     """Calls fmha_fwd (no options) or fmha_fwd_ex; returns dict of host numpy results.
 
     nvfp4_scale: a given per-tensor scale s_g (single-pass NVFP4); want_amax: also return max|O|
-    through opts.out_amax."""
+    through opts.out_amax; wide_variant: opts.wide_variant for D = 512 (None: automatic)."""
     B, Hq, Sq, D = q.shape
     Hkv, Skv = k.shape[1], k.shape[2]
     lse = torch.full((B, Hq, Sq), float("nan"), dtype=torch.float32, device="cuda")
     res = {}
-    if out_kind == "bf16" and seqlens is None and num_splits is None and not causal:
+    if out_kind == "bf16" and seqlens is None and num_splits is None and not causal and wide_variant is None:
         out = torch.full((B, Hq, Sq, D), float("nan"), dtype=torch.bfloat16, device="cuda")
         F.fmha_fwd(q, k, v, out, lse, scale)
         torch.cuda.synchronize()
@@ -47,10 +47,11 @@ def run_attention(F, q, k, v, scale, out_kind="bf16", seqlens=None, num_splits=N
             out = torch.full((B, Hq, Sq, D), float("nan"), dtype=dt, device="cuda")
             scales = ts = f32 = None
         ns = 0 if num_splits is None else num_splits
-        opts = F.make_opts(kind, seqlens, ns, None, scales, ts, f32, causal, sg_in, amax)
+        wv = F.FMHA_WIDE_AUTO if wide_variant is None else wide_variant
+        opts = F.make_opts(kind, seqlens, ns, None, scales, ts, f32, causal, sg_in, amax, wv)
         wsb = F.fmha_workspace_size(B, Hq, Hkv, Sq, Skv, D, opts)
         ws = torch.empty(max(wsb, 1), dtype=torch.uint8, device="cuda") if wsb else None
-        opts = F.make_opts(kind, seqlens, ns, ws, scales, ts, f32, causal, sg_in, amax)
+        opts = F.make_opts(kind, seqlens, ns, ws, scales, ts, f32, causal, sg_in, amax, wv)
         res["workspace_bytes"] = wsb
         F.fmha_fwd_ex(q, k, v, out, lse, scale, opts)
         torch.cuda.synchronize()
