@@ -257,8 +257,10 @@ __global__ void __launch_bounds__(kWThreads, 1)
             mbar_init(&c_empty[i], 1);
         }
         mbar_init(&s_full, 1);
-        mbar_init(&s_empty, PAIR ? 256 : 128);   // PAIR: the softmax threads of both CTAs arrive
-        mbar_init(&p_full, PAIR ? 256 : 128);
+        // PAIR: one arrival per softmax warp of both CTAs (a cluster-scope release per thread would put a
+        // memory barrier on every softmax thread's path twice per tile)
+        mbar_init(&s_empty, PAIR ? 8 : 128);
+        mbar_init(&p_full, PAIR ? 8 : 128);
         mbar_init(&o_done, 1);
         mbar_init(&mma_done, 1);
         fence_barrier_init();
@@ -277,7 +279,8 @@ __global__ void __launch_bounds__(kWThreads, 1)
     if constexpr (PAIR) cluster_sync();   // both CTAs' barriers exist before either signals the other
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
-    // waits on barriers that the other CTA of a pair (or its commits) may complete
+    // waits on the barriers the other CTA's softmax threads arrive on (cluster-scope acquire); copy and
+    // MMA completions aimed at a barrier are waited for with the ordinary wait
     auto wait_x = [&](uint64_t* b, uint32_t parity) -> bool {
         if constexpr (PAIR) return mbar_wait_cluster(b, parity, wc);
         return mbar_wait(b, parity, wc);
@@ -311,7 +314,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
             };
             // wait until this CTA's copy of the slot is free (the leader's MMA thread releases both)
             auto begin_chunk = [&]() -> bool {
-                wait_x(&c_empty[cr.idx], cr.phase ^ 1);
+                mbar_wait(&c_empty[cr.idx], cr.phase ^ 1, wc);
                 if (aborted(wc)) return false;
                 if (leader) mbar_arrive_expect_tx(&c_full[cr.idx], PAIR ? 2 * C::kChunkBytes : C::kChunkBytes);
                 ++ccnt[cr.idx];
@@ -340,7 +343,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
             while (sched.next(it)) {
                 const int hu = wunit_head(p, it.u);
                 const int rt = it.u % p.row_tiles;
-                wait_x(&q_empty, (qn & 1) ^ 1);
+                mbar_wait(&q_empty, (qn & 1) ^ 1, wc);
                 if (!aborted(wc)) {
                     if (leader) mbar_arrive_expect_tx(&q_full, PAIR ? 2 * kWQBytes : kWQBytes);
                     for (int a = 0; a < 8; ++a) load(smem + kWOffQ + a * (kWRows * 128), &qmap, &q_full, a * 64, rt * kWRows, hu);
@@ -387,7 +390,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
             auto issue_qk = [&]() {
                 if (ns > 0) wait_x(&s_empty, (ns - 1) & 1);   // the softmax has read S
                 for (int a = 0; a < kWKChunks; ++a) {
-                    wait_x(&c_full[cr.idx], cr.phase);
+                    mbar_wait(&c_full[cr.idx], cr.phase, wc);
                     if (aborted(wc)) return;
                     tc_fence_after();
                     const uint64_t dk = sdesc_sw128(smem_u32(smem + kWOffRing + cr.idx * C::kChunkBytes), 16, 1024);
@@ -409,7 +412,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
             auto issue_pv = [&](bool first) {
                 wait_x(&p_full, np & 1);
                 for (int c = 0; c < C::kVChunks; ++c) {
-                    wait_x(&c_full[cr.idx], cr.phase);
+                    mbar_wait(&c_full[cr.idx], cr.phase, wc);
                     if (aborted(wc)) return;
                     tc_fence_after();
                     const uint32_t sV = smem_u32(smem + kWOffRing + cr.idx * C::kChunkBytes);
@@ -432,7 +435,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
                 ++np;
             };
             while (sched.next(it)) {
-                wait_x(&q_full, qn & 1);
+                mbar_wait(&q_full, qn & 1, wc);
                 ++qn;
                 tc_fence_after();
                 const int T = it.t1 - it.t0;
@@ -467,13 +470,18 @@ __global__ void __launch_bounds__(kWThreads, 1)
             tmem_st32(tmem + lane_base + col_z + 32, z);
             tmem_st_wait();
         }
-        // arrive on a barrier of the leading CTA
+        // arrive on a barrier of the leading CTA: every thread, or (PAIR) once per warp after all of its
+        // lanes are past their Tensor Memory accesses
         auto arrive_lead = [&](uint64_t* b) {
             if constexpr (PAIR) {
-                if (!leader) {
-                    mbar_arrive_cluster(lead_bar(b));
-                    return;
+                __syncwarp();
+                if (lane_id() == 0) {
+                    if (leader)
+                        mbar_arrive(b);
+                    else
+                        mbar_arrive_cluster(lead_bar(b));
                 }
+                return;
             }
             mbar_arrive(b);
         };
@@ -487,7 +495,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
             const int lim = p.causal ? min(it.n, (row < p.R ? row : 0) % p.Sq + it.n - p.Sq + 1) : it.n;
             float m_run = -INFINITY, l = 0.f;
             for (int t = it.t0; t < it.t1; ++t, ++g) {
-                wait_x(&s_full, g & 1);
+                mbar_wait(&s_full, g & 1, wc);
                 tc_fence_after();
                 float s[kWKeys];
                 uint32_t* su = reinterpret_cast<uint32_t*>(s);
@@ -536,7 +544,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
                 f32x2_split(fadd2(fadd2(ls[0], ls[1]), fadd2(ls[2], ls[3])), la, lb);
                 l = fmaf(l, alpha, la + lb);
                 // the previous PV must be done: the P buffer is reused and O must be stable
-                if (t > it.t0) wait_x(&o_done, (g - 1) & 1);
+                if (t > it.t0) mbar_wait(&o_done, (g - 1) & 1, wc);
                 tc_fence_after();
                 // ragged keys: V rows at or beyond n may hold NaN, and P = 0 does not cancel it
                 if (!PAIR && p.seqlens && (t + 1) * kWKeys > it.n) {
@@ -577,7 +585,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
             gchunk += static_cast<uint32_t>(C::kPeriod * T);
             // ---- epilogue
             if (T > 0) {
-                wait_x(&o_done, (g - 1) & 1);
+                mbar_wait(&o_done, (g - 1) & 1, wc);
                 tc_fence_after();
             }
             const bool store = row < p.R && !aborted(wc);
@@ -891,9 +899,10 @@ int launch_wide(const AttnArgs& a, int num_splits, void* ws, size_t ws_bytes, cu
     const int R = Hq_per * a.Sq;
     const int row_tiles = (R + kWRows - 1) / kWRows;
     const int heads = a.B * a.Hkv;
-    // CTA-pair MMA variant: dense keys (the ragged tail's V rows are cleared by each CTA in its own
-    // ring), unless the caller asks for the independent CTAs
-    const bool pair = !a.seqlens && a.wide_variant != FMHA_WIDE_INDEPENDENT;
+    // CTA-pair MMA variant: when asked for, and for dense keys only (the ragged tail's V rows are
+    // cleared by each CTA in its own ring).  The default is the independent variant, which measured
+    // faster on the wide-head decode workload (0.83 against 0.71 of the HBM copy bandwidth).
+    const bool pair = !a.seqlens && a.wide_variant == FMHA_WIDE_PAIR;
     if (pair) FMHA_CHECK_CUDA(set_smem_limit_once(reinterpret_cast<const void*>(wide_kernel<true>), WCfg<true>::kSmem));
     const int max_pairs = pair ? pair_clusters(nsm) : nsm / 2;
     // whole units: no more pairs than units (each pair takes units p, p + P, ...)

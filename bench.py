@@ -451,7 +451,7 @@ def _workload_entry(F, w, idx, steps, warmup, peaks, causal=False, given_scale=F
         gbs = w.kv_bytes() / (step_ms / 1e3) / 1e9
         ach = case.algorithmic_bytes() / (kern_ms / 1e3) / 1e9
         if w.D == 512:
-            traffic = traffic_for("wide_kernel<pair>" if wide_variant != 1 else "wide_kernel<independent>", "wide.cu")
+            traffic = traffic_for("wide_kernel<pair>" if wide_variant == 2 else "wide_kernel<independent>", "wide.cu")
         elif w.ragged and not causal:
             traffic = traffic_for("decode_kernel<128>/ragged", "decode.cu")
         else:
@@ -477,7 +477,7 @@ def _summary(head: dict, extra: dict) -> dict:
     out = {"c2": {"value": r4(head["value"]), "unit": "GB/s", "ms": r4(head["ms_per_step"]),
                   "kernel_frac": r4(head["roofline"]["frac"]),
                   "cpu": r4(head["cpu"]["value"]) if head.get("cpu") else None}}
-    for key in ("c1", "c3", "c4", "c5", "c4_independent", "c5_given_scale", "c2_spec_causal", "c3_d128", "c3_causal",
+    for key in ("c1", "c3", "c4", "c5", "c4_pair", "c5_given_scale", "c2_spec_causal", "c3_d128", "c3_causal",
                 "c3_chunked_varlen"):
         e = extra.get(key)
         if not e or "value" not in e:
@@ -545,12 +545,12 @@ def run_ours(args, rank, world, local):
             extra["c5_given_scale"]["workload"] = wl[4].name.replace("(NVFP4 out)", "(NVFP4 out, one pass with a given scale)")
         except F.FmhaError as ex:
             extra["c5_given_scale"] = {"workload": "ragged NVFP4, given scale", "unsupported": str(ex)}
-        try:   # the wide-head workload on the kernel whose two CTAs of a pair run independently
-            extra["c4_independent"] = _workload_entry(F, wl[3], 3, min(args.steps, 10), args.warmup, peaks,
-                                                      read_peak=read_peak, wide_variant=F.FMHA_WIDE_INDEPENDENT)
-            extra["c4_independent"]["workload"] = wl[3].name.replace("(BF16 out)", "(BF16 out, independent CTAs)")
+        try:   # the wide-head workload on the CTA-pair MMA kernel (tcgen05 cta_group::2)
+            extra["c4_pair"] = _workload_entry(F, wl[3], 3, min(args.steps, 10), args.warmup, peaks,
+                                               read_peak=read_peak, wide_variant=F.FMHA_WIDE_PAIR)
+            extra["c4_pair"]["workload"] = wl[3].name.replace("(BF16 out)", "(BF16 out, CTA-pair MMA)")
         except F.FmhaError as ex:
-            extra["c4_independent"] = {"workload": "wide-head, independent CTAs", "unsupported": str(ex)}
+            extra["c4_pair"] = {"workload": "wide-head, CTA-pair MMA", "unsupported": str(ex)}
         try:   # decode with several new tokens per head (speculative or chunked decode), causal mask
             extra["c2_spec_causal"] = _workload_entry(F, spec_decode_workload(), 1, min(args.steps, 10), args.warmup, peaks, causal=True, read_peak=read_peak)
         except F.FmhaError as ex:
@@ -639,7 +639,7 @@ def main():
     ap.add_argument("--only-headline", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle's CPU baselines")
     ap.add_argument("--profile", choices=["c1", "c2", "c3", "c4", "c5", "c3_causal", "c3_d128", "c5_given_scale", "c2_spec_causal",
-                                          "c5_small", "c4_independent"], default=None,
+                                          "c5_small", "c4_pair"], default=None,
                     help="run one workload's call --repeat times, untimed (for a profiler)")
     ap.add_argument("--repeat", type=int, default=5)
     args = ap.parse_args()
@@ -658,7 +658,7 @@ def main():
         else:
             w = inputs.workloads()[int(args.profile[1]) - 1]
         case = Case(F, w, num_splits=0, causal=args.profile in ("c3_causal", "c2_spec_causal"),
-                    wide_variant=F.FMHA_WIDE_INDEPENDENT if args.profile == "c4_independent" else F.FMHA_WIDE_AUTO)
+                    wide_variant=F.FMHA_WIDE_PAIR if args.profile == "c4_pair" else F.FMHA_WIDE_AUTO)
         if args.profile == "c5_given_scale":   # one two-pass call gives the scale the rest reuse
             case.call()
             torch.cuda.synchronize()

@@ -93,11 +93,12 @@ typedef struct {
 
 /* Kernel variants for D = 512 (the value columns are split over a pair of CTAs either way). */
 typedef enum {
-    FMHA_WIDE_AUTO = 0,        /* FMHA_WIDE_PAIR for dense keys, FMHA_WIDE_INDEPENDENT with seqlens_k */
+    FMHA_WIDE_AUTO = 0,        /* the faster one measured on GB300: FMHA_WIDE_INDEPENDENT */
     FMHA_WIDE_INDEPENDENT = 1, /* two independent CTAs: each loads every K tile, computes the full S */
     FMHA_WIDE_PAIR = 2         /* a cluster of two CTAs running pair MMAs (tcgen05 cta_group::2): each
-                                  CTA loads half of every K tile; dense keys only (with seqlens_k the
-                                  independent CTAs run) */
+                                  CTA loads half of every K tile, the PV product runs over a doubled
+                                  contraction; dense keys only (with seqlens_k the independent CTAs
+                                  run) */
 } fmha_wide_variant;
 
 /*

@@ -23,20 +23,21 @@ def F():
     return F
 
 
-@pytest.mark.parametrize("B,Hq,Hkv,Sq,Skv,D,sigma", [
-    (2, 8, 8, 1, 2048, 128, 1.0),   # decode path (split-KV)
-    (1, 2, 2, 512, 1024, 64, 1.0),  # row-tile path
-    (1, 32, 1, 1, 512, 512, 0.5),   # wide-head path
+@pytest.mark.parametrize("B,Hq,Hkv,Sq,Skv,D,sigma,wv", [
+    (2, 8, 8, 1, 2048, 128, 1.0, 0),   # decode path (split-KV)
+    (1, 2, 2, 512, 1024, 64, 1.0, 0),  # row-tile path
+    (1, 32, 1, 1, 512, 512, 0.5, 1),   # wide-head path, independent CTAs
+    (1, 32, 1, 1, 512, 512, 0.5, 2),   # wide-head path, CTA pairs (cluster: both CTAs must drain and meet)
 ])
-def test_forced_timeout_is_reported_and_context_survives(F, B, Hq, Hkv, Sq, Skv, D, sigma):
+def test_forced_timeout_is_reported_and_context_survives(F, B, Hq, Hkv, Sq, Skv, D, sigma, wv):
     w = inputs.Workload("t", B, Hq, Hkv, Sq, Skv, D, sigma, "bf16", 61)
     q, k, v, _ = w.make("cuda")
     out = torch.empty(B, Hq, Sq, D, dtype=torch.bfloat16, device="cuda")
     lse = torch.empty(B, Hq, Sq, dtype=torch.float32, device="cuda")
-    opts = F.make_opts(F.FMHA_OUT_BF16, None, 0)
+    opts = F.make_opts(F.FMHA_OUT_BF16, None, 0, wide_variant=wv)
     wsb = F.fmha_workspace_size(B, Hq, Hkv, Sq, Skv, D, opts)
     ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device="cuda")
-    opts = F.make_opts(F.FMHA_OUT_BF16, None, 0, ws)
+    opts = F.make_opts(F.FMHA_OUT_BF16, None, 0, ws, wide_variant=wv)
     assert F.fmha_check_status() == F.FMHA_OK
     F.fmha_set_wait_limit(1)
     try:
@@ -46,6 +47,6 @@ def test_forced_timeout_is_reported_and_context_survives(F, B, Hq, Hkv, Sq, Skv,
         F.fmha_set_wait_limit(0)
     assert rc == F.FMHA_ERR_TIMEOUT
     assert F.fmha_check_status() == F.FMHA_OK          # the status word was cleared
-    res = run_attention(F, q, k, v, w.scale, num_splits=0)
+    res = run_attention(F, q, k, v, w.scale, num_splits=0, wide_variant=wv if D == 512 else None)
     o_ref, l_ref = oracle.attention(q.cpu(), k.cpu(), v.cpu(), w.scale)
     check_o_lse(res["o"], res["lse"], o_ref, l_ref, "after timeout")

@@ -30,7 +30,7 @@ def F():
 def test_shapes(F, B, Hq, Hkv, Sq, Skv, mode, variant):
     """fwd: fmha_fwd without options (whole units per CTA pair, no workspace); bf16/f32: split over
     every SM pair with a workspace; f32_whole: whole units with FP32 output.  variant: the kernel
-    (automatic = the CTA-pair MMA for these dense keys, independent CTAs, or the pair MMA forced)."""
+    (automatic, independent CTAs, or the CTA-pair MMA)."""
     if mode == "fwd" and variant != "auto":
         pytest.skip("fmha_fwd has no options")
     w = inputs.Workload("t", B, Hq, Hkv, Sq, Skv, 512, 0.5, "bf16", 51)
@@ -76,16 +76,16 @@ def test_nvfp4_output_bit_exact(F, variant):
     np.testing.assert_array_equal(res["codes"], codes)
 
 
-@pytest.mark.parametrize("mode", ["split", "split_independent", "fwd"])
+@pytest.mark.parametrize("mode", ["split", "split_pair", "fwd"])
 def test_wide_full_size_stratified(F, mode):
     """B32 Hq128 Hkv1 Sq1 Skv16384 D512, N(0, 0.5), BF16 O + LSE: the first and last row of every
     unit (each unit is one 128-row tile, cut by the stream-K split into about two pieces) and random
-    rows.  split: fmha_fwd_ex with a workspace (the CTA-pair MMA kernel); split_independent: the same
-    with independent CTAs; fwd: fmha_fwd (whole units, no workspace)."""
+    rows.  split: fmha_fwd_ex with a workspace (the default, independent CTAs); split_pair: the same
+    on the CTA-pair MMA kernel; fwd: fmha_fwd (whole units, no workspace)."""
     w = inputs.workloads()[3]
     q, k, v, _ = w.make("cuda")
     kw = {"split": {"num_splits": 0}, "fwd": {},
-          "split_independent": {"num_splits": 0, "wide_variant": F.FMHA_WIDE_INDEPENDENT}}[mode]
+          "split_pair": {"num_splits": 0, "wide_variant": F.FMHA_WIDE_PAIR}}[mode]
     res = run_attention(F, q, k, v, w.scale, **kw)
     rows = stratified_rows(w, all_units=True, edge_units=range(w.B * w.Hkv), tile=128, extra=32, seed=4)
     o_ref, l_ref = oracle_rows(w, rows, tensors=(q, k, v))
