@@ -264,6 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ int ep_abort, fx_last;          // softmax warps: abort snapshot, "this CTA merges"
     __shared__ int fx_n;
     __shared__ int fx_slot[kMaxFixSlots];
+    __shared__ float fx_w[kN][4], fx_lse[kN];   // merge: per column, the partials' weights and the merged LSE
 
     const int warp = threadIdx.x / 32;
     if (blockIdx.x == 0 && threadIdx.x == 0 && p.nv_ts) *p.nv_ts = *p.nv_sg;   // single-pass NVFP4: report s_g
@@ -616,12 +617,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (p.fixup && !final_here) {
                 // stream-K fixup: publish this partial, count the unit's arrivals, and let the CTA
-                // that completes the unit merge it (O = sum exp(lse_i - lse) O_i, as the combine)
-                __threadfence();
+                // that completes the unit merge it (O = sum exp(lse_i - lse) O_i, as the combine).
+                // The CTA barrier orders every thread's partial stores before thread 0's device-scope
+                // fence, which releases them all (release is cumulative) ahead of its arrival: one
+                // fence waits for the stores instead of 128.
                 named_bar_sync(1, 128);
                 if (tid == 0) {
                     const int n = unit_partial_slots(p, it.u, static_cast<int>(gridDim.x), fx_slot, kMaxFixSlots);
                     fx_n = n;
+                    __threadfence();
                     const int arrived = n > 0 ? arrive_unit(p.unit_ctr + it.u, p.gen, n) : 0;
                     // -1: the counter kept changing under us (another call on this workspace):
                     // the unit may stay unmerged, so say so instead of failing silently
@@ -634,36 +638,41 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int ns = fx_n;
                     float amax_m = 0.f;
                     if (ns <= 4) {
-                        // the usual case: four columns at a time, every partial LSE and this thread's
-                        // element of every partial O for them loaded in one round (a column at a
-                        // time made one dependent L2 round trip per column)
-                        for (int q0 = 0; q0 < G; q0 += 4) {
-                            float lv[4][4], ov[4][4];
+                        // the usual case: this thread's element of every partial O of every column, and
+                        // (threads q < G) column q's partial LSEs, all in flight at once, so the merge
+                        // costs one L2 round trip whatever the number of columns (a round per few
+                        // columns was one dependent trip each, slow while the other CTAs stream)
+                        float ov[kN][4];
 #pragma unroll
-                            for (int c = 0; c < 4; ++c)
+                        for (int q = 0; q < kN; ++q)
 #pragma unroll
-                                for (int i = 0; i < 4; ++i) {
-                                    const bool use = q0 + c < G && i < ns;
-                                    const size_t sl = static_cast<size_t>(fx_slot[i < ns ? i : 0]) * kN + (use ? q0 + c : 0);
-                                    lv[c][i] = use ? __ldcg(p.part_lse + sl) : -INFINITY;
-                                    ov[c][i] = (use && tid < D) ? __ldcg(p.part_o + sl * D + tid) : 0.f;
-                                }
-#pragma unroll
-                            for (int c = 0; c < 4; ++c) {
-                                const int q = q0 + c;
-                                if (q >= G) break;
-                                const float mx = fmaxf(fmaxf(lv[c][0], lv[c][1]), fmaxf(lv[c][2], lv[c][3]));
-                                const bool any = mx > -INFINITY;
-                                float sum = 0.f;
-#pragma unroll
-                                for (int i = 0; i < 4; ++i) sum += (any && i < ns) ? __expf(lv[c][i] - mx) : 0.f;
-                                const float lse_all = any ? mx + __logf(sum) : -INFINITY;
-                                float o = 0.f;
-#pragma unroll
-                                for (int i = 0; i < 4; ++i)
-                                    if (any && i < ns) o = fmaf(__expf(lv[c][i] - lse_all), ov[c][i], o);
-                                if (tid < D) write_final(static_cast<size_t>(it.u) * G + q, o, lse_all, amax_m);
+                            for (int i = 0; i < 4; ++i) {
+                                const bool use = q < G && i < ns && tid < D;
+                                ov[q][i] = use ? __ldcg(p.part_o + (static_cast<size_t>(fx_slot[i < ns ? i : 0]) * kN + q) * D + tid) : 0.f;
                             }
+                        if (tid < G) {
+                            float lv[4];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                lv[i] = i < ns ? __ldcg(p.part_lse + static_cast<size_t>(fx_slot[i]) * kN + tid) : -INFINITY;
+                            const float mx = fmaxf(fmaxf(lv[0], lv[1]), fmaxf(lv[2], lv[3]));
+                            const bool any = mx > -INFINITY;   // partials without a visible key carry -inf
+                            float sum = 0.f;
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) sum += (any && i < ns) ? __expf(lv[i] - mx) : 0.f;
+                            const float lse_all = any ? mx + __logf(sum) : -INFINITY;
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) fx_w[tid][i] = (any && i < ns) ? __expf(lv[i] - lse_all) : 0.f;
+                            fx_lse[tid] = lse_all;
+                        }
+                        named_bar_sync(1, 128);
+#pragma unroll
+                        for (int q = 0; q < kN; ++q) {
+                            if (q >= G) break;
+                            float o = 0.f;
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) o = fmaf(fx_w[q][i], ov[q][i], o);
+                            if (tid < D) write_final(static_cast<size_t>(it.u) * G + q, o, fx_lse[q], amax_m);
                         }
                     } else {
                         for (int q = 0; q < G; ++q) {

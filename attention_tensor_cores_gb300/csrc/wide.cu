@@ -237,7 +237,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
     using C = WCfg<PAIR>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    __shared__ uint64_t q_full, q_empty, c_full[C::kSlots], c_empty[C::kSlots];
+    __shared__ uint64_t q_full[8], q_empty, c_full[C::kSlots], c_empty[C::kSlots];   // q_full: one per Q atom
     __shared__ uint64_t s_full, s_empty, p_full, o_done, mma_done;
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
@@ -250,7 +250,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
     const WaitCtl wc{&abort_flag, p.status, p.limit};
     if (threadIdx.x == 0) {
         abort_flag = 0;
-        mbar_init(&q_full, 1);
+        for (int a = 0; a < 8; ++a) mbar_init(&q_full[a], 1);
         mbar_init(&q_empty, 1);
         for (int i = 0; i < C::kSlots; ++i) {
             mbar_init(&c_full[i], 1);
@@ -299,8 +299,9 @@ __global__ void __launch_bounds__(kWThreads, 1)
             tma_prefetch_desc(&kmap);
             tma_prefetch_desc(&vmap);
             WRing cr(C::kSlots);
-            uint32_t qn = 0, ccnt[C::kSlots];
+            uint32_t qn = 0, ccnt[C::kSlots], qcnt[8];   // items, and copies per ring slot / Q atom
             for (int i = 0; i < C::kSlots; ++i) ccnt[i] = 0;
+            for (int a = 0; a < 8; ++a) qcnt[a] = 0;
             // a copy into this CTA's shared memory, completing on the current slot's barrier; with PAIR
             // the leader's barrier counts both CTAs' bytes
             auto load = [&](uint8_t* dst, const CUtensorMap* m, uint64_t* bar, int x, int y, int z) {
@@ -320,8 +321,15 @@ __global__ void __launch_bounds__(kWThreads, 1)
                 ++ccnt[cr.idx];
                 return true;
             };
-            auto load_k = [&](int hu, int t) {
+            // K chunks of tile t; with q_rt >= 0 (an item's first tile) each Q atom goes right before the K
+            // chunk it multiplies, so the first MMAs wait for 32 KB instead of the whole 128 KB of Q
+            auto load_k = [&](int hu, int t, int q_rt) {
                 for (int a = 0; a < kWKChunks; ++a) {
+                    if (q_rt >= 0 && !aborted(wc)) {
+                        if (leader) mbar_arrive_expect_tx(&q_full[a], PAIR ? 2 * (kWRows * 128) : kWRows * 128);
+                        load(smem + kWOffQ + a * (kWRows * 128), &qmap, &q_full[a], a * 64, q_rt * kWRows, hu);
+                        ++qcnt[a];
+                    }
                     if (begin_chunk())
                         load(smem + kWOffRing + cr.idx * C::kChunkBytes, &kmap, &c_full[cr.idx], a * 64,
                              t * kWKeys + (PAIR ? 64 * half : 0), hu);
@@ -341,18 +349,14 @@ __global__ void __launch_bounds__(kWThreads, 1)
                 }
             };
             while (sched.next(it)) {
+                if (it.t1 <= it.t0) continue;   // a unit without keys: no Q either (its O is zero)
                 const int hu = wunit_head(p, it.u);
                 const int rt = it.u % p.row_tiles;
-                mbar_wait(&q_empty, (qn & 1) ^ 1, wc);
-                if (!aborted(wc)) {
-                    if (leader) mbar_arrive_expect_tx(&q_full, PAIR ? 2 * kWQBytes : kWQBytes);
-                    for (int a = 0; a < 8; ++a) load(smem + kWOffQ + a * (kWRows * 128), &qmap, &q_full, a * 64, rt * kWRows, hu);
-                }
+                mbar_wait(&q_empty, (qn & 1) ^ 1, wc);   // the previous item's MMAs are done with Q
                 ++qn;
-                if (it.t1 <= it.t0) continue;
-                load_k(hu, it.t0);
+                load_k(hu, it.t0, rt);
                 for (int t = it.t0 + 1; t < it.t1 && !aborted(wc); ++t) {
-                    load_k(hu, t);
+                    load_k(hu, t, -1);
                     load_v(hu, t - 1);
                 }
                 load_v(hu, it.t1 - 1);
@@ -362,7 +366,8 @@ __global__ void __launch_bounds__(kWThreads, 1)
             if (leader) {
                 for (int i = 0; i < C::kSlots; ++i)
                     if (ccnt[i]) wdrain(&c_full[i], (ccnt[i] - 1) & 1, kDrainLimit);
-                if (qn) wdrain(&q_full, (qn - 1) & 1, kDrainLimit);
+                for (int a = 0; a < 8; ++a)
+                    if (qcnt[a]) wdrain(&q_full[a], (qcnt[a] - 1) & 1, kDrainLimit);
             } else {
                 for (int i = 0; i < C::kSlots; ++i)
                     if (ccnt[i]) wdrain(&c_empty[i], (ccnt[i] - 1) & 1, kDrainLimit);
@@ -387,9 +392,11 @@ __global__ void __launch_bounds__(kWThreads, 1)
             uint32_t qn = 0, ns = 0, np = 0;   // items, QKs and PVs so far (kernel life)
             const uint32_t sQ = smem_u32(smem + kWOffQ);
             const uint64_t dq0 = sdesc_sw128(sQ, 16, 1024);
-            auto issue_qk = [&]() {
+            // first_q: the item's first QK, whose Q atoms may still be landing (atom a with K chunk a)
+            auto issue_qk = [&](bool first_q) {
                 if (ns > 0) wait_x(&s_empty, (ns - 1) & 1);   // the softmax has read S
                 for (int a = 0; a < kWKChunks; ++a) {
+                    if (first_q) mbar_wait(&q_full[a], (qn - 1) & 1, wc);
                     mbar_wait(&c_full[cr.idx], cr.phase, wc);
                     if (aborted(wc)) return;
                     tc_fence_after();
@@ -435,14 +442,13 @@ __global__ void __launch_bounds__(kWThreads, 1)
                 ++np;
             };
             while (sched.next(it)) {
-                mbar_wait(&q_full, qn & 1, wc);
-                ++qn;
-                tc_fence_after();
                 const int T = it.t1 - it.t0;
-                if (T > 0 && !aborted(wc)) {
-                    issue_qk();
+                if (T <= 0) continue;   // no keys, no Q loaded (the producer skips it too)
+                ++qn;
+                if (!aborted(wc)) {
+                    issue_qk(true);
                     for (int j = 1; j < T && !aborted(wc); ++j) {
-                        issue_qk();
+                        issue_qk(false);
                         issue_pv(j == 1);
                     }
                     if (!aborted(wc)) issue_pv(T == 1);
