@@ -6,6 +6,7 @@
 #include <cudaTypedefs.h>
 
 #include <atomic>
+#include <cmath>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -254,9 +255,11 @@ static size_t workspace_bytes(const AttnArgs& a, int num_splits)
 }
 
 static int validate(const void* q, const void* k, const void* v, const void* out, int B, int Hq, int Hkv, int Sq,
-                    int Skv, int D, const fmha_opts* o)
+                    int Skv, int D, float scale, const fmha_opts* o)
 {
     if (!q || !k || !v || !out) return set_error(FMHA_ERR_INVALID, "NULL q/k/v/out");
+    // the kernels take each row's maximum of the raw scores and scale it afterwards, which needs scale > 0
+    if (!(scale > 0.f) || !(scale < INFINITY)) return set_error(FMHA_ERR_INVALID, "scale must be a positive finite number");
     if (B < 0 || Hq <= 0 || Hkv <= 0 || Sq < 0 || Skv <= 0)
         return set_error(FMHA_ERR_INVALID, "need B >= 0, Hq > 0, Hkv > 0, Sq >= 0, Skv >= 1");
     if (Hq % Hkv != 0) return set_error(FMHA_ERR_INVALID, "Hq must be a multiple of Hkv");
@@ -321,7 +324,7 @@ size_t fmha_workspace_size(int B, int Hq, int Hkv, int Sq, int Skv, int D, const
 int fmha_fwd_ex(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq, int Hkv, int Sq,
                 int Skv, int D, float scale, fmha_stream_t stream, const fmha_opts* opts)
 {
-    int rc = validate(q, k, v, out, B, Hq, Hkv, Sq, Skv, D, opts);
+    int rc = validate(q, k, v, out, B, Hq, Hkv, Sq, Skv, D, scale, opts);
     if (rc) return rc;
     if (lse && (reinterpret_cast<uintptr_t>(lse) & 3)) return set_error(FMHA_ERR_INVALID, "lse must be 4-byte aligned");
     if (!device_status_ptr()) return set_error(FMHA_ERR_CUDA, "no CUDA device");

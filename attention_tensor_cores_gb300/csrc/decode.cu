@@ -1019,6 +1019,8 @@ extern "C" int fmha_fwd_decode_noalloc(const void* q, const void* k, const void*
     if (B < 0 || Hq <= 0 || Hkv <= 0 || Sq < 0 || Skv <= 0 || Hq % Hkv != 0)
         return set_error(FMHA_ERR_INVALID, "fmha_fwd_decode_noalloc: need B >= 0, Sq >= 0, Skv >= 1, Hq % Hkv == 0");
     if (D != 64 && D != 128) return set_error(FMHA_ERR_INVALID, "fmha_fwd_decode_noalloc: D must be 64 or 128");
+    if (!(scale > 0.f) || !(scale < INFINITY))
+        return set_error(FMHA_ERR_INVALID, "fmha_fwd_decode_noalloc: scale must be a positive finite number");
     if (static_cast<long long>(Hq / Hkv) * Sq > 16)
         return set_error(FMHA_ERR_INVALID, "fmha_fwd_decode_noalloc: at most 16 query rows per key/value head");
     auto mis = [](const void* p, uintptr_t m) { return (reinterpret_cast<uintptr_t>(p) & m) != 0; };

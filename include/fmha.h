@@ -104,7 +104,8 @@ typedef enum {
 /*
  * Attention forward with default options (BF16 output, dense keys, no workspace, no split).
  *   q: BF16 [B,Hq,Sq,D]; k, v: BF16 [B,Hkv,Skv,D]; out: BF16 [B,Hq,Sq,D];
- *   lse: FP32 [B,Hq,Sq] or NULL; scale: multiplies Q K^T before the softmax.
+ *   lse: FP32 [B,Hq,Sq] or NULL; scale: multiplies Q K^T before the softmax, a positive finite number
+ *   (FMHA_ERR_INVALID otherwise: the kernels scale each row's maximum score after taking it).
  * Same as fmha_fwd_ex(..., opts = NULL): every (b, kv-head) unit is handled whole by one CTA (for
  * D = 512 by one CTA pair, each CTA writing its half of the value columns), so nothing needs a
  * workspace.  Decode shapes with few units leave SMs idle this way; fmha_fwd_ex with a workspace

@@ -22,7 +22,7 @@ def test_exports_every_declared_function(lib):
 
 
 def test_error_strings(lib):
-    for code in range(6):
+    for code in range(7):
         assert lib.fmha_error_string(code).decode().startswith("FMHA_")
     assert b"unknown" in lib.fmha_error_string(99)
 
@@ -33,3 +33,11 @@ def test_null_pointers_rejected_without_device(lib):
     fake = ctypes.c_void_p(0x1000)
     assert lib.fmha_qk_gemm(fake, fake, fake, 1, 128, 48, None) == F.FMHA_ERR_INVALID
     assert lib.fmha_qk_gemm(ctypes.c_void_p(0x1008), fake, fake, 1, 128, 64, None) == F.FMHA_ERR_INVALID
+
+
+def test_non_positive_or_non_finite_scale_rejected_without_device(lib):
+    fake = ctypes.c_void_p(0x1000)
+    for sc in (0.0, -0.125, float("nan"), float("inf")):
+        assert lib.fmha_fwd(fake, fake, fake, fake, None, 1, 1, 1, 1, 16, 64, sc, None) == F.FMHA_ERR_INVALID
+        assert b"scale" in lib.fmha_last_error()
+        assert lib.fmha_fwd_decode_noalloc(fake, fake, fake, fake, None, 1, 1, 1, 1, 16, 64, sc, None, None) == F.FMHA_ERR_INVALID

@@ -1,0 +1,68 @@
+"""GPU edge and degenerate cases through the C ABI: empty problems, and a zero query, where every
+visible key has the same score, so O is the plain mean of the visible value rows and LSE = ln n
+(a closed form that does not depend on the keys), on every kernel path including the causal mask."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from attention_tensor_cores_gb300 import inputs
+from attn_util import check_o_lse, run_attention
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def F():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import attention_tensor_cores_gb300 as F
+    F.load()
+    return F
+
+
+@pytest.mark.parametrize("B,Sq,D", [(0, 1, 128), (2, 0, 64), (0, 300, 64), (0, 1, 512)])
+def test_empty_problem_is_a_no_op(F, B, Sq, D):
+    q = torch.zeros(max(B, 1), 4, max(Sq, 1), D, dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros(max(B, 1), 2, 16, D, dtype=torch.bfloat16, device="cuda")
+    out = torch.full_like(q, float("nan"))
+    lse = torch.full(q.shape[:3], float("nan"), dtype=torch.float32, device="cuda")
+    lib = F.load()
+    import ctypes
+    P = lambda t: ctypes.c_void_p(t.data_ptr())
+    s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    launches = F.fmha_launch_count()
+    assert lib.fmha_fwd(P(q), P(k), P(k), P(out), P(lse), B, 4, 2, Sq, 16, D, 0.125, s) == F.FMHA_OK
+    torch.cuda.synchronize()
+    assert F.fmha_check_status() == 0
+    assert F.fmha_launch_count() == launches      # nothing launched
+    assert torch.isnan(out).all() and torch.isnan(lse).all()   # nothing written
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Sq,Skv,D,causal,splits", [
+    (2, 8, 2, 1, 3000, 128, False, 0),     # decode, split
+    (2, 32, 8, 4, 500, 64, True, 0),       # multi-token decode, causal
+    (1, 2, 2, 300, 700, 64, False, None),  # row tiles D = 64
+    (1, 2, 1, 400, 400, 128, True, 0),     # row tiles D = 128, causal
+    (2, 128, 1, 1, 700, 512, False, 0),    # wide head, split
+    (1, 16, 1, 2, 300, 512, True, 1),      # wide head, whole units, causal
+])
+def test_zero_query_gives_mean_of_visible_values(F, B, Hq, Hkv, Sq, Skv, D, causal, splits):
+    w = inputs.Workload("t", B, Hq, Hkv, Sq, Skv, D, 1.0, "bf16", 95)
+    _, k, v, _ = w.make("cuda")
+    q = torch.zeros(B, Hq, Sq, D, dtype=torch.bfloat16, device="cuda")
+    kw = {} if splits is None else {"num_splits": splits}
+    if causal:
+        kw["causal"] = True
+    res = run_attention(F, q, k, v, w.scale, **kw)
+    vv = v.double().cpu().numpy()
+    g = Hq // Hkv
+    o_ref = np.zeros((B * Hq * Sq, D))
+    l_ref = np.zeros(B * Hq * Sq)
+    for r in range(B * Hq * Sq):
+        b, hq, i = r // (Hq * Sq), (r // Sq) % Hq, r % Sq
+        n = min(Skv, i + Skv - Sq + 1) if causal else Skv   # bottom-right aligned
+        o_ref[r] = vv[b, hq // g, :n].mean(axis=0)
+        l_ref[r] = math.log(n)
+    check_o_lse(res["o"], res["lse"], o_ref, l_ref, "zero query")
