@@ -639,7 +639,7 @@ def main():
     ap.add_argument("--only-headline", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle's CPU baselines")
     ap.add_argument("--profile", choices=["c1", "c2", "c3", "c4", "c5", "c3_causal", "c3_d128", "c5_given_scale", "c2_spec_causal",
-                                          "c5_small", "c4_pair"], default=None,
+                                          "c5_small", "c4_pair", "nvfp4"], default=None,
                     help="run one workload's call --repeat times, untimed (for a profiler)")
     ap.add_argument("--repeat", type=int, default=5)
     args = ap.parse_args()
@@ -649,6 +649,17 @@ def main():
         ge.build()
         import attention_tensor_cores_gb300 as F
         from attention_tensor_cores_gb300 import inputs
+        if args.profile == "nvfp4":   # the standalone two-pass quantiser on 64 Mi FP32 values (256 MiB)
+            n = 1 << 26
+            x = torch.randn(n, generator=torch.Generator().manual_seed(7)).cuda()
+            qq = torch.empty(n // 2, dtype=torch.uint8, device="cuda")
+            sc = torch.empty(F.nvfp4_scales_bytes(n), dtype=torch.uint8, device="cuda")
+            for _ in range(args.repeat):
+                F.nvfp4_quantize(x, qq, sc)
+            torch.cuda.synchronize()
+            assert F.fmha_check_status() == 0
+            print(f"profile run of nvfp4_quantize on {n} values: {args.repeat} calls ok")
+            return
         if args.profile == "c2_spec_causal":
             w = spec_decode_workload()
         elif args.profile == "c3_d128":
