@@ -72,6 +72,8 @@ struct DecodeParams {
     const int32_t* prefix;   // [U+1] tile prefix (ragged split mode), else NULL
     int tiles_uniform;       // tiles per unit when prefix == NULL
     int split;               // 1 = stream-K partition, 0 = whole units per CTA
+    int pieces;              // split mode, uniform lengths: each unit cut into P / U (or one more) pieces, one
+                             // piece per CTA (one epilogue per CTA), instead of equal tile ranges
     // outputs
     void* out;               // BF16 or F32 [U*G][D] (NULL when writing FP32 staging only)
     int out_f32;             // 1: `out` is FP32
@@ -122,6 +124,25 @@ struct Sched {
         p = pp;
         cta = c;
         nctas = n;
+        if (p->split && p->pieces) {
+            // CTA c holds piece c - first(u) of unit u: units below r have k + 1 pieces, the others k
+            const int k = n / p->U, r = n % p->U;
+            int uu, piece, np;
+            if (c < r * (k + 1)) {
+                uu = c / (k + 1);
+                piece = c % (k + 1);
+                np = k + 1;
+            } else {
+                const int c2 = c - r * (k + 1);
+                uu = r + c2 / k;
+                piece = c2 % k;
+                np = k;
+            }
+            const long long Tu = p->tiles_uniform;
+            g = static_cast<long long>(uu) * Tu + (piece * Tu) / np;
+            g1 = static_cast<long long>(uu) * Tu + ((piece + 1) * Tu) / np;
+            return;
+        }
         if (p->split) {
             const long long T = p->prefix ? p->prefix[p->U] : static_cast<long long>(p->U) * p->tiles_uniform;
             g = (static_cast<long long>(c) * T) / n;
@@ -221,6 +242,16 @@ __device__ __forceinline__ float warp_sum(float v)
 // most cap) and returns how many there are; 0 for a unit without tiles.
 __device__ int unit_partial_slots(const DecodeParams& p, int u, int P, int* slots, int cap)
 {
+    if (p.pieces) {   // the CTAs holding unit u's pieces are consecutive; a piece may be empty
+        const int k = P / p.U, r = P % p.U;
+        const int np = u < r ? k + 1 : k;
+        const int c0 = u < r ? u * (k + 1) : r * (k + 1) + (u - r) * k;
+        const long long Tu = p.tiles_uniform;
+        int n = 0;
+        for (int i = 0; i < np && n < cap; ++i)
+            if ((i * Tu) / np != ((i + 1) * Tu) / np) slots[n++] = u + c0 + i;
+        return n;
+    }
     int tiles;
     long long Tu, T;
     if (p.prefix) {
@@ -916,6 +947,10 @@ int run_decode(const AttnArgs& a, bool split, void* ws, cudaStream_t st)
     // combine launch).  Measured slower for ragged batches, which keep the combine kernel (it also
     // writes units without keys); single-pass NVFP4 keeps it too (one block per row encodes).
     p.fixup = (split && !a.nv_sg && !a.seqlens && nsm <= kMaxFixSlots) ? 1 : 0;
+    // Many query columns per unit make a split epilogue (partial store, arrival, merge) cost several
+    // tiles' time; when every unit can have two or more CTAs, one piece per CTA bounds each CTA to one
+    // epilogue (equal tile ranges give some CTAs the end of one unit and the start of the next).
+    p.pieces = (p.fixup && G >= 8 && 2 * U <= nsm && p.tiles_uniform >= 2 * (nsm / U + 1)) ? 1 : 0;
     p.unit_ctr = split ? reinterpret_cast<unsigned long long*>(base + w.ctr_off) : nullptr;
     p.gen = next_call_tag();
     p.status = device_status_ptr();

@@ -140,3 +140,15 @@ def test_chunked_prefill_ragged_causal_d128(F, num_splits):
     res = run_attention(F, q, k, v, w.scale, seqlens=sl_t, num_splits=num_splits, causal=True)
     o_ref, l_ref = oracle.attention(q.cpu(), k.cpu(), v.cpu(), w.scale, seqlens_k=np.array(sl, np.int32), causal=True)
     check_o_lse(res["o"], res["lse"], o_ref, l_ref, "chunked prefill")
+
+
+def test_speculative_decode_full_size_every_row(F):
+    """B8 Hq32 Hkv8 Sq4 Skv8192 D128, causal (16 query columns per key/value head): every one of the
+    1024 rows against the oracle.  64 units for 152 or so CTAs: each unit is cut into two or three
+    pieces, one per CTA, merged in the kernel by the CTA that completes the unit."""
+    w = inputs.Workload("speculative decode", 8, 32, 8, 4, 8192, 128, 1.0, "bf16", 1006)
+    q, k, v, _ = w.make("cuda")
+    res = run_attention(F, q, k, v, w.scale, num_splits=0, causal=True)
+    rows = np.arange(w.B * w.Hq * w.Sq, dtype=np.int64)
+    o_ref, l_ref = oracle_rows(w, rows, causal=True, tensors=(q, k, v))
+    check_o_lse(res["o"], res["lse"], o_ref, l_ref, "speculative decode full size")
