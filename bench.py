@@ -34,10 +34,18 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # named kernel, with the sha256 of its source file at capture time; reported only while the
 # source is unchanged.
 TRAFFIC = {
-    # decode B8 H32 Sq1 Skv4096 D128: read 537,087,744 + written 2,807,296 bytes (profiles/decode_kernel_decode-B8-H32-Skv4096-D128.md)
-    "decode_kernel<128>": {"bytes": 539895040, "source_sha": "460587cc58668c69"},
-    # wide-head B32 Hq128 Hkv1 Skv16384 D512: read 1,081,711,616 + written 10,590,208 bytes (profiles/wide_kernel_wide-head-B32-Hq128-Hkv1-Skv16384-D512.md)
-    "wide_kernel": {"bytes": 1092301824, "source_sha": "18992f252617a94f"},
+    # decode B8 H32 Sq1 Skv4096 D128: read 537,100,544 + written 3,378,688 bytes
+    # (profiles/decode_kernel_decode-B8-H32-Skv4096-D128.md)
+    "decode_kernel<128>": {"bytes": 540479232, "source_sha": "d9b1268a1cb1c68d"},
+    # ragged GQA decode B64 Hq32 Hkv8 Skv<=32768 D128: the quarter-size workload (B16) read 1,005,878,016 +
+    # wrote 368,384 bytes for 1,001,226,240 algorithmic K/V bytes (1.005x); scaled by the K/V bytes to the
+    # full workload's 4,106,002,432 (profiles/side-kernels_ragged-decode-wide-combine-nvfp4.md)
+    "decode_kernel<128>/ragged": {"bytes": 4126589976, "source_sha": "d9b1268a1cb1c68d"},
+    # wide-head B32 Hq128 Hkv1 Skv16384 D512, independent CTAs: read 1,081,726,976 + written 10,267,392
+    # bytes (profiles/wide_kernel_wide-head-B32-Hq128-Hkv1-Skv16384-D512.md)
+    "wide_kernel<independent>": {"bytes": 1091994368, "source_sha": "9c5cf7172015beea"},
+    # same workload, CTA-pair MMA: read 1,081,826,048 + written 10,286,592 bytes (same file)
+    "wide_kernel<pair>": {"bytes": 1092112640, "source_sha": "9c5cf7172015beea"},
 }
 
 
@@ -452,7 +460,7 @@ def _workload_entry(F, w, idx, steps, warmup, peaks, causal=False, given_scale=F
         ach = case.algorithmic_bytes() / (kern_ms / 1e3) / 1e9
         if w.D == 512:
             traffic = traffic_for("wide_kernel<pair>" if wide_variant == 2 else "wide_kernel<independent>", "wide.cu")
-        elif w.ragged and not causal:
+        elif w.ragged and not causal and not given_scale:
             traffic = traffic_for("decode_kernel<128>/ragged", "decode.cu")
         else:
             traffic = None
