@@ -757,30 +757,65 @@ __global__ void __launch_bounds__(kWRows) wide_combine_kernel(const __grid_const
     // so that every lane takes part in the warp reduction below
     const int row = (u % p.row_tiles) * kWRows + r;
     const bool live = row < p.R;
-    // merged LSE of this row; partials without a visible key carry lse = -inf and weigh 0
-    float mx = -INFINITY;
-    for (int i = 0; i < ns; ++i) mx = fmaxf(mx, p.part_lse[static_cast<size_t>(slots[i]) * kWRows + r]);
-    const bool any = mx > -INFINITY;
-    float sum = 0.f;
-    if (any)
-        for (int i = 0; i < ns; ++i) sum += __expf(p.part_lse[static_cast<size_t>(slots[i]) * kWRows + r] - mx);
-    const float lse_v = (ns > 0 && any) ? mx + __logf(sum) : -INFINITY;
+    // merged LSE of this row (partials without a visible key carry lse = -inf and weigh 0) and the
     // weighted sum of this row's 32 columns over the partials
     float acc[kCombCols];
 #pragma unroll
     for (int k = 0; k < kCombCols; ++k) acc[k] = 0.f;
-    for (int j = 0; j < ns && any; ++j) {
-        const int sl = slots[j];
-        const float w = __expf(p.part_lse[static_cast<size_t>(sl) * kWRows + r] - lse_v);
-        float4 x[kCombCols / 4];
+    float lse_v = -INFINITY;
+    if (ns <= 4) {
+        // the usual case (a unit cut by the stream-K split into at most four pieces): every partial LSE
+        // and every partial column of this row in flight at once, one memory round trip
+        float lv[4];
+        float4 x[4][kCombCols / 4];
 #pragma unroll
-        for (int k = 0; k < kCombCols / 4; ++k) x[k] = *reinterpret_cast<const float4*>(p.part_o + wpart_index(sl, r, col0 + 4 * k));
+        for (int i = 0; i < 4; ++i) {
+            const size_t sl = ns > 0 ? static_cast<size_t>(slots[i < ns ? i : 0]) : 0;   // a valid slot even when unused
+            lv[i] = i < ns ? p.part_lse[sl * kWRows + r] : -INFINITY;
 #pragma unroll
-        for (int k = 0; k < kCombCols / 4; ++k) {
-            acc[4 * k] = fmaf(w, x[k].x, acc[4 * k]);
-            acc[4 * k + 1] = fmaf(w, x[k].y, acc[4 * k + 1]);
-            acc[4 * k + 2] = fmaf(w, x[k].z, acc[4 * k + 2]);
-            acc[4 * k + 3] = fmaf(w, x[k].w, acc[4 * k + 3]);
+            for (int k = 0; k < kCombCols / 4; ++k)
+                x[i][k] = i < ns ? *reinterpret_cast<const float4*>(p.part_o + wpart_index(sl, r, col0 + 4 * k))
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        const float mx = fmaxf(fmaxf(lv[0], lv[1]), fmaxf(lv[2], lv[3]));
+        if (mx > -INFINITY) {
+            float sum = 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) sum += __expf(lv[i] - mx);   // exp(-inf) = 0 for the unused slots
+            lse_v = mx + __logf(sum);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float w = __expf(lv[i] - lse_v);
+#pragma unroll
+                for (int k = 0; k < kCombCols / 4; ++k) {
+                    acc[4 * k] = fmaf(w, x[i][k].x, acc[4 * k]);
+                    acc[4 * k + 1] = fmaf(w, x[i][k].y, acc[4 * k + 1]);
+                    acc[4 * k + 2] = fmaf(w, x[i][k].z, acc[4 * k + 2]);
+                    acc[4 * k + 3] = fmaf(w, x[i][k].w, acc[4 * k + 3]);
+                }
+            }
+        }
+    } else {
+        float mx = -INFINITY;
+        for (int i = 0; i < ns; ++i) mx = fmaxf(mx, p.part_lse[static_cast<size_t>(slots[i]) * kWRows + r]);
+        const bool any = mx > -INFINITY;
+        float sum = 0.f;
+        if (any)
+            for (int i = 0; i < ns; ++i) sum += __expf(p.part_lse[static_cast<size_t>(slots[i]) * kWRows + r] - mx);
+        lse_v = any ? mx + __logf(sum) : -INFINITY;
+        for (int j = 0; j < ns && any; ++j) {
+            const int sl = slots[j];
+            const float w = __expf(p.part_lse[static_cast<size_t>(sl) * kWRows + r] - lse_v);
+            float4 x[kCombCols / 4];
+#pragma unroll
+            for (int k = 0; k < kCombCols / 4; ++k) x[k] = *reinterpret_cast<const float4*>(p.part_o + wpart_index(sl, r, col0 + 4 * k));
+#pragma unroll
+            for (int k = 0; k < kCombCols / 4; ++k) {
+                acc[4 * k] = fmaf(w, x[k].x, acc[4 * k]);
+                acc[4 * k + 1] = fmaf(w, x[k].y, acc[4 * k + 1]);
+                acc[4 * k + 2] = fmaf(w, x[k].z, acc[4 * k + 2]);
+                acc[4 * k + 3] = fmaf(w, x[k].w, acc[4 * k + 3]);
+            }
         }
     }
     const size_t orow = static_cast<size_t>(hu) * p.R + (live ? row : 0);
