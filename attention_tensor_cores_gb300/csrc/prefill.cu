@@ -130,6 +130,16 @@ __device__ __forceinline__ void item_coords(const PrefillParams& p, int r, int& 
     pair = p.pairs - 1 - level;
 }
 
+// Fixed (counter-free) item order: round k of CTA c takes item k*G + c.  With the causal mask, whose
+// items are numbered heaviest first, odd rounds take k*G + G-1-c instead, so a CTA that drew a heavy
+// item in one round draws a light one in the next and the CTAs' totals even out.
+template <bool CAUSAL>
+__device__ __forceinline__ int fixed_item(int k)
+{
+    const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+    return k * G + ((CAUSAL && (k & 1)) ? G - 1 - c : c);
+}
+
 // Key tiles query tile q of a pair needs: none when its rows are all past R; with the causal
 // mask only those up to the last key its rows can see (row r sees keys < r % Sq + n - Sq + 1).
 template <bool CAUSAL, int kTN>
@@ -243,7 +253,8 @@ __global__ void __launch_bounds__(prefill_threads<RING>(), 1)
                 for (int i = 0; i < S; ++i) kcnt[i] = vcnt[i] = 0;
                 for (int i = 0; i < QS; ++i) qcnt[i] = 0;
                 PRing ir(kItemSlots);
-                int item = (RING && p.sched) ? atomicAdd(p.sched, 1) : static_cast<int>(blockIdx.x);
+                int round = 0;   // fixed order: this CTA's round
+                int item = (RING && p.sched) ? atomicAdd(p.sched, 1) : fixed_item<CAUSAL>(0);
                 for (;;) {
                     const bool more = item < n_items;
                     if constexpr (RING) {
@@ -261,9 +272,10 @@ __global__ void __launch_bounds__(prefill_threads<RING>(), 1)
                     const int T = max(tile_count<CAUSAL, C::kTN>(p, pair, 0, n), tile_count<CAUSAL, C::kTN>(p, pair, 1, n));
                     // the next item is claimed once this one's loads are issued, so a CTA takes new
                     // work only shortly before it runs out
-                    const int next = item + static_cast<int>(gridDim.x);
+                    const int next = fixed_item<CAUSAL>(round + 1);
                     if (T == 0) {
                         item = (RING && p.sched) ? atomicAdd(p.sched, 1) : next;
+                        ++round;
                         continue;
                     }
                     mbar_wait(&q_empty[qr.idx], qr.phase ^ 1, wc);
@@ -298,6 +310,7 @@ __global__ void __launch_bounds__(prefill_threads<RING>(), 1)
                         vr.advance();
                     }
                     item = (RING && p.sched) ? atomicAdd(p.sched, 1) : next;
+                    ++round;
                 }
                 for (int i = 0; i < S; ++i) {
                     if (kcnt[i]) drain_wait_p(&k_full[i], (kcnt[i] - 1) & 1, kDrainLimit);
@@ -317,7 +330,7 @@ __global__ void __launch_bounds__(prefill_threads<RING>(), 1)
                 uint32_t nqk_all = 0;        // QKs issued over the kernel's life (shared S buffer)
                 uint32_t npv[2] = {0, 0};    // PVs issued per query tile
                 PRing ir(kItemSlots);
-                int next_fixed = static_cast<int>(blockIdx.x);
+                int round = 0;
                 for (;;) {
                     int item;
                     if constexpr (RING) {
@@ -327,9 +340,8 @@ __global__ void __launch_bounds__(prefill_threads<RING>(), 1)
                         ir.advance();
                         if (item < 0) break;
                     } else {
-                        item = next_fixed;
+                        item = fixed_item<CAUSAL>(round++);
                         if (item >= n_items) break;
-                        next_fixed += static_cast<int>(gridDim.x);
                     }
                     int u, pair;
                     item_coords<CAUSAL>(p, item, u, pair);
@@ -432,7 +444,7 @@ __global__ void __launch_bounds__(prefill_threads<RING>(), 1)
         uint32_t gt = 0;     // tiles processed by this warpgroup over the kernel's life (S/P/O rings)
         uint32_t gring = 0;  // K/V ring position of the current item's first tile
         PRing ir(kItemSlots);
-        int next_fixed = static_cast<int>(blockIdx.x);
+        int round = 0;
         for (;;) {
             int item;
             if constexpr (RING) {
@@ -444,9 +456,8 @@ __global__ void __launch_bounds__(prefill_threads<RING>(), 1)
                 ir.advance();
                 if (item < 0) break;
             } else {
-                item = next_fixed;
+                item = fixed_item<CAUSAL>(round++);
                 if (item >= n_items) break;
-                next_fixed += static_cast<int>(gridDim.x);
             }
             int u, pair;
             item_coords<CAUSAL>(p, item, u, pair);
