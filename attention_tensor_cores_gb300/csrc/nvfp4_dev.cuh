@@ -6,14 +6,16 @@
 //   block scale  sc   = E4M3(amax_b / (6 s_g))
 //   element code c_i  = E2M1(x_i / (dec(sc) s_g)), sign kept
 //
-// Each decision compares |x| with t * s_g for a threshold t that is a grid midpoint times a small
-// exact factor (6 for the block scale, dec(sc) for the elements), so t has at most 7 significant
-// bits and is exact in FP32.  The product is kept exactly as hi + lo with hi = fl(t s_g) and
-// lo = fma(t, s_g, -hi).  d = |x| - hi is exact when |x| is within a factor of two of hi
-// (Sterbenz) and otherwise so far from hi that comparing it with lo still gives the right sign, so
-// "d against lo" decides "|x| against t s_g" exactly.  lo is exact while t s_g stays well inside
-// the normal range; for s_g outside [2^-90, 2^100] the FP64 route below is used instead (rounding
-// of FP64 quotients, whose products with the grid midpoints have at most 31 significant bits).
+// Each decision asks whether |x| rounds up across a threshold t * s_g, where t is a grid midpoint
+// times a small exact factor (6 for the block scale, dec(sc) for the elements), so t has at most 7
+// significant bits and is exact in FP32.  Rounding up means |x| > t s_g, or |x| == t s_g when the
+// upper code is even.  Write t s_g = hi + lo exactly (hi = fl(t s_g), lo = fma(t, s_g, -hi)).  No
+// float lies strictly between hi and t s_g, so for a float |x| that question is the single
+// comparison |x| >= U with U = hi when lo < 0 (or lo == 0 and the tie rounds up) and U = the next
+// float above hi otherwise.  The bounds are computed once per block, so each element costs seven
+// plain comparisons.  lo is exact while t s_g stays well inside the normal range; for s_g outside
+// [2^-90, 2^100] the FP64 route below is used instead (rounding of FP64 quotients, whose products
+// with the grid midpoints have at most 31 significant bits).
 #pragma once
 
 #include <cstdint>
@@ -70,13 +72,13 @@ __device__ __forceinline__ float e4m3_value_f32(uint32_t c)
     return e ? __uint_as_float(((e + 120u) << 23) | (m << 20)) : static_cast<float>(m) * 0x1p-9f;
 }
 
-// Sign of (a - t * s) for a >= 0, with t * s taken exactly (see the file comment): -1, 0 or 1.
-__device__ __forceinline__ int cmp_exact_product(float a, float t, float s)
+// Smallest float a >= 0 that rounds up across the threshold t * s (t * s taken exactly: see the
+// file comment); tie_up: whether a == t * s rounds up.
+__device__ __forceinline__ float round_up_bound(float t, float s, bool tie_up)
 {
     const float hi = __fmul_rn(t, s);
     const float lo = __fmaf_rn(t, s, -hi);
-    const float d = __fsub_rn(a, hi);
-    return (d > lo) - (d < lo);
+    return (lo < 0.f || (lo == 0.f && tie_up)) ? hi : __uint_as_float(__float_as_uint(hi) + 1u);
 }
 
 // Approximate E4M3 code of q >= 0 (may be one off near a midpoint; corrected by the caller).
@@ -97,52 +99,46 @@ __device__ __forceinline__ uint32_t e4m3_candidate(float q)
 // E4M3 block scale of a block with max |x| = ab under s_g (FP32 route).
 __device__ __forceinline__ uint32_t e4m3_block_scale_f32(float ab, float sg)
 {
-    uint32_t c = e4m3_candidate(__fdiv_rn(ab, __fmul_rn(6.f, sg)));
-    // move to the exact nearest code: compare ab with 6 * midpoint * s_g (6 * midpoint is exact)
+    // candidate from an approximate quotient (within one code of the nearest), then moved to the
+    // exact nearest code across the midpoints 6 * (v_c + v_c+1) / 2 * s_g (6 * midpoint is exact)
+    uint32_t c = e4m3_candidate(__fdividef(ab, __fmul_rn(6.f, sg)));
 #pragma unroll 1
     for (int it = 0; it < 3 && c < 0x7E; ++it) {
-        const int s = cmp_exact_product(ab, __fmul_rn(e4m3_value_f32(c) + e4m3_value_f32(c + 1), 3.f), sg);
-        if (s > 0 || (s == 0 && !((c + 1) & 1))) ++c;
+        const float t = __fmul_rn(e4m3_value_f32(c) + e4m3_value_f32(c + 1), 3.f);
+        if (ab >= round_up_bound(t, sg, !((c + 1) & 1))) ++c;
         else break;
     }
 #pragma unroll 1
     for (int it = 0; it < 3 && c > 0; ++it) {
-        const int s = cmp_exact_product(ab, __fmul_rn(e4m3_value_f32(c - 1) + e4m3_value_f32(c), 3.f), sg);
-        if (s < 0 || (s == 0 && !((c - 1) & 1))) --c;
+        const float t = __fmul_rn(e4m3_value_f32(c - 1) + e4m3_value_f32(c), 3.f);
+        if (!(ab >= round_up_bound(t, sg, !(c & 1)))) --c;
         else break;
     }
     return c;
 }
 
-// Rounding thresholds of one block: mid_k * dec(sc) * s_g as exact pairs (hi_k, lo_k).
-struct E2m1Thresholds {
-    float hi[7], lo[7];
+// Round-up bounds of one block's E2M1 midpoints mid_k * dec(sc) * s_g (ties to the even code: a
+// tie at midpoint k rounds up when k is odd).
+struct E2m1Bounds {
+    float u[7];
 };
 
-__device__ __forceinline__ E2m1Thresholds e2m1_thresholds(float dsc, float sg)
+__device__ __forceinline__ E2m1Bounds e2m1_bounds(float dsc, float sg)
 {
     const float mids[7] = {0.25f, 0.75f, 1.25f, 1.75f, 2.5f, 3.5f, 5.0f};
-    E2m1Thresholds t;
+    E2m1Bounds b;
 #pragma unroll
-    for (int k = 0; k < 7; ++k) {
-        const float m = __fmul_rn(mids[k], dsc);   // exact: at most 7 significant bits
-        t.hi[k] = __fmul_rn(m, sg);
-        t.lo[k] = __fmaf_rn(m, sg, -t.hi[k]);
-    }
-    return t;
+    for (int k = 0; k < 7; ++k) b.u[k] = round_up_bound(__fmul_rn(mids[k], dsc), sg, k & 1);   // mid * dsc exact
+    return b;
 }
 
-__device__ __forceinline__ uint32_t e2m1_code_f32(float x, const E2m1Thresholds& t)
+__device__ __forceinline__ uint32_t e2m1_code_f32(float x, const E2m1Bounds& b)
 {
     const float a = fabsf(x);
     uint32_t c = 0;
 #pragma unroll
-    for (int k = 0; k < 7; ++k) {
-        const float d = __fsub_rn(a, t.hi[k]);
-        // above the midpoint: round up; on it: up only when the upper code (k + 1) is even
-        if (d > t.lo[k] || (d == t.lo[k] && (k & 1))) c = k + 1;
-    }
-    return c | (signbit(x) ? 8u : 0u);
+    for (int k = 0; k < 7; ++k) c += a >= b.u[k] ? 1u : 0u;
+    return c | ((__float_as_uint(x) >> 28) & 8u);
 }
 
 // ---- block encoders --------------------------------------------------------------------------------
@@ -163,7 +159,7 @@ __device__ __forceinline__ uint32_t nvfp4_encode16(const float* v, float sg, uin
     if (nvfp4_fp32_route(sg)) {
         const uint32_t sc = e4m3_block_scale_f32(ab, sg);
         if (sc == 0) return 0;
-        const E2m1Thresholds t = e2m1_thresholds(e4m3_value_f32(sc), sg);
+        const E2m1Bounds t = e2m1_bounds(e4m3_value_f32(sc), sg);
 #pragma unroll
         for (int i = 0; i < 8; ++i) lo |= e2m1_code_f32(v[i], t) << (4 * i);
 #pragma unroll
@@ -193,7 +189,7 @@ __device__ __forceinline__ void nvfp4_encode_lanes(float x, float sg, int col, u
     if (nvfp4_scale_usable(sg)) {
         if (nvfp4_fp32_route(sg)) {
             sc = e4m3_block_scale_f32(ab, sg);
-            if (sc) c = e2m1_code_f32(x, e2m1_thresholds(e4m3_value_f32(sc), sg));
+            if (sc) c = e2m1_code_f32(x, e2m1_bounds(e4m3_value_f32(sc), sg));
         } else {
             sc = e4m3_round_sat_f64(static_cast<double>(ab) / (6.0 * static_cast<double>(sg)));
             const double den = e4m3_value_f64(sc) * static_cast<double>(sg);
