@@ -12,10 +12,11 @@
 // upper code is even.  Write t s_g = hi + lo exactly (hi = fl(t s_g), lo = fma(t, s_g, -hi)).  No
 // float lies strictly between hi and t s_g, so for a float |x| that question is the single
 // comparison |x| >= U with U = hi when lo < 0 (or lo == 0 and the tie rounds up) and U = the next
-// float above hi otherwise.  The bounds are computed once per block, so each element costs seven
-// plain comparisons.  lo is exact while t s_g stays well inside the normal range; for s_g outside
-// [2^-90, 2^100] the FP64 route below is used instead (rounding of FP64 quotients, whose products
-// with the grid midpoints have at most 31 significant bits).
+// float above hi otherwise.  A block computes its seven element bounds once; they increase with
+// the midpoint, so each element takes a binary search of three comparisons.  lo is exact while
+// t s_g stays well inside the normal range; for s_g outside [2^-90, 2^100] the FP64 route below is
+// used instead (rounding of FP64 quotients, whose products with the grid midpoints have at most 31
+// significant bits).
 #pragma once
 
 #include <cstdint>
@@ -81,39 +82,33 @@ __device__ __forceinline__ float round_up_bound(float t, float s, bool tie_up)
     return (lo < 0.f || (lo == 0.f && tie_up)) ? hi : __uint_as_float(__float_as_uint(hi) + 1u);
 }
 
-// Approximate E4M3 code of q >= 0 (may be one off near a midpoint; corrected by the caller).
-__device__ __forceinline__ uint32_t e4m3_candidate(float q)
+// Round-up bound of E4M3 code c in 1..126 for the block scale: the smallest amax_b that rounds to
+// c or above is 6 s_g times the midpoint between the values of codes c - 1 and c (ties to the even
+// code).  That midpoint is (2c - 1) 2^-10 for c <= 8 (the subnormal codes and the first normal one).
+// Above, it is the float halfway between the two values' bit patterns: normal codes are 2^20 apart
+// in FP32 bits (v_c has bits (c << 20) + 0x3C000000), and within a binade, and across one since the
+// midpoint lies in the lower binade, FP32 values are linear in their bits.  6 * midpoint has at most
+// 7 significant bits, so it is exact.
+__device__ __forceinline__ float e4m3_up_bound(uint32_t c, float sg)
 {
-    if (!(q > 0.f)) return 0;
-    if (q >= 448.f) return 0x7E;
-    const int E = static_cast<int>((__float_as_uint(q) >> 23) & 0xFF) - 127;   // floor(log2 q), q normal
-    const int e = E + 7;
-    uint32_t c;
-    if (e >= 1)
-        c = static_cast<uint32_t>(8 * (e - 1)) + static_cast<uint32_t>(rintf(q * __uint_as_float(static_cast<uint32_t>(130 - E) << 23)));
-    else
-        c = static_cast<uint32_t>(rintf(q * 512.f));
-    return c > 0x7E ? 0x7Eu : c;
+    const float odd = __fsub_rn(__uint_as_float(0x4B000000u + 2u * c - 1u), 8388608.f);   // 2c - 1, exact
+    const float mid = c > 8u ? __uint_as_float((c << 20) + 0x3BF80000u) : __fmul_rn(odd, 0x1p-10f);
+    return round_up_bound(__fmul_rn(mid, 6.f), sg, !(c & 1u));
 }
 
-// E4M3 block scale of a block with max |x| = ab under s_g (FP32 route).
+// E4M3 block scale of a block with max |x| = ab under s_g (FP32 route).  A candidate comes from the
+// approximate quotient q = ab * (1 / (6 s_g)) (relative error a few 2^-24), rounded half up at
+// E4M3 resolution on q's bits; normal E4M3 values are more than 2^-4 apart relative to their size
+// (2^-9 apart below 2^-6), so the candidate is at most one code from the exact nearest and one exact
+// check on each side settles it.
 __device__ __forceinline__ uint32_t e4m3_block_scale_f32(float ab, float sg)
 {
-    // candidate from an approximate quotient (within one code of the nearest), then moved to the
-    // exact nearest code across the midpoints 6 * (v_c + v_c+1) / 2 * s_g (6 * midpoint is exact)
-    uint32_t c = e4m3_candidate(__fdividef(ab, __fmul_rn(6.f, sg)));
-#pragma unroll 1
-    for (int it = 0; it < 3 && c < 0x7E; ++it) {
-        const float t = __fmul_rn(e4m3_value_f32(c) + e4m3_value_f32(c + 1), 3.f);
-        if (ab >= round_up_bound(t, sg, !((c + 1) & 1))) ++c;
-        else break;
-    }
-#pragma unroll 1
-    for (int it = 0; it < 3 && c > 0; ++it) {
-        const float t = __fmul_rn(e4m3_value_f32(c - 1) + e4m3_value_f32(c), 3.f);
-        if (!(ab >= round_up_bound(t, sg, !(c & 1)))) --c;
-        else break;
-    }
+    const float q = __fmul_rn(ab, __fdividef(1.f, __fmul_rn(6.f, sg)));
+    uint32_t c = q < 0x1p-6f ? __float_as_uint(__fadd_rn(q, 0x1p14f)) - 0x46800000u   // rint(q * 2^9)
+                             : ((__float_as_uint(q) + 0x80000u) >> 20) - 960u;        // 8 e + m, e = exponent - 120
+    c = min(c, 0x7Eu);
+    if (c < 0x7Eu && ab >= e4m3_up_bound(c + 1u, sg)) ++c;
+    else if (c > 0u && !(ab >= e4m3_up_bound(c, sg))) --c;
     return c;
 }
 
@@ -132,13 +127,27 @@ __device__ __forceinline__ E2m1Bounds e2m1_bounds(float dsc, float sg)
     return b;
 }
 
+// The bounds increase with k, so the code (how many bounds |x| reaches) takes a binary search of
+// three comparisons.  A NaN reaches none.
 __device__ __forceinline__ uint32_t e2m1_code_f32(float x, const E2m1Bounds& b)
 {
     const float a = fabsf(x);
-    uint32_t c = 0;
-#pragma unroll
-    for (int k = 0; k < 7; ++k) c += a >= b.u[k] ? 1u : 0u;
-    return c | ((__float_as_uint(x) >> 28) & 8u);
+    const bool p2 = a >= b.u[3];
+    const bool p1 = a >= (p2 ? b.u[5] : b.u[1]);
+    const float u0 = p2 ? b.u[4] : b.u[0], u2 = p2 ? b.u[6] : b.u[2];
+    const bool p0 = a >= (p1 ? u2 : u0);
+    return (p2 ? 4u : 0u) + (p1 ? 2u : 0u) + (p0 ? 1u : 0u) + ((__float_as_uint(x) >> 28) & 8u);
+}
+
+// The same search for one value, computing only the three bounds it visits.
+__device__ __forceinline__ uint32_t e2m1_code_f32(float x, float dsc, float sg)
+{
+    const float a = fabsf(x);
+    const bool p2 = a >= round_up_bound(__fmul_rn(1.75f, dsc), sg, true);
+    const bool p1 = a >= round_up_bound(__fmul_rn(p2 ? 3.5f : 0.75f, dsc), sg, true);
+    const float m0 = p2 ? (p1 ? 5.f : 2.5f) : (p1 ? 1.25f : 0.25f);
+    const bool p0 = a >= round_up_bound(__fmul_rn(m0, dsc), sg, false);
+    return (p2 ? 4u : 0u) + (p1 ? 2u : 0u) + (p0 ? 1u : 0u) + ((__float_as_uint(x) >> 28) & 8u);
 }
 
 // ---- block encoders --------------------------------------------------------------------------------
@@ -189,7 +198,7 @@ __device__ __forceinline__ void nvfp4_encode_lanes(float x, float sg, int col, u
     if (nvfp4_scale_usable(sg)) {
         if (nvfp4_fp32_route(sg)) {
             sc = e4m3_block_scale_f32(ab, sg);
-            if (sc) c = e2m1_code_f32(x, e2m1_bounds(e4m3_value_f32(sc), sg));
+            if (sc) c = e2m1_code_f32(x, e4m3_value_f32(sc), sg);
         } else {
             sc = e4m3_round_sat_f64(static_cast<double>(ab) / (6.0 * static_cast<double>(sg)));
             const double den = e4m3_value_f64(sc) * static_cast<double>(sg);

@@ -117,6 +117,37 @@ def test_standalone_scaled_quantiser_ties(F):
     np.testing.assert_array_equal(q.cpu().numpy(), codes)
 
 
+def _e4m3_value(c):
+    e, m = c >> 3, c & 7
+    return m * 2.0 ** -9 if e == 0 else (8 + m) * 2.0 ** (e - 10)
+
+
+@pytest.mark.parametrize("sg", [2.0 ** -7 * 1.5, float(np.float32(1.37 * 2.0 ** -20)), float(np.float32(0.911 * 2.0 ** 33))])
+def test_standalone_block_scale_every_boundary(F, sg):
+    """Every E4M3 rounding boundary of the block scale: a block whose max |x| is the float nearest
+    to 6 s_g times the midpoint between codes c - 1 and c, and the floats one unit below and above
+    it, for c = 1..126 (ties fall to the even code when the product is exact)."""
+    blocks = []
+    for c in range(1, 127):
+        t = 6.0 * 0.5 * (_e4m3_value(c - 1) + _e4m3_value(c)) * sg     # exact in FP64
+        f = np.float32(t)
+        for top in (np.nextafter(f, np.float32(0)), f, np.nextafter(f, np.float32(np.inf))):
+            blk = np.full(16, top, np.float32) * np.float32(0.5) ** np.arange(16, dtype=np.float32)
+            blk[1::2] *= -1
+            blocks.append(blk)
+    x = np.concatenate(blocks).astype(np.float32)
+    xt = torch.from_numpy(x).cuda()
+    n = x.size
+    q = torch.zeros(n // 2, dtype=torch.uint8, device="cuda")
+    sc = torch.zeros(n // 16, dtype=torch.uint8, device="cuda")
+    F.nvfp4_quantize_scaled(xt, q, sc, torch.tensor([sg], dtype=torch.float32, device="cuda"))
+    torch.cuda.synchronize()
+    codes, scales = oracle.nvfp4_quantize_scaled(x, sg)
+    np.testing.assert_array_equal(sc.cpu().numpy(), scales)
+    np.testing.assert_array_equal(q.cpu().numpy(), codes)
+    assert len(set(scales.tolist())) >= 120
+
+
 def test_two_pass_reports_amax(F):
     """Two-pass NVFP4 with opts.out_amax: the caller's word is the |O| max the quantiser uses, so it
     equals max |O| of the FP32 output and s_g = fp32(amax / 2688)."""
