@@ -499,7 +499,11 @@ __global__ void __launch_bounds__(prefill_threads<RING>(), 1)
                     alpha = ex2_approx(m_run - mt);
                     m_run = mt;
                 }
-                // p = 2^(s*c - m) with packed FP32x2 scale-subtract and sums
+                // p = 2^(s*c - m) with packed FP32x2 scale-subtract and sums.  With the shared S
+                // buffer (D = 128) P goes to Tensor Memory 64 keys at a time as it is produced
+                // (measured 1 % faster there; at D = 64 it measured 2 % slower than one store
+                // after all the exponentials).
+                constexpr bool kChunkP = C::kSharedS;
                 const uint64_t cc = f32x2(p.c, p.c);
                 // causal: a row with no visible key yet keeps m = -inf (no -inf - -inf = NaN)
                 const float mu = (CAUSAL && m_run == -INFINITY) ? 0.f : -m_run;
@@ -507,22 +511,34 @@ __global__ void __launch_bounds__(prefill_threads<RING>(), 1)
                 uint32_t pk[kTN / 2];
                 uint64_t ls[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-                for (int i = 0; i < kTN; i += 2) {
-                    float x0, x1;
-                    f32x2_split(ffma2(f32x2(s[i], s[i + 1]), cc, nm), x0, x1);
-                    const float p0 = ex2_approx(x0);
-                    const float p1 = ex2_approx(x1);
-                    ls[(i >> 1) & 3] = fadd2(ls[(i >> 1) & 3], f32x2(p0, p1));
-                    pk[i >> 1] = pack_bf16x2(p0, p1);
+                for (int c = 0; c < kTN / 64; ++c) {
+#pragma unroll
+                    for (int i = c * 64; i < c * 64 + 64; i += 2) {
+                        float x0, x1;
+                        f32x2_split(ffma2(f32x2(s[i], s[i + 1]), cc, nm), x0, x1);
+                        const float p0 = ex2_approx(x0);
+                        const float p1 = ex2_approx(x1);
+                        ls[(i >> 1) & 3] = fadd2(ls[(i >> 1) & 3], f32x2(p0, p1));
+                        pk[i >> 1] = pack_bf16x2(p0, p1);
+                    }
+                    if constexpr (kChunkP) {
+                        if (c == 0) {
+                            // PV of the previous tile must be done: its P buffer is reused
+                            if (j > 0) mbar_wait(&o_done[q], (gt - 1) & 1, wc);
+                            tc_fence_after();
+                            __syncwarp();   // tcgen05.st is warp-collective
+                        }
+                        tmem_st32(tP + c * 32, pk + c * 32);
+                    }
                 }
-                float la, lb, lc, ld;
+                float la, lb;
                 f32x2_split(fadd2(fadd2(ls[0], ls[1]), fadd2(ls[2], ls[3])), la, lb);
-                (void)lc;
-                (void)ld;
                 l = fmaf(l, alpha, la + lb);
-                // PV of the previous tile must be done: its P buffer is reused and O must be stable.
-                if (j > 0) mbar_wait(&o_done[q], (gt - 1) & 1, wc);
-                tc_fence_after();
+                if constexpr (!kChunkP) {
+                    // PV of the previous tile must be done: its P buffer is reused and O must be stable.
+                    if (j > 0) mbar_wait(&o_done[q], (gt - 1) & 1, wc);
+                    tc_fence_after();
+                }
                 // tcgen05.ld/st are warp-collective (.sync.aligned): rescale if any lane of the warp
                 // needs it (alpha = 1 for the others), never under a per-lane branch.
                 if (__any_sync(0xffffffffu, rescale) && j > 0) {
@@ -553,8 +569,10 @@ __global__ void __launch_bounds__(prefill_threads<RING>(), 1)
                     fence_proxy_async_smem();
                 }
                 __syncwarp();
+                if constexpr (!kChunkP) {
 #pragma unroll
-                for (int c = 0; c < kTN / 64; ++c) tmem_st32(tP + c * 32, pk + c * 32);
+                    for (int c = 0; c < kTN / 64; ++c) tmem_st32(tP + c * 32, pk + c * 32);
+                }
                 tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(&p_full[q]);
