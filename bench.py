@@ -31,8 +31,8 @@ METRIC = "decode KV GB/s and prefill TFLOP/s per GB300; fraction of HBM / tensor
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu capture of the
-# named kernel, with the sha256 of its source file at capture time; reported only while the
-# source is unchanged.
+# named kernel, with the sha256 of its source file and the shared device headers at capture time;
+# reported only while those sources are unchanged.
 TRAFFIC = {
     # decode B8 H32 Sq1 Skv4096 D128: read 537,100,544 + written 3,378,688 bytes
     # (profiles/decode_kernel_decode-B8-H32-Skv4096-D128.md)
@@ -125,9 +125,16 @@ def load_peaks():
     return FALLBACK_PEAKS, "fallback"
 
 
+# headers every kernel file includes: a change there changes the kernels too
+KERNEL_HEADERS = ("internal.h", "ptx.cuh", "nvfp4_dev.cuh")
+
+
 def source_sha(name: str) -> str:
-    p = os.path.join(ROOT, "attention_tensor_cores_gb300", "csrc", name)
-    return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
+    """sha256 (first 16 hex digits) of a kernel file followed by the shared device headers."""
+    h = hashlib.sha256()
+    for f in (name,) + KERNEL_HEADERS:
+        h.update(open(os.path.join(ROOT, "attention_tensor_cores_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
 
 
 def traffic_for(kernel: str, src: str, launches_per_step: int = 1):
