@@ -34,18 +34,18 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # named kernel, with the sha256 of its source file and the shared device headers at capture time;
 # reported only while those sources are unchanged.
 TRAFFIC = {
-    # decode B8 H32 Sq1 Skv4096 D128: read 537,100,544 + written 3,378,688 bytes
+    # decode B8 H32 Sq1 Skv4096 D128: read 537,138,688 + written 3,301,888 bytes
     # (profiles/decode_kernel_decode-B8-H32-Skv4096-D128.md)
-    "decode_kernel<128>": {"bytes": 540479232, "source_sha": "d9b1268a1cb1c68d"},
-    # ragged GQA decode B64 Hq32 Hkv8 Skv<=32768 D128: the quarter-size workload (B16) read 1,005,878,016 +
-    # wrote 368,384 bytes for 1,001,226,240 algorithmic K/V bytes (1.005x); scaled by the K/V bytes to the
+    "decode_kernel<128>": {"bytes": 540440576, "source_sha": "17f62e5631bfa11c"},
+    # ragged GQA decode B64 Hq32 Hkv8 Skv<=32768 D128: the quarter-size workload (B16) read 1,005,942,016 +
+    # wrote 333,056 bytes for 1,001,226,240 algorithmic K/V bytes (1.005x); scaled by the K/V bytes to the
     # full workload's 4,106,002,432 (profiles/side-kernels_ragged-decode-wide-combine-nvfp4.md)
-    "decode_kernel<128>/ragged": {"bytes": 4126589976, "source_sha": "d9b1268a1cb1c68d"},
-    # wide-head B32 Hq128 Hkv1 Skv16384 D512, independent CTAs: read 1,081,726,976 + written 10,267,392
+    "decode_kernel<128>/ragged": {"bytes": 4126707559, "source_sha": "17f62e5631bfa11c"},
+    # wide-head B32 Hq128 Hkv1 Skv16384 D512, independent CTAs: read 1,081,725,696 + written 10,418,688
     # bytes (profiles/wide_kernel_wide-head-B32-Hq128-Hkv1-Skv16384-D512.md)
-    "wide_kernel<independent>": {"bytes": 1091994368, "source_sha": "9c5cf7172015beea"},
-    # same workload, CTA-pair MMA: read 1,081,826,048 + written 10,286,592 bytes (same file)
-    "wide_kernel<pair>": {"bytes": 1092112640, "source_sha": "9c5cf7172015beea"},
+    "wide_kernel<independent>": {"bytes": 1092144384, "source_sha": "fc24eba4f080698b"},
+    # same workload, CTA-pair MMA: read 1,081,825,536 + written 10,624,512 bytes (same file)
+    "wide_kernel<pair>": {"bytes": 1092450048, "source_sha": "fc24eba4f080698b"},
 }
 
 
