@@ -23,9 +23,13 @@
 //    a normalised partial (O_i, lse_i) to slot u + c of the workspace and the combine kernel
 //    merges them: lse = log sum_i exp(lse_i), O = sum_i exp(lse_i - lse) O_i.  Ragged batches
 //    balance by construction.  With num_splits == 1 each CTA takes whole units instead.
-//  * Roles: warps 0-3 softmax/epilogue, warp 4 TMA producer, warp 5 MMA issuer.  Every wait is
-//    bounded; a timeout flips the CTA into a drain mode (no new TMA/MMA, loops run out) and sets
-//    the device status word.
+//  * Roles (decode_kernel<D, CAUSAL, EPI>): warps 0-3 softmax.  EPI (units of several query
+//    columns): warps 4-7 epilogue, warp 8 TMA producer, warp 9 MMA issuer, warps 10-11 only complete
+//    their warpgroup; at the end of a work item the softmax warps hand its accumulators to the
+//    epilogue warps (Tensor Memory, two buffers) and go on with the next item while the epilogue
+//    normalises, stores and merges.  !EPI (one column): warp 4 producer, warp 5 MMA, and the softmax
+//    warps run each item's short epilogue themselves.  Every wait is bounded; a timeout flips the
+//    CTA into a drain mode (no new TMA/MMA, loops run out) and sets the device status word.
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -40,7 +44,19 @@ namespace {
 
 constexpr int kTileKV = 128;    // keys per tile = MMA M
 constexpr int kN = 16;          // query rows per unit, padded (MMA N)
-constexpr int kThreads = 192;   // 4 softmax warps + producer + MMA
+// EPI: softmax, epilogue and control warpgroups (warps 0-3, 4-7, 8-11: producer 8, MMA 9); else the
+// softmax warps run each item's epilogue themselves and warps 4 and 5 are the producer and the MMA.
+template <bool EPI>
+constexpr int decode_threads() { return EPI ? 384 : 192; }
+template <bool EPI>
+constexpr int tma_warp() { return EPI ? 8 : 4; }
+template <bool EPI>
+constexpr int mma_warp() { return EPI ? 9 : 5; }
+// setmaxnreg split of the launch's 168 registers a thread: on each SM quarter one warp of each
+// warpgroup, 232 + 184 + 88 = 504 of its 512, and 128 * 504 = 384 * 168 in all
+constexpr uint32_t kRegsSm = 232, kRegsEpi = 184, kRegsCtl = 88;
+static_assert(128 * (kRegsSm + kRegsEpi + kRegsCtl) <= decode_threads<true>() * 168, "register split exceeds the launch allocation");
+static_assert(kRegsSm + kRegsEpi + kRegsCtl <= 512, "register split exceeds an SM quarter");
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleD = 8.0f;   // log2 units: a column's reference max moves only when exceeded by more
@@ -57,7 +73,7 @@ struct DecodeCfg {
     static constexpr int kOffV = kOffK + kStages * kKVBytes;
     static constexpr int kOffP = kOffV + kStages * kKVBytes;
     static constexpr int kSmemBytes = kOffP + 2 * kPBytes + 1024;   // + alignment slack
-    static constexpr uint32_t kTmemCols = 64;              // S[2] x 16, O[2] x 16
+    static constexpr uint32_t kTmemCols = 128;             // S[2] x 16, O[2] x 16, handoff[2] x 32
 };
 
 struct DecodeParams {
@@ -72,8 +88,6 @@ struct DecodeParams {
     const int32_t* prefix;   // [U+1] tile prefix (ragged split mode), else NULL
     int tiles_uniform;       // tiles per unit when prefix == NULL
     int split;               // 1 = stream-K partition, 0 = whole units per CTA
-    int pieces;              // split mode, uniform lengths: each unit cut into P / U (or one more) pieces, one
-                             // piece per CTA (one epilogue per CTA), instead of equal tile ranges
     // outputs
     void* out;               // BF16 or F32 [U*G][D] (NULL when writing FP32 staging only)
     int out_f32;             // 1: `out` is FP32
@@ -124,25 +138,6 @@ struct Sched {
         p = pp;
         cta = c;
         nctas = n;
-        if (p->split && p->pieces) {
-            // CTA c holds piece c - first(u) of unit u: units below r have k + 1 pieces, the others k
-            const int k = n / p->U, r = n % p->U;
-            int uu, piece, np;
-            if (c < r * (k + 1)) {
-                uu = c / (k + 1);
-                piece = c % (k + 1);
-                np = k + 1;
-            } else {
-                const int c2 = c - r * (k + 1);
-                uu = r + c2 / k;
-                piece = c2 % k;
-                np = k;
-            }
-            const long long Tu = p->tiles_uniform;
-            g = static_cast<long long>(uu) * Tu + (piece * Tu) / np;
-            g1 = static_cast<long long>(uu) * Tu + ((piece + 1) * Tu) / np;
-            return;
-        }
         if (p->split) {
             const long long T = p->prefix ? p->prefix[p->U] : static_cast<long long>(p->U) * p->tiles_uniform;
             g = (static_cast<long long>(c) * T) / n;
@@ -242,16 +237,6 @@ __device__ __forceinline__ float warp_sum(float v)
 // most cap) and returns how many there are; 0 for a unit without tiles.
 __device__ int unit_partial_slots(const DecodeParams& p, int u, int P, int* slots, int cap)
 {
-    if (p.pieces) {   // the CTAs holding unit u's pieces are consecutive; a piece may be empty
-        const int k = P / p.U, r = P % p.U;
-        const int np = u < r ? k + 1 : k;
-        const int c0 = u < r ? u * (k + 1) : r * (k + 1) + (u - r) * k;
-        const long long Tu = p.tiles_uniform;
-        int n = 0;
-        for (int i = 0; i < np && n < cap; ++i)
-            if ((i * Tu) / np != ((i + 1) * Tu) / np) slots[n++] = u + c0 + i;
-        return n;
-    }
     int tiles;
     long long Tu, T;
     if (p.prefix) {
@@ -274,8 +259,8 @@ __device__ int unit_partial_slots(const DecodeParams& p, int u, int P, int* slot
 
 constexpr int kMaxFixSlots = 512;
 
-template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int D, bool CAUSAL, bool EPI>
+__global__ void __launch_bounds__(decode_threads<EPI>(), 1)
     decode_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                   const __grid_constant__ CUtensorMap vmap, const __grid_constant__ DecodeParams p)
 {
@@ -286,6 +271,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     __shared__ uint64_t q_full[2], q_empty[2], k_full[S], k_empty[S], v_full[S], v_empty[S];
     __shared__ uint64_t s_full[2], s_empty[2], p_full[2], p_empty[2], o_full[2], o_empty[2], mma_done;
+    __shared__ uint64_t ep_full[2], ep_empty[2];   // softmax -> epilogue handoff
+    __shared__ float ep_m[2][kN];                  // the columns' reference maxima
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
     __shared__ float red_max[2][4][kN];
@@ -312,6 +299,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&p_empty[i], 1);
             mbar_init(&o_full[i], 1);
             mbar_init(&o_empty[i], 128);
+            mbar_init(&ep_full[i], 128);
+            mbar_init(&ep_empty[i], 128);
         }
         for (int i = 0; i < S; ++i) {
             mbar_init(&k_full[i], 1);
@@ -322,20 +311,196 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&mma_done, 1);
         fence_barrier_init();
     }
-    if (warp == 5) {
+    if (warp == mma_warp<EPI>()) {
         tmem_alloc(&tmem_slot, C::kTmemCols);
         tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = tmem_slot;   // S buffers at columns 0/16, O buffers at 32/48
+    const uint32_t tmem = tmem_slot;   // S buffers at columns 0/16, O buffers at 32/48, handoff at 64/96
 
     Sched sched;
     sched.init(&p, blockIdx.x, gridDim.x);
     Item it;
 
-    if (warp == 4) {
+    // The epilogue of one item, run by 128 threads: the epilogue warpgroup (named barrier 2) when a
+    // unit has several query columns, else the softmax warps themselves (barrier 1), for which the
+    // epilogue is short and an extra warpgroup's handoff measured slower.  tid: O^T row (Tensor
+    // Memory lane) and output column, ew: warp within the group.
+    auto run_epilogue = [&](const Item& it, bool empty, const float (&m)[kN], const float (&l)[kN],
+                            const float (&acc)[kN], int tid, int ew, int bar) {
+        const int lane = static_cast<int>(lane_id());
+        const int G = p.G;
+        const float nv_sg = p.nv_sg ? *p.nv_sg : 0.f;
+        // final output of one row at column tid (tid < D); the |O| max goes to amax_acc
+        auto write_final = [&](size_t row, float o, float lse_v, float& amax_acc) {
+            if (p.o_stage) p.o_stage[row * D + tid] = o;
+            if (p.amax_bits) amax_acc = fmaxf(amax_acc, fabsf(o));
+            if (p.out) {
+                if (p.out_f32)
+                    static_cast<float*>(p.out)[row * D + tid] = o;
+                else
+                    static_cast<uint16_t*>(p.out)[row * D + tid] = float_to_bf16_bits(o);
+            }
+            if (tid == 0 && p.lse) p.lse[row] = lse_v;
+        };
+        // ---- epilogue: L = sum over the 128 key lanes, O = acc · (1 / L), lse = ln2 * (m + log2 L)
+        if (!empty) {
+            if (G == 1) {
+                const float s = warp_sum(l[0]);
+                if (lane == 0) red_sum[ew][0] = s;
+            } else {
+                // all columns' butterflies interleaved: five rounds of independent shuffles
+                float v[kN];
+#pragma unroll
+                for (int q = 0; q < kN; ++q) v[q] = q < G ? l[q] : 0.f;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+                    for (int q = 0; q < kN; ++q) v[q] += __shfl_xor_sync(0xffffffffu, v[q], o);
+                if (lane == 0)
+#pragma unroll
+                    for (int q = 0; q < kN; ++q)
+                        if (q < G) red_sum[ew][q] = v[q];
+            }
+        }
+        // red_sum is complete, and every thread is past its reads of the previous item's
+        // col_inv / col_lse (an empty item has no tile barriers in between)
+        named_bar_sync(bar, 128);
+        // one thread per column: L, then 1 / L and the LSE for every thread of the CTA
+        if (tid < G) {
+            const float Lq = empty ? 0.f : (red_sum[0][tid] + red_sum[1][tid]) + (red_sum[2][tid] + red_sum[3][tid]);
+            float mq = m[0];
+#pragma unroll
+            for (int q = 1; q < kN; ++q)
+                if (q == tid) mq = m[q];
+            const bool none = !(Lq > 0.f);   // no visible key in this range
+            col_inv[tid] = none ? 0.f : 1.f / Lq;
+            col_lse[tid] = none ? -INFINITY : (mq + __log2f(Lq)) * kLn2;
+        }
+        // one abort decision for all four warps (named barriers and shuffles below)
+        if (tid == 0) ep_abort = aborted(wc) ? 1 : 0;
+        named_bar_sync(bar, 128);
+        if (ep_abort) return;
+        // single-pass NVFP4 in split mode: whole units also go through the combine, which
+        // encodes every row in parallel (encoding here would lengthen the CTAs holding many
+        // short units)
+        const bool final_here = it.whole && !(p.split && p.nv_codes);
+        float local_amax = 0.f;
+        if (tid < D) {
+#pragma unroll
+            for (int q = 0; q < kN; ++q) {
+                if (q >= G) break;
+                const float o = col_inv[q] > 0.f ? acc[q] * col_inv[q] : 0.f;   // 0: no visible key in this range
+                const float lse_v = col_lse[q];
+                const size_t row = static_cast<size_t>(it.u) * G + q;
+                if (final_here) {
+                    write_final(row, o, lse_v, local_amax);
+                    // single-pass NVFP4: a warp holds 32 consecutive columns of the row
+                    if (p.nv_codes) nvfp4_encode_lanes(o, nv_sg, tid, p.nv_codes + row * (D / 2), p.nv_scales + row * (D / 16));
+                } else {
+                    p.part_o[(static_cast<size_t>(it.slot) * kN + q) * D + tid] = o;
+                    if (tid == 0) p.part_lse[static_cast<size_t>(it.slot) * kN + q] = lse_v;
+                }
+            }
+        }
+        if (p.amax_bits && final_here) {
+            const float wm = warp_max(local_amax);
+            if (lane == 0 && wm > 0.f) atomicMax(p.amax_bits, __float_as_uint(wm));
+        }
+        if (p.fixup && !final_here) {
+            // stream-K fixup: publish this partial, count the unit's arrivals, and let the CTA
+            // that completes the unit merge it (O = sum exp(lse_i - lse) O_i, as the combine).
+            // The CTA barrier orders every thread's partial stores before thread 0's device-scope
+            // fence, which releases them all (release is cumulative) ahead of its arrival: one
+            // fence waits for the stores instead of 128.
+            named_bar_sync(bar, 128);
+            if (tid == 0) {
+                const int n = unit_partial_slots(p, it.u, static_cast<int>(gridDim.x), fx_slot, kMaxFixSlots);
+                fx_n = n;
+                __threadfence();
+                const int arrived = n > 0 ? arrive_unit(p.unit_ctr + it.u, p.gen, n) : 0;
+                // -1: the counter kept changing under us (another call on this workspace):
+                // the unit may stay unmerged, so say so instead of failing silently
+                if (arrived < 0) atomicExch(p.status, kDevMergeLost);
+                fx_last = (arrived == n && n > 0) ? 1 : 0;
+            }
+            named_bar_sync(bar, 128);
+            if (fx_last) {
+                __threadfence();
+                const int ns = fx_n;
+                float amax_m = 0.f;
+                if (ns <= 4) {
+                    // the usual case: this thread's element of every partial O of every column, and
+                    // (threads q < G) column q's partial LSEs, all in flight at once, so the merge
+                    // costs one L2 round trip whatever the number of columns (a round per few
+                    // columns was one dependent trip each, slow while the other CTAs stream)
+                    float ov[kN][4];
+#pragma unroll
+                    for (int q = 0; q < kN; ++q)
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const bool use = q < G && i < ns && tid < D;
+                            ov[q][i] = use ? __ldcg(p.part_o + (static_cast<size_t>(fx_slot[i < ns ? i : 0]) * kN + q) * D + tid) : 0.f;
+                        }
+                    if (tid < G) {
+                        float lv[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            lv[i] = i < ns ? __ldcg(p.part_lse + static_cast<size_t>(fx_slot[i]) * kN + tid) : -INFINITY;
+                        const float mx = fmaxf(fmaxf(lv[0], lv[1]), fmaxf(lv[2], lv[3]));
+                        const bool any = mx > -INFINITY;   // partials without a visible key carry -inf
+                        float sum = 0.f;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) sum += (any && i < ns) ? __expf(lv[i] - mx) : 0.f;
+                        const float lse_all = any ? mx + __logf(sum) : -INFINITY;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) fx_w[tid][i] = (any && i < ns) ? __expf(lv[i] - lse_all) : 0.f;
+                        fx_lse[tid] = lse_all;
+                    }
+                    named_bar_sync(bar, 128);
+#pragma unroll
+                    for (int q = 0; q < kN; ++q) {
+                        if (q >= G) break;
+                        float o = 0.f;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) o = fmaf(fx_w[q][i], ov[q][i], o);
+                        if (tid < D) write_final(static_cast<size_t>(it.u) * G + q, o, fx_lse[q], amax_m);
+                    }
+                } else {
+                    for (int q = 0; q < G; ++q) {
+                        float mx = -INFINITY;
+                        for (int i = 0; i < ns; ++i) mx = fmaxf(mx, __ldcg(p.part_lse + static_cast<size_t>(fx_slot[i]) * kN + q));
+                        // partials without a visible key carry lse = -inf and weigh 0; all of them -> empty row
+                        const bool any = mx > -INFINITY;
+                        float sum = 0.f;
+                        if (any)
+                            for (int i = 0; i < ns; ++i) sum += __expf(__ldcg(p.part_lse + static_cast<size_t>(fx_slot[i]) * kN + q) - mx);
+                        const float lse_all = (ns > 0 && any) ? mx + __logf(sum) : -INFINITY;
+                        if (tid < D) {
+                            float o = 0.f;
+                            if (any)
+                                for (int i = 0; i < ns; ++i) {
+                                    const size_t sl = static_cast<size_t>(fx_slot[i]) * kN + q;
+                                    o = fmaf(__expf(__ldcg(p.part_lse + sl) - lse_all), __ldcg(p.part_o + sl * D + tid), o);
+                                }
+                            write_final(static_cast<size_t>(it.u) * G + q, o, lse_all, amax_m);
+                        }
+                    }
+                }
+                if (p.amax_bits) {
+                    const float wm = warp_max(amax_m);
+                    if (lane == 0 && wm > 0.f) atomicMax(p.amax_bits, __float_as_uint(wm));
+                }
+            }
+        }
+    };
+
+    // Each setmaxnreg dominates only its own role's code and is executed by whole warpgroups.
+    if (warp >= tma_warp<EPI>()) {
+        if constexpr (EPI) setmaxnreg_dec<kRegsCtl>();
+      if (warp == tma_warp<EPI>()) {
         // ------------------------------------------------ TMA producer
         if (lane_id() == 0) {
             tma_prefetch_desc(&qmap);
@@ -387,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 2; ++i)
                 if (qcnt[i]) drain_wait(&q_full[i], (qcnt[i] - 1) & 1, kDrainLimit);
         }
-    } else if (warp == 5) {
+      } else if (warp == mma_warp<EPI>()) {
         // ------------------------------------------------ MMA issuer
         if (lane_id() == 0) {
             constexpr uint32_t idesc_qk = idesc_bf16_f32(128, kN, false, false);
@@ -448,26 +613,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(&mma_done);
             drain_wait(&mma_done, 0, kDrainLimit);
         }
-    } else {
-        // ------------------------------------------------ softmax / correction / epilogue (128 threads)
+      }
+    } else if (warp < 4) {
+        if constexpr (EPI) setmaxnreg_inc<kRegsSm>();
+        // ------------------------------------------------ softmax / correction (128 threads)
         const int tid = threadIdx.x;
         const int lane = static_cast<int>(lane_id());
         const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
         const int G = p.G;
-        const float nv_sg = p.nv_sg ? *p.nv_sg : 0.f;
-        // final output of one row at column tid (tid < D); the |O| max goes to amax_acc
-        auto write_final = [&](size_t row, float o, float lse_v, float& amax_acc) {
-            if (p.o_stage) p.o_stage[row * D + tid] = o;
-            if (p.amax_bits) amax_acc = fmaxf(amax_acc, fabsf(o));
-            if (p.out) {
-                if (p.out_f32)
-                    static_cast<float*>(p.out)[row * D + tid] = o;
-                else
-                    static_cast<uint16_t*>(p.out)[row * D + tid] = float_to_bf16_bits(o);
-            }
-            if (tid == 0 && p.lse) p.lse[row] = lse_v;
-        };
-        Ring sr(2), pr(2), orr(2), vr(S);
+        Ring sr(2), pr(2), orr(2), vr(S), hr(2);
         uint32_t tile_ctr = 0;
         while (sched.next(it)) {
             float m[kN], l[kN], acc[kN], alpha_prev[kN];
@@ -581,163 +735,72 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (it.t1 > it.t0) consume(alpha_prev);
 
-            // ---- epilogue: L = sum over the 128 key lanes, O = acc · (1 / L), lse = ln2 * (m + log2 L)
-            const bool empty = it.t1 <= it.t0;
-            if (!empty) {
-                if (G == 1) {
-                    const float s = warp_sum(l[0]);
-                    if (lane == 0) red_sum[warp][0] = s;
-                } else {
-                    // all columns' butterflies interleaved: five rounds of independent shuffles
-                    float v[kN];
-#pragma unroll
-                    for (int q = 0; q < kN; ++q) v[q] = q < G ? l[q] : 0.f;
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-                        for (int q = 0; q < kN; ++q) v[q] += __shfl_xor_sync(0xffffffffu, v[q], o);
-                    if (lane == 0)
-#pragma unroll
-                        for (int q = 0; q < kN; ++q)
-                            if (q < G) red_sum[warp][q] = v[q];
-                }
+            if constexpr (!EPI) {
+                run_epilogue(it, it.t1 <= it.t0, m, l, acc, tid, warp, 1);
+                continue;
             }
-            // red_sum is complete, and every thread is past its reads of the previous item's
-            // col_inv / col_lse (an empty item has no tile barriers in between)
-            named_bar_sync(1, 128);
-            // one thread per column: L, then 1 / L and the LSE for every thread of the CTA
-            if (tid < G) {
-                const float Lq = empty ? 0.f : (red_sum[0][tid] + red_sum[1][tid]) + (red_sum[2][tid] + red_sum[3][tid]);
-                float mq = m[0];
-#pragma unroll
-                for (int q = 1; q < kN; ++q)
-                    if (q == tid) mq = m[q];
-                const bool none = !(Lq > 0.f);   // no visible key in this range
-                col_inv[tid] = none ? 0.f : 1.f / Lq;
-                col_lse[tid] = none ? -INFINITY : (mq + __log2f(Lq)) * kLn2;
-            }
-            // one abort decision for all four warps (named barriers and shuffles below)
-            if (tid == 0) ep_abort = aborted(wc) ? 1 : 0;
-            named_bar_sync(1, 128);
-            if (ep_abort) continue;
-            // single-pass NVFP4 in split mode: whole units also go through the combine, which
-            // encodes every row in parallel (encoding here would lengthen the CTAs holding many
-            // short units)
-            const bool final_here = it.whole && !(p.split && p.nv_codes);
-            float local_amax = 0.f;
-            if (tid < D) {
+            // ---- hand the item to the epilogue warpgroup: acc and the partial column sums l through
+            // Tensor Memory (lane tid), the reference maxima through shared memory; the softmax goes
+            // on with the next item meanwhile.  Both sides walk the same item sequence and take part
+            // in every handoff whatever their waits return (a timeout only drains).
+            {
+                mbar_wait(&ep_empty[hr.idx], hr.phase ^ 1, wc);
+                tc_fence_after();
+                __syncwarp();   // tcgen05.st is warp-collective
+                uint32_t hv[32];
 #pragma unroll
                 for (int q = 0; q < kN; ++q) {
-                    if (q >= G) break;
-                    const float o = col_inv[q] > 0.f ? acc[q] * col_inv[q] : 0.f;   // 0: no visible key in this range
-                    const float lse_v = col_lse[q];
-                    const size_t row = static_cast<size_t>(it.u) * G + q;
-                    if (final_here) {
-                        write_final(row, o, lse_v, local_amax);
-                        // single-pass NVFP4: a warp holds 32 consecutive columns of the row
-                        if (p.nv_codes) nvfp4_encode_lanes(o, nv_sg, tid, p.nv_codes + row * (D / 2), p.nv_scales + row * (D / 16));
-                    } else {
-                        p.part_o[(static_cast<size_t>(it.slot) * kN + q) * D + tid] = o;
-                        if (tid == 0) p.part_lse[static_cast<size_t>(it.slot) * kN + q] = lse_v;
-                    }
+                    hv[q] = __float_as_uint(acc[q]);
+                    hv[kN + q] = __float_as_uint(l[q]);
                 }
+                tmem_st32(tmem + lane_base + 64 + hr.idx * 32, hv);
+                tmem_st_wait();
+                if (tid == 0)
+#pragma unroll
+                    for (int q = 0; q < kN; ++q) ep_m[hr.idx][q] = m[q];
+                tc_fence_before();
+                mbar_arrive(&ep_full[hr.idx]);
             }
-            if (p.amax_bits && final_here) {
-                const float wm = warp_max(local_amax);
-                if (lane == 0 && wm > 0.f) atomicMax(p.amax_bits, __float_as_uint(wm));
-            }
-            if (p.fixup && !final_here) {
-                // stream-K fixup: publish this partial, count the unit's arrivals, and let the CTA
-                // that completes the unit merge it (O = sum exp(lse_i - lse) O_i, as the combine).
-                // The CTA barrier orders every thread's partial stores before thread 0's device-scope
-                // fence, which releases them all (release is cumulative) ahead of its arrival: one
-                // fence waits for the stores instead of 128.
-                named_bar_sync(1, 128);
-                if (tid == 0) {
-                    const int n = unit_partial_slots(p, it.u, static_cast<int>(gridDim.x), fx_slot, kMaxFixSlots);
-                    fx_n = n;
-                    __threadfence();
-                    const int arrived = n > 0 ? arrive_unit(p.unit_ctr + it.u, p.gen, n) : 0;
-                    // -1: the counter kept changing under us (another call on this workspace):
-                    // the unit may stay unmerged, so say so instead of failing silently
-                    if (arrived < 0) atomicExch(p.status, kDevMergeLost);
-                    fx_last = (arrived == n && n > 0) ? 1 : 0;
-                }
-                named_bar_sync(1, 128);
-                if (fx_last) {
-                    __threadfence();
-                    const int ns = fx_n;
-                    float amax_m = 0.f;
-                    if (ns <= 4) {
-                        // the usual case: this thread's element of every partial O of every column, and
-                        // (threads q < G) column q's partial LSEs, all in flight at once, so the merge
-                        // costs one L2 round trip whatever the number of columns (a round per few
-                        // columns was one dependent trip each, slow while the other CTAs stream)
-                        float ov[kN][4];
-#pragma unroll
-                        for (int q = 0; q < kN; ++q)
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                const bool use = q < G && i < ns && tid < D;
-                                ov[q][i] = use ? __ldcg(p.part_o + (static_cast<size_t>(fx_slot[i < ns ? i : 0]) * kN + q) * D + tid) : 0.f;
-                            }
-                        if (tid < G) {
-                            float lv[4];
-#pragma unroll
-                            for (int i = 0; i < 4; ++i)
-                                lv[i] = i < ns ? __ldcg(p.part_lse + static_cast<size_t>(fx_slot[i]) * kN + tid) : -INFINITY;
-                            const float mx = fmaxf(fmaxf(lv[0], lv[1]), fmaxf(lv[2], lv[3]));
-                            const bool any = mx > -INFINITY;   // partials without a visible key carry -inf
-                            float sum = 0.f;
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) sum += (any && i < ns) ? __expf(lv[i] - mx) : 0.f;
-                            const float lse_all = any ? mx + __logf(sum) : -INFINITY;
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) fx_w[tid][i] = (any && i < ns) ? __expf(lv[i] - lse_all) : 0.f;
-                            fx_lse[tid] = lse_all;
-                        }
-                        named_bar_sync(1, 128);
-#pragma unroll
-                        for (int q = 0; q < kN; ++q) {
-                            if (q >= G) break;
-                            float o = 0.f;
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) o = fmaf(fx_w[q][i], ov[q][i], o);
-                            if (tid < D) write_final(static_cast<size_t>(it.u) * G + q, o, fx_lse[q], amax_m);
-                        }
-                    } else {
-                        for (int q = 0; q < G; ++q) {
-                            float mx = -INFINITY;
-                            for (int i = 0; i < ns; ++i) mx = fmaxf(mx, __ldcg(p.part_lse + static_cast<size_t>(fx_slot[i]) * kN + q));
-                            // partials without a visible key carry lse = -inf and weigh 0; all of them -> empty row
-                            const bool any = mx > -INFINITY;
-                            float sum = 0.f;
-                            if (any)
-                                for (int i = 0; i < ns; ++i) sum += __expf(__ldcg(p.part_lse + static_cast<size_t>(fx_slot[i]) * kN + q) - mx);
-                            const float lse_all = (ns > 0 && any) ? mx + __logf(sum) : -INFINITY;
-                            if (tid < D) {
-                                float o = 0.f;
-                                if (any)
-                                    for (int i = 0; i < ns; ++i) {
-                                        const size_t sl = static_cast<size_t>(fx_slot[i]) * kN + q;
-                                        o = fmaf(__expf(__ldcg(p.part_lse + sl) - lse_all), __ldcg(p.part_o + sl * D + tid), o);
-                                    }
-                                write_final(static_cast<size_t>(it.u) * G + q, o, lse_all, amax_m);
-                            }
-                        }
-                    }
-                    if (p.amax_bits) {
-                        const float wm = warp_max(amax_m);
-                        if (lane == 0 && wm > 0.f) atomicMax(p.amax_bits, __float_as_uint(wm));
-                    }
-                }
-            }
+            hr.advance();
         }
+    } else {
+      if constexpr (EPI) {
+        setmaxnreg_inc<kRegsEpi>();
+        // ------------------------------------------------ epilogue (128 threads): the items the softmax
+        // warpgroup hands over, in order; thread tid owns O^T row tid (Tensor Memory lane tid)
+        const int tid = threadIdx.x - 128;
+        const int ew = warp - 4;
+        const uint32_t lane_base = static_cast<uint32_t>(ew * 32) << 16;
+        Ring hr(2);
+        while (sched.next(it)) {   // the softmax warpgroup's sequence of items
+            mbar_wait(&ep_full[hr.idx], hr.phase, wc);
+            tc_fence_after();
+            __syncwarp();   // tcgen05.ld is warp-collective
+            const bool empty = it.t1 <= it.t0;
+            float m[kN], l[kN], acc[kN];
+            {
+                uint32_t hv[32];
+                tmem_ld32(tmem + lane_base + 64 + hr.idx * 32, hv);
+                tmem_ld_wait();
+#pragma unroll
+                for (int q = 0; q < kN; ++q) {
+                    acc[q] = __uint_as_float(hv[q]);
+                    l[q] = __uint_as_float(hv[kN + q]);
+                    m[q] = ep_m[hr.idx][q];
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&ep_empty[hr.idx]);
+            hr.advance();
+
+            run_epilogue(it, empty, m, l, acc, tid, ew, 2);
+        }
+      }
     }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) tmem_dealloc(tmem, C::kTmemCols);
+    if (warp == mma_warp<EPI>()) tmem_dealloc(tmem, C::kTmemCols);
 }
 
 // Exclusive prefix of per-unit tile counts (ragged keys), one block.
@@ -947,10 +1010,6 @@ int run_decode(const AttnArgs& a, bool split, void* ws, cudaStream_t st)
     // combine launch).  Measured slower for ragged batches, which keep the combine kernel (it also
     // writes units without keys); single-pass NVFP4 keeps it too (one block per row encodes).
     p.fixup = (split && !a.nv_sg && !a.seqlens && nsm <= kMaxFixSlots) ? 1 : 0;
-    // Many query columns per unit make a split epilogue (partial store, arrival, merge) cost several
-    // tiles' time; when every unit can have two or more CTAs, one piece per CTA bounds each CTA to one
-    // epilogue (equal tile ranges give some CTAs the end of one unit and the start of the next).
-    p.pieces = (p.fixup && G >= 8 && 2 * U <= nsm && p.tiles_uniform >= 2 * (nsm / U + 1)) ? 1 : 0;
     p.unit_ctr = split ? reinterpret_cast<unsigned long long*>(base + w.ctr_off) : nullptr;
     p.gen = next_call_tag();
     p.status = device_status_ptr();
@@ -961,11 +1020,20 @@ int run_decode(const AttnArgs& a, bool split, void* ws, cudaStream_t st)
         FMHA_CHECK_LAUNCH("tile_prefix_kernel");
         count_launch();
     }
-    FMHA_CHECK_CUDA(set_smem_limit_once(reinterpret_cast<const void*>(decode_kernel<D, CAUSAL>), C::kSmemBytes));
+    // The epilogue warpgroup takes each item's epilogue off the softmax warps when a unit has several
+    // query columns (publishing a 16-column partial costs several tiles' streaming time); with one
+    // column the epilogue is short and the six-warp kernel, whose softmax warps run it, measured faster.
+    const bool epi = G > 1;
+    const void* fn = epi ? reinterpret_cast<const void*>(decode_kernel<D, CAUSAL, true>)
+                         : reinterpret_cast<const void*>(decode_kernel<D, CAUSAL, false>);
+    FMHA_CHECK_CUDA(set_smem_limit_once(fn, C::kSmemBytes));
     const int grid = split ? nsm : (U < nsm ? U : nsm);
     if (grid > 0) {
         timing_mark_begin(st);
-        decode_kernel<D, CAUSAL><<<grid, kThreads, C::kSmemBytes, st>>>(qmap, kmap, vmap, p);
+        if (epi)
+            decode_kernel<D, CAUSAL, true><<<grid, decode_threads<true>(), C::kSmemBytes, st>>>(qmap, kmap, vmap, p);
+        else
+            decode_kernel<D, CAUSAL, false><<<grid, decode_threads<false>(), C::kSmemBytes, st>>>(qmap, kmap, vmap, p);
         timing_mark_end(st);
         FMHA_CHECK_LAUNCH("decode_kernel");
         count_launch();

@@ -144,8 +144,10 @@ def test_chunked_prefill_ragged_causal_d128(F, num_splits):
 
 def test_speculative_decode_full_size_every_row(F):
     """B8 Hq32 Hkv8 Sq4 Skv8192 D128, causal (16 query columns per key/value head): every one of the
-    1024 rows against the oracle.  64 units for 152 or so CTAs: each unit is cut into two or three
-    pieces, one per CTA, merged in the kernel by the CTA that completes the unit."""
+    1024 rows against the oracle.  64 units for 152 or so CTAs: the stream-K split gives each CTA
+    about 27 of the 4096 key tiles, so units are cut into two or three parts and many CTAs end one
+    unit and start the next (their first epilogue runs on the epilogue warps while the next unit
+    streams); the CTA that completes a unit merges it."""
     w = inputs.Workload("speculative decode", 8, 32, 8, 4, 8192, 128, 1.0, "bf16", 1006)
     q, k, v, _ = w.make("cuda")
     res = run_attention(F, q, k, v, w.scale, num_splits=0, causal=True)
