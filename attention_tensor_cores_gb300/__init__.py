@@ -83,6 +83,8 @@ def load(path: str | None = None):
             "fmha_fwd": ([V, V, V, V, V, I, I, I, I, I, I, F, V], I),
             "fmha_fwd_ex": ([V, V, V, V, V, I, I, I, I, I, I, F, V, ctypes.POINTER(fmha_opts)], I),
             "fmha_workspace_size": ([I, I, I, I, I, I, ctypes.POINTER(fmha_opts)], S),
+            "fmha_fwd_host": ([V, V, V, V, V, I, I, I, I, I, I, F, V, ctypes.POINTER(fmha_opts), V, S], I),
+            "fmha_host_buffer_size": ([I, I, I, I, I, I, ctypes.POINTER(fmha_opts)], S),
             "nvfp4_quantize": ([V, V, V, I64, V], I),
             "nvfp4_quantize_scaled": ([V, V, V, I64, V, V], I),
             "nvfp4_scales_bytes": ([I64], S),
@@ -181,6 +183,26 @@ def fmha_fwd_ex(q, k, v, out, lse, scale: float, opts: fmha_opts | None = None, 
     rc = load().fmha_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Sq, Skv, D,
                             float(scale), _stream(stream), None if opts is None else ctypes.byref(opts))
     _check(rc, "fmha_fwd_ex")
+
+
+def fmha_host_buffer_size(B, Hq, Hkv, Sq, Skv, D, opts: fmha_opts | None = None) -> int:
+    return int(load().fmha_host_buffer_size(B, Hq, Hkv, Sq, Skv, D, None if opts is None else ctypes.byref(opts)))
+
+
+def fmha_fwd_host(q, k, v, out, lse, scale: float, dev_buf, opts: fmha_opts | None = None, stream=None):
+    """Attention from host memory: q/k/v/out/lse are CPU tensors (page-locked for asynchronous copies,
+    lse may be None), dev_buf a CUDA byte tensor of at least fmha_host_buffer_size() bytes.  Returns
+    once enqueued on `stream`; synchronise before reading out / lse."""
+    for t in (q, k, v, out, lse):
+        if t is not None and (t.is_cuda or not t.is_contiguous()):
+            raise FmhaError(FMHA_ERR_INVALID, "q/k/v/out/lse must be contiguous host tensors")
+    _need_cuda(dev_buf)
+    B, Hq, Sq, D = q.shape
+    Hkv, Skv = k.shape[1], k.shape[2]
+    rc = load().fmha_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Sq, Skv, D, float(scale),
+                              _stream(stream), None if opts is None else ctypes.byref(opts), _ptr(dev_buf),
+                              dev_buf.numel() * dev_buf.element_size())
+    _check(rc, "fmha_fwd_host")
 
 
 def nvfp4_scales_bytes(n: int) -> int:

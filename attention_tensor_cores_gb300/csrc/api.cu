@@ -384,6 +384,143 @@ int fmha_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
     return fmha_fwd_ex(q, k, v, out, lse, B, Hq, Hkv, Sq, Skv, D, scale, stream, nullptr);
 }
 
+// ---- attention from host memory ----------------------------------------------------------------------------
+// dev_buf: staged Q | K | V | O | LSE | attention workspace (sized for the largest batch chunk).
+struct HostLayout {
+    size_t q, k, v, o, lse, ws, ws_bytes, total;
+    int chunks, bc;   // batch chunks and entries per chunk (the last chunk may have fewer)
+};
+
+static fmha_opts host_call_opts(const fmha_opts* o)
+{
+    fmha_opts w{};
+    w.out_kind = o ? o->out_kind : FMHA_OUT_BF16;
+    w.num_splits = o ? o->num_splits : 0;
+    w.causal = o ? o->causal : 0;
+    w.wide_variant = o ? o->wide_variant : FMHA_WIDE_AUTO;
+    return w;
+}
+
+static HostLayout host_layout(int B, int Hq, int Hkv, int Sq, int Skv, int D, const fmha_opts* o)
+{
+    HostLayout L{};
+    const size_t esz = (o && o->out_kind == FMHA_OUT_F32) ? 4 : 2;
+    const size_t nq = static_cast<size_t>(B) * Hq * Sq * D, nkv = static_cast<size_t>(B) * Hkv * Skv * D;
+    const int want = B >= 2 ? (B < 4 ? B : 4) : 1;
+    L.bc = B > 0 ? (B + want - 1) / want : 0;
+    L.chunks = B > 0 ? (B + L.bc - 1) / L.bc : 0;
+    size_t off = 0;
+    L.q = off;
+    off += align256(nq * 2);
+    L.k = off;
+    off += align256(nkv * 2);
+    L.v = off;
+    off += align256(nkv * 2);
+    L.o = off;
+    off += align256(nq * esz);
+    L.lse = off;
+    off += align256(static_cast<size_t>(B) * Hq * Sq * 4);
+    const fmha_opts w = host_call_opts(o);
+    L.ws_bytes = L.bc > 0 ? fmha_workspace_size(L.bc, Hq, Hkv, Sq, Skv, D, &w) : 0;
+    L.ws = off;
+    off += align256(L.ws_bytes);
+    L.total = off;
+    return L;
+}
+
+// Per device: the copy stream and events of chunked host calls (created once, kept for the
+// library's lifetime) and the lock that keeps one host thread enqueuing at a time.
+struct HostAux {
+    cudaStream_t cs;
+    cudaEvent_t start, copied[4];
+    bool ready;
+};
+static HostAux g_host_aux[kMaxDevices];
+static std::mutex g_host_mu;
+
+static HostAux* host_aux()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    HostAux& h = g_host_aux[dev];
+    if (!h.ready) {
+        if (cudaStreamCreateWithFlags(&h.cs, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
+        bool ok = cudaEventCreateWithFlags(&h.start, cudaEventDisableTiming) == cudaSuccess;
+        for (int i = 0; i < 4 && ok; ++i) ok = cudaEventCreateWithFlags(&h.copied[i], cudaEventDisableTiming) == cudaSuccess;
+        if (!ok) return nullptr;
+        h.ready = true;
+    }
+    return &h;
+}
+
+size_t fmha_host_buffer_size(int B, int Hq, int Hkv, int Sq, int Skv, int D, const fmha_opts* opts)
+{
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Sq < 0 || Skv <= 0 || Hq % Hkv) return 0;
+    return host_layout(B, Hq, Hkv, Sq, Skv, D, opts).total;
+}
+
+int fmha_fwd_host(const void* q_host, const void* k_host, const void* v_host, void* out_host, float* lse_host, int B,
+                  int Hq, int Hkv, int Sq, int Skv, int D, float scale, fmha_stream_t stream, const fmha_opts* opts,
+                  void* dev_buf, size_t dev_buf_bytes)
+{
+    if (!q_host || !k_host || !v_host || !out_host) return set_error(FMHA_ERR_INVALID, "fmha_fwd_host: NULL host pointer");
+    if (opts && (opts->seqlens_k || opts->out_kind == FMHA_OUT_NVFP4 || opts->out_scales || opts->out_tensor_scale ||
+                 opts->out_f32 || opts->nvfp4_scale_in || opts->out_amax || opts->workspace || opts->workspace_bytes))
+        return set_error(FMHA_ERR_UNSUPPORTED,
+                         "fmha_fwd_host: options limited to out_kind (BF16/F32), num_splits, causal and wide_variant");
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Sq < 0 || Skv <= 0 || Hq % Hkv)
+        return set_error(FMHA_ERR_INVALID, "need B >= 0, Hq > 0, Hkv > 0 dividing Hq, Sq >= 0, Skv >= 1");
+    const HostLayout L = host_layout(B, Hq, Hkv, Sq, Skv, D, opts);
+    if (!dev_buf || (reinterpret_cast<uintptr_t>(dev_buf) & 255) || dev_buf_bytes < L.total)
+        return set_error(FMHA_ERR_WORKSPACE, "fmha_fwd_host: dev_buf missing, not 256-byte aligned or smaller than fmha_host_buffer_size()");
+    uint8_t* base = static_cast<uint8_t*>(dev_buf);
+    fmha_opts w = host_call_opts(opts);
+    int rc = validate(base + L.q, base + L.k, base + L.v, base + L.o, B, Hq, Hkv, Sq, Skv, D, scale, &w);
+    if (rc) return rc;
+    if (!device_status_ptr()) return set_error(FMHA_ERR_CUDA, "no CUDA device");
+    if (static_cast<long long>(B) * Hq * Sq == 0) return FMHA_OK;
+    w.workspace = L.ws_bytes ? base + L.ws : nullptr;
+    w.workspace_bytes = L.ws_bytes;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const size_t esz = w.out_kind == FMHA_OUT_F32 ? 4 : 2;
+    const size_t qb = static_cast<size_t>(Hq) * Sq * D * 2, kvb = static_cast<size_t>(Hkv) * Skv * D * 2;
+    const size_t ob = static_cast<size_t>(Hq) * Sq * D * esz, lb = static_cast<size_t>(Hq) * Sq * 4;
+
+    std::lock_guard<std::mutex> lock(g_host_mu);
+    HostAux* aux = nullptr;
+    if (L.chunks > 1) {
+        aux = host_aux();
+        if (!aux) return set_error(FMHA_ERR_CUDA, "fmha_fwd_host: cannot create the copy stream");
+        // the copies must not overwrite staging that earlier work on `stream` still reads
+        FMHA_CHECK_CUDA(cudaEventRecord(aux->start, st));
+        FMHA_CHECK_CUDA(cudaStreamWaitEvent(aux->cs, aux->start, 0));
+    }
+    const auto* qh = static_cast<const uint8_t*>(q_host);
+    const auto* kh = static_cast<const uint8_t*>(k_host);
+    const auto* vh = static_cast<const uint8_t*>(v_host);
+    for (int c = 0; c < L.chunks; ++c) {
+        const int b0 = c * L.bc, nb = (B - b0 < L.bc) ? B - b0 : L.bc;
+        cudaStream_t cs = aux ? aux->cs : st;
+        FMHA_CHECK_CUDA(cudaMemcpyAsync(base + L.q + b0 * qb, qh + b0 * qb, nb * qb, cudaMemcpyHostToDevice, cs));
+        FMHA_CHECK_CUDA(cudaMemcpyAsync(base + L.k + b0 * kvb, kh + b0 * kvb, nb * kvb, cudaMemcpyHostToDevice, cs));
+        FMHA_CHECK_CUDA(cudaMemcpyAsync(base + L.v + b0 * kvb, vh + b0 * kvb, nb * kvb, cudaMemcpyHostToDevice, cs));
+        if (aux) {
+            FMHA_CHECK_CUDA(cudaEventRecord(aux->copied[c], cs));
+            FMHA_CHECK_CUDA(cudaStreamWaitEvent(st, aux->copied[c], 0));
+        }
+        float* lse_dev = lse_host ? reinterpret_cast<float*>(base + L.lse + b0 * lb) : nullptr;
+        rc = fmha_fwd_ex(base + L.q + b0 * qb, base + L.k + b0 * kvb, base + L.v + b0 * kvb, base + L.o + b0 * ob, lse_dev,
+                         nb, Hq, Hkv, Sq, Skv, D, scale, stream, &w);
+        if (rc) return rc;
+        FMHA_CHECK_CUDA(cudaMemcpyAsync(static_cast<uint8_t*>(out_host) + b0 * ob, base + L.o + b0 * ob, nb * ob,
+                                        cudaMemcpyDeviceToHost, st));
+        if (lse_host)
+            FMHA_CHECK_CUDA(cudaMemcpyAsync(reinterpret_cast<uint8_t*>(lse_host) + b0 * lb, lse_dev, nb * lb,
+                                            cudaMemcpyDeviceToHost, st));
+    }
+    return FMHA_OK;
+}
+
 // ---- standalone NVFP4 ------------------------------------------------------------------------------------
 static size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
 

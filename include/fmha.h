@@ -126,6 +126,34 @@ int fmha_fwd_ex(const void* q, const void* k, const void* v, void* out, float* l
 size_t fmha_workspace_size(int B, int Hq, int Hkv, int Sq, int Skv, int D, const fmha_opts* opts);
 
 /*
+ * Attention from host memory: copies Q, K and V to the device, runs fmha_fwd_ex, and copies O and
+ * the LSE back, all ordered after the work already on `stream`.  Returns once everything is
+ * enqueued: synchronise `stream` before reading out_host / lse_host.
+ *   q_host, k_host, v_host: host BF16 arrays in the fmha_fwd layouts; out_host: host O, BF16 or
+ *   (opts->out_kind == FMHA_OUT_F32) FP32 [B,Hq,Sq,D]; lse_host: host FP32 [B,Hq,Sq] or NULL.
+ *   Page-locked host memory (cudaHostAlloc, cudaHostRegister) makes the copies asynchronous;
+ *   pageable memory works, but the copies then hold up the calling thread.
+ *   dev_buf: device memory of at least fmha_host_buffer_size() bytes, 256-byte aligned, owned by the
+ *   caller; it stages Q, K, V, O and the LSE and holds the attention workspace, so the call
+ *   allocates nothing.  Calls that share dev_buf must be ordered on one stream.
+ *   opts: as for fmha_fwd_ex, limited to out_kind (BF16 or F32), num_splits, causal and
+ *   wide_variant; seqlens_k, the NVFP4 fields and the workspace fields must be NULL / 0
+ *   (FMHA_ERR_UNSUPPORTED otherwise).  opts == NULL: BF16 output, automatic split-KV.
+ * With B >= 2 the batch runs in up to four chunks of whole batch entries, so that the copy of one
+ * chunk's inputs overlaps the attention of the one before (an internal copy stream per device, joined
+ * back to `stream` through events; calls from several host threads are serialised while they
+ * enqueue).  Errors: FMHA_ERR_INVALID (NULL or bad arguments), FMHA_ERR_WORKSPACE (dev_buf missing,
+ * misaligned or too small), FMHA_ERR_UNSUPPORTED, FMHA_ERR_CUDA; with an error nothing is enqueued,
+ * except for FMHA_ERR_CUDA from a failing copy or launch, after which out_host is unspecified.
+ */
+int fmha_fwd_host(const void* q_host, const void* k_host, const void* v_host, void* out_host, float* lse_host, int B,
+                  int Hq, int Hkv, int Sq, int Skv, int D, float scale, fmha_stream_t stream, const fmha_opts* opts,
+                  void* dev_buf, size_t dev_buf_bytes);
+
+/* Bytes of device memory fmha_fwd_host needs for this problem and these options (0 if invalid). */
+size_t fmha_host_buffer_size(int B, int Hq, int Hkv, int Sq, int Skv, int D, const fmha_opts* opts);
+
+/*
  * NVFP4 quantisation of an FP32 tensor x[n], n % 16 == 0 (the NVFP4 step of the pages' kernel
  * plan, "FP4 quantization for NVFP4-1.1"):
  *   s_g = fp32(amax / (6 * 448)); per block of 16: sc = E4M3(amax_block / (6 s_g)) (round to
