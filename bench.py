@@ -34,13 +34,16 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # named kernel, with the sha256 of its source file and the shared device headers at capture time;
 # reported only while those sources are unchanged.
 TRAFFIC = {
-    # decode B8 H32 Sq1 Skv4096 D128: read 537,138,688 + written 3,301,888 bytes
+    # decode B8 H32 Sq1 Skv4096 D128 (decode_kernel<128, 0, 0>): read 537,078,784 + written 3,066,624 bytes
     # (profiles/decode_kernel_decode-B8-H32-Skv4096-D128.md)
-    "decode_kernel<128>": {"bytes": 540440576, "source_sha": "17f62e5631bfa11c"},
-    # ragged GQA decode B64 Hq32 Hkv8 Skv<=32768 D128: the quarter-size workload (B16) read 1,005,942,016 +
-    # wrote 333,056 bytes for 1,001,226,240 algorithmic K/V bytes (1.005x); scaled by the K/V bytes to the
-    # full workload's 4,106,002,432 (profiles/side-kernels_ragged-decode-wide-combine-nvfp4.md)
-    "decode_kernel<128>/ragged": {"bytes": 4126707559, "source_sha": "17f62e5631bfa11c"},
+    "decode_kernel<128>": {"bytes": 540145408, "source_sha": "72771f3dc9e65a4a"},
+    # ragged GQA decode B64 Hq32 Hkv8 Skv<=32768 D128 (decode_kernel<128, 0, 1>): the quarter-size workload
+    # (B16) read 1,005,915,904 + wrote 372,736 bytes for 1,001,226,240 algorithmic K/V bytes (1.005x); scaled
+    # by the K/V bytes to the full workload's 4,106,002,432 (profiles/side-kernels_ragged-decode-wide-combine-nvfp4.md)
+    "decode_kernel<128>/ragged": {"bytes": 4126763201, "source_sha": "72771f3dc9e65a4a"},
+    # speculative decode B8 Hq32 Hkv8 Sq4 Skv8192 D128, causal (decode_kernel<128, 1, 1>): read 268,838,912 +
+    # written 2,815,232 bytes (profiles/decode_kernel_decode-B8-H32-Skv4096-D128.md)
+    "decode_kernel<128>/speculative": {"bytes": 271654144, "source_sha": "72771f3dc9e65a4a"},
     # wide-head B32 Hq128 Hkv1 Skv16384 D512, independent CTAs: read 1,081,725,696 + written 10,418,688
     # bytes (profiles/wide_kernel_wide-head-B32-Hq128-Hkv1-Skv16384-D512.md)
     "wide_kernel<independent>": {"bytes": 1092144384, "source_sha": "fc24eba4f080698b"},
@@ -469,6 +472,8 @@ def _workload_entry(F, w, idx, steps, warmup, peaks, causal=False, given_scale=F
             traffic = traffic_for("wide_kernel<pair>" if wide_variant == 2 else "wide_kernel<independent>", "wide.cu")
         elif w.ragged and not causal and not given_scale:
             traffic = traffic_for("decode_kernel<128>/ragged", "decode.cu")
+        elif causal and w.Sq == 4 and w.Skv == 8192 and w.B == 8:
+            traffic = traffic_for("decode_kernel<128>/speculative", "decode.cu")
         else:
             traffic = None
         roof = hbm_roofline(ach, peaks, read_peak)
