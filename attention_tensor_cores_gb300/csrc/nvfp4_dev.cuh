@@ -12,11 +12,11 @@
 // upper code is even.  Write t s_g = hi + lo exactly (hi = fl(t s_g), lo = fma(t, s_g, -hi)).  No
 // float lies strictly between hi and t s_g, so for a float |x| that question is the single
 // comparison |x| >= U with U = hi when lo < 0 (or lo == 0 and the tie rounds up) and U = the next
-// float above hi otherwise.  A block computes its seven element bounds once; they increase with
-// the midpoint, so each element takes a binary search of three comparisons.  lo is exact while
-// t s_g stays well inside the normal range; for s_g outside [2^-90, 2^100] the FP64 route below is
-// used instead (rounding of FP64 quotients, whose products with the grid midpoints have at most 31
-// significant bits).
+// float above hi otherwise.  A block computes its seven element bounds once and counts, per element,
+// the bounds |x| reaches; one value alone takes a binary search over the bounds it needs.  lo is
+// exact while t s_g stays well inside the normal range; for s_g outside [2^-90, 2^100] the FP64
+// route below is used instead (rounding of FP64 quotients, whose products with the grid midpoints
+// have at most 31 significant bits).
 #pragma once
 
 #include <cstdint>
@@ -116,6 +116,7 @@ __device__ __forceinline__ uint32_t e4m3_block_scale_f32(float ab, float sg)
 // tie at midpoint k rounds up when k is odd).
 struct E2m1Bounds {
     float u[7];
+    float K, P[7];   // the step form: K = 2^(23 - e), e the exponent of pred(u[0]); P[k] = K * pred(u[k])
 };
 
 __device__ __forceinline__ E2m1Bounds e2m1_bounds(float dsc, float sg)
@@ -124,22 +125,30 @@ __device__ __forceinline__ E2m1Bounds e2m1_bounds(float dsc, float sg)
     E2m1Bounds b;
 #pragma unroll
     for (int k = 0; k < 7; ++k) b.u[k] = round_up_bound(__fmul_rn(mids[k], dsc), sg, k & 1);   // mid * dsc exact
+    b.K = __uint_as_float((277u - ((__float_as_uint(b.u[0]) - 1u) >> 23)) << 23);
+#pragma unroll
+    for (int k = 0; k < 7; ++k) b.P[k] = __fmul_rn(b.K, __uint_as_float(__float_as_uint(b.u[k]) - 1u));   // exact
     return b;
 }
 
-// The bounds increase with k, so the code (how many bounds |x| reaches) takes a binary search of
-// three comparisons.  A NaN reaches none.
+// E2M1 code of x from a block's bounds: how many bounds |x| reaches, counted on the FMA pipe (a
+// search's comparisons and selects would load the ALU pipe instead).  |x| >= u[k] exactly when
+// |x| > pred(u[k]), as no float lies between them.  The fma K |x| - P[k] is exact before its one
+// rounding, so its sign is right, and when positive it is at least K times the gap between
+// pred(u[k]) and the next float, which is at least 2^(e - 23) = 1 / K: its saturation is 1 or 0
+// (a NaN saturates to 0).  The seven steps are summed onto 1.5 * 2^23, whose low mantissa bits then
+// hold the count.
 __device__ __forceinline__ uint32_t e2m1_code_f32(float x, const E2m1Bounds& b)
 {
     const float a = fabsf(x);
-    const bool p2 = a >= b.u[3];
-    const bool p1 = a >= (p2 ? b.u[5] : b.u[1]);
-    const float u0 = p2 ? b.u[4] : b.u[0], u2 = p2 ? b.u[6] : b.u[2];
-    const bool p0 = a >= (p1 ? u2 : u0);
-    return (p2 ? 4u : 0u) + (p1 ? 2u : 0u) + (p0 ? 1u : 0u) + ((__float_as_uint(x) >> 28) & 8u);
+    float acc = 12582912.f;
+#pragma unroll
+    for (int k = 0; k < 7; ++k) acc = __fadd_rn(acc, __saturatef(__fmaf_rn(a, b.K, -b.P[k])));
+    return (__float_as_uint(acc) - 0x4B400000u) | ((__float_as_uint(x) >> 28) & 8u);
 }
 
-// The same search for one value, computing only the three bounds it visits.
+// The code of one value by a binary search over the bounds, which increase with k: three
+// comparisons, computing only the three bounds the search visits.  A NaN reaches none.
 __device__ __forceinline__ uint32_t e2m1_code_f32(float x, float dsc, float sg)
 {
     const float a = fabsf(x);
