@@ -1027,7 +1027,13 @@ int run_decode(const AttnArgs& a, bool split, void* ws, cudaStream_t st)
     const void* fn = epi ? reinterpret_cast<const void*>(decode_kernel<D, CAUSAL, true>)
                          : reinterpret_cast<const void*>(decode_kernel<D, CAUSAL, false>);
     FMHA_CHECK_CUDA(set_smem_limit_once(fn, C::kSmemBytes));
-    const int grid = split ? nsm : (U < nsm ? U : nsm);
+    // one CTA per SM, or one per key tile when a uniform-length problem has fewer tiles than SMs (a
+    // small problem then launches only the CTAs that have work)
+    int grid = split ? nsm : (U < nsm ? U : nsm);
+    if (split && !p.prefix) {
+        const long long tiles = static_cast<long long>(U) * p.tiles_uniform;
+        if (tiles < grid) grid = static_cast<int>(tiles);
+    }
     if (grid > 0) {
         timing_mark_begin(st);
         if (epi)
