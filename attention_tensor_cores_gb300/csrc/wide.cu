@@ -946,8 +946,13 @@ int launch_wide(const AttnArgs& a, int num_splits, void* ws, size_t ws_bytes, cu
     const bool pair = !a.seqlens && a.wide_variant == FMHA_WIDE_PAIR;
     if (pair) FMHA_CHECK_CUDA(set_smem_limit_once(reinterpret_cast<const void*>(wide_kernel<true>), WCfg<true>::kSmem));
     const int max_pairs = pair ? pair_clusters(nsm) : nsm / 2;
-    // whole units: no more pairs than units (each pair takes units p, p + P, ...)
-    const int npairs = whole ? min(max_pairs, heads * row_tiles) : max_pairs;
+    // whole units: no more pairs than units (each pair takes units p, p + P, ...); split with uniform
+    // lengths: no more pairs than 32-key tiles, so that a small problem launches only pairs with work
+    int npairs = whole ? min(max_pairs, heads * row_tiles) : max_pairs;
+    if (!whole && !a.seqlens) {
+        const long long tiles = static_cast<long long>(heads) * row_tiles * ((a.Skv + kWKeys - 1) / kWKeys);
+        if (tiles < npairs) npairs = static_cast<int>(tiles);
+    }
     CUtensorMap qmap, kmap, vmap;
     {
         const uint64_t dims[3] = {static_cast<uint64_t>(kWD), static_cast<uint64_t>(R), static_cast<uint64_t>(heads)};
