@@ -170,8 +170,10 @@ def test_bad_arguments_return_codes(F):
 
 @pytest.mark.parametrize("B,Hq,Hkv,Skv,D", [
     (1, 8, 1, 160000, 128),   # one unit over every CTA: up to one partial per SM, merged by the last arrival
-    (1, 4, 1, 1000, 64),      # fewer key tiles than CTAs: some CTAs hold no tiles
+    (1, 4, 1, 1000, 64),      # fewer key tiles than SMs: one CTA per tile (8 CTAs, 4 query columns)
     (3, 16, 2, 777, 128),     # several units, partial tail tiles
+    (1, 1, 1, 5100, 64),      # one column, 40 tiles: 40 CTAs, one partial each, merged (more than four)
+    (1, 16, 1, 5100, 128),    # 16 columns (epilogue warpgroup), 40 CTAs of one tile, 40 partials merged
 ])
 def test_split_merge_in_kernel(F, B, Hq, Hkv, Skv, D):
     """Split-KV units are merged inside the decode kernel by the CTA that completes them."""
