@@ -425,6 +425,10 @@ __global__ void __launch_bounds__(decode_threads<EPI>(), 1)
                 // the unit may stay unmerged, so say so instead of failing silently
                 if (arrived < 0) atomicExch(p.status, kDevMergeLost);
                 fx_last = (arrived == n && n > 0) ? 1 : 0;
+                // every arrival of this call is in: clear the counter for the next call.  A CUDA graph
+                // replays a call with the same tag, so its arrivals must not be left over (0 carries
+                // no call's tag: tags are never 0).
+                if (fx_last) atomicExch(p.unit_ctr + it.u, 0ull);
             }
             named_bar_sync(bar, 128);
             if (fx_last) {

@@ -151,7 +151,8 @@ __device__ __forceinline__ void named_bar_sync(int id, int n)
 
 // Counts one arrival at a unit's counter and returns the count of this call's arrivals so far.
 // The counter carries this call's tag in its upper 48 bits, so whatever an earlier call (or the
-// caller) left in it reads as zero arrivals: no reset between calls is needed.  The CAS loop fails
+// caller) left in it reads as zero arrivals; the last arrival clears it, which a CUDA graph's replays
+// (the same tag each time) need.  The CAS loop fails
 // only when another CTA arrived in between, so within one call it ends after at most `need` (at
 // most a few hundred) retries.  Returns -1 after 4096 failures, which only calls that overlap on
 // one workspace can cause; the caller reports that through the status word.
