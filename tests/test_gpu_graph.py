@@ -94,3 +94,31 @@ def test_graph_replay_matches_direct_call(F, name):
     else:
         o = bufs["out"].float().cpu().numpy().reshape(-1, w.D)
     check_o_lse(o, bufs["lse"].cpu().numpy().reshape(-1), o_ref, l_ref, f"graph {name}")
+
+
+def test_graph_replay_of_host_entry_point(F):
+    """fmha_fwd_host in a CUDA graph: its copy stream joins the capture through events, the copies
+    become memcpy nodes on the page-locked host buffers, and a replay gives the same bits."""
+    w = inputs.Workload("t", 4, 8, 2, 1, 1500, 128, 1.0, "bf16", 82)
+    q, k, v, _ = w.make("cpu")
+    q, k, v = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    out = torch.zeros(w.B, w.Hq, w.Sq, w.D, dtype=torch.float32).pin_memory()
+    lse = torch.zeros(w.B, w.Hq, w.Sq, dtype=torch.float32).pin_memory()
+    opts = F.make_opts(F.FMHA_OUT_F32)
+    buf = torch.empty(F.fmha_host_buffer_size(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.D, opts), dtype=torch.uint8,
+                      device="cuda")
+    F.fmha_fwd_host(q, k, v, out, lse, w.scale, buf, opts)
+    torch.cuda.synchronize()
+    direct_o, direct_l = out.clone(), lse.clone()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        F.fmha_fwd_host(q, k, v, out, lse, w.scale, buf, opts)
+    torch.cuda.synchronize()
+    for _ in range(2):
+        out.zero_()
+        lse.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, direct_o) and torch.equal(lse, direct_l)
+    o_ref, l_ref = oracle.attention(q, k, v, w.scale)
+    check_o_lse(out.numpy().reshape(-1, w.D), lse.numpy().reshape(-1), o_ref, l_ref, "graph host")
