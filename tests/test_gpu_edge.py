@@ -1,12 +1,14 @@
-"""GPU edge and degenerate cases through the C ABI: empty problems, and a zero query, where every
+"""GPU edge and degenerate cases through the C ABI: empty problems; a zero query, where every
 visible key has the same score, so O is the plain mean of the visible value rows and LSE = ln n
-(a closed form that does not depend on the keys), on every kernel path including the causal mask."""
+(a closed form that does not depend on the keys), on every kernel path including the causal mask;
+and shapes at the edges of the dispatch and the mask against the oracle."""
 import math
 
 import numpy as np
 import pytest
 import torch
 
+import oracle
 from attention_tensor_cores_gb300 import inputs
 from attn_util import check_o_lse, run_attention
 
@@ -66,3 +68,27 @@ def test_zero_query_gives_mean_of_visible_values(F, B, Hq, Hkv, Sq, Skv, D, caus
         o_ref[r] = vv[b, hq // g, :n].mean(axis=0)
         l_ref[r] = math.log(n)
     check_o_lse(res["o"], res["lse"], o_ref, l_ref, "zero query")
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Sq,Skv,D,causal,splits", [
+    (1, 17, 1, 1, 300, 64, False, 0),      # G = 17: the first shape on the row-tile path (17 of 128 rows)
+    (1, 17, 1, 1, 300, 128, False, None),  # the same at D = 128, whole units
+    (1, 2, 2, 200, 1, 64, False, 0),       # row tiles, a single key
+    (1, 2, 2, 200, 1, 128, True, 0),       # row tiles, one key: only the last query sees it
+    (2, 8, 2, 4, 2, 128, True, 0),         # decode (16 columns), causal with Sq > Skv: queries that see nothing
+    (1, 16, 1, 1, 1, 512, False, 0),       # wide head, a single key
+    (1, 32, 1, 4, 2, 512, True, 1),        # wide head, causal with Sq > Skv, whole units
+])
+def test_boundary_shapes_against_oracle(F, B, Hq, Hkv, Sq, Skv, D, causal, splits):
+    """Shapes at the edges of the dispatch and of the mask: the decode / row-tile boundary, one key per
+    head on every path, and causal queries with no visible key (O = 0, LSE = -inf)."""
+    w = inputs.Workload("t", B, Hq, Hkv, Sq, Skv, D, 1.0, "bf16", 96)
+    q, k, v, _ = w.make("cuda")
+    kw = {} if splits is None else {"num_splits": splits}
+    if causal:
+        kw["causal"] = True
+    res = run_attention(F, q, k, v, w.scale, **kw)
+    o_ref, l_ref = oracle.attention(q.cpu(), k.cpu(), v.cpu(), w.scale, causal=causal)
+    check_o_lse(res["o"], res["lse"], o_ref, l_ref, "boundary shape")
+    if causal and Sq > Skv:
+        assert np.isneginf(l_ref).any() and np.all(res["o"][np.isneginf(l_ref)] == 0.0)
