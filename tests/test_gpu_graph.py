@@ -57,7 +57,7 @@ def _setup(F, name):
         F.fmha_fwd_ex(q, k, v, bufs["out"], bufs["lse"], w.scale, opts)
 
     # opts holds only the workspace's address: the tensor must outlive every call and replay (torch
-    # returns freed memory to the driver when a capture begins)
+    # frees its cached memory with cudaFree when a capture begins)
     call.workspace = ws
     return w, (q, k, v), bufs, call
 
