@@ -34,16 +34,16 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # named kernel, with the sha256 of its source file and the shared device headers at capture time;
 # reported only while those sources are unchanged.
 TRAFFIC = {
-    # decode B8 H32 Sq1 Skv4096 D128 (decode_kernel<128, 0, 0>): read 537,084,160 + written 2,957,312 bytes
-    # (profiles/decode_kernel_decode-B8-H32-Skv4096-D128.md)
-    "decode_kernel<128>": {"bytes": 540041472, "source_sha": "efcd09784d8abb76"},
+    # decode B8 H32 Sq1 Skv4096 D128 (decode_kernel<128, 0, 0>, 128 CTAs of two whole units): read
+    # 537,037,824 + written 2,838,784 bytes (profiles/decode_kernel_decode-B8-H32-Skv4096-D128.md)
+    "decode_kernel<128>": {"bytes": 539876608, "source_sha": "2eefc8e21129a4a0"},
     # ragged GQA decode B64 Hq32 Hkv8 Skv<=32768 D128 (decode_kernel<128, 0, 1>): the quarter-size workload
-    # (B16) read 1,005,861,376 + wrote 365,568 bytes for 1,001,226,240 algorithmic K/V bytes (1.005x); scaled
+    # (B16) read 1,005,862,144 + wrote 374,016 bytes for 1,001,226,240 algorithmic K/V bytes (1.005x); scaled
     # by the K/V bytes to the full workload's 4,106,002,432 (profiles/side-kernels_ragged-decode-wide-combine-nvfp4.md)
-    "decode_kernel<128>/ragged": {"bytes": 4126510187, "source_sha": "efcd09784d8abb76"},
-    # speculative decode B8 Hq32 Hkv8 Sq4 Skv8192 D128, causal (decode_kernel<128, 1, 1>): read 268,838,400 +
-    # written 3,020,032 bytes (profiles/decode_kernel_decode-B8-H32-Skv4096-D128.md)
-    "decode_kernel<128>/speculative": {"bytes": 271858432, "source_sha": "efcd09784d8abb76"},
+    "decode_kernel<128>/ragged": {"bytes": 4126547982, "source_sha": "2eefc8e21129a4a0"},
+    # speculative decode B8 Hq32 Hkv8 Sq4 Skv8192 D128, causal (decode_kernel<128, 1, 1>): read 268,839,680 +
+    # written 2,982,144 bytes (profiles/decode_kernel_decode-B8-H32-Skv4096-D128.md)
+    "decode_kernel<128>/speculative": {"bytes": 271821824, "source_sha": "2eefc8e21129a4a0"},
     # wide-head B32 Hq128 Hkv1 Skv16384 D512, independent CTAs: read 1,081,725,184 + written 10,468,096
     # bytes (profiles/wide_kernel_wide-head-B32-Hq128-Hkv1-Skv16384-D512.md)
     "wide_kernel<independent>": {"bytes": 1092193280, "source_sha": "921408e1310a6fac"},
