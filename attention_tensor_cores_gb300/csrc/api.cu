@@ -116,6 +116,20 @@ void timing_mark_end(cudaStream_t st)
     g_ev_begin = g_ev_end = nullptr;
 }
 
+unsigned pdl_attribute(cudaStream_t st, cudaLaunchAttribute* attr)
+{
+    // a graph being captured keeps plain stream order (its nodes then depend on whole kernels)
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    if (cs != cudaStreamCaptureStatusNone) return 0;
+    attr->id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr->val.programmaticStreamSerializationAllowed = 1;
+    return 1;
+}
+
 // ---- TMA tensor maps -------------------------------------------------------------------------------
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 {

@@ -285,7 +285,7 @@ __global__ void __launch_bounds__(decode_threads<EPI>(), 1)
     __shared__ float fx_w[kN][4], fx_lse[kN];   // merge: per column, the partials' weights and the merged LSE
 
     const int warp = threadIdx.x / 32;
-    if (blockIdx.x == 0 && threadIdx.x == 0 && p.nv_ts) *p.nv_ts = *p.nv_sg;   // single-pass NVFP4: report s_g
+    griddep_launch_dependents();
     const WaitCtl wc{&abort_flag, p.status, p.limit};
 
     if (threadIdx.x == 0) {
@@ -319,6 +319,8 @@ __global__ void __launch_bounds__(decode_threads<EPI>(), 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_slot;   // S buffers at columns 0/16, O buffers at 32/48, handoff at 64/96
+    griddep_wait();   // the previous kernel of the stream has completed: global memory from here on
+    if (blockIdx.x == 0 && threadIdx.x == 0 && p.nv_ts) *p.nv_ts = *p.nv_sg;   // single-pass NVFP4: report s_g
 
     Sched sched;
     sched.init(&p, blockIdx.x, gridDim.x);
@@ -810,6 +812,8 @@ __global__ void __launch_bounds__(decode_threads<EPI>(), 1)
 // Exclusive prefix of per-unit tile counts (ragged keys), one block.
 __global__ void __launch_bounds__(1024) tile_prefix_kernel(const int32_t* seqlens, int Hkv, int U, int32_t* prefix)
 {
+    griddep_launch_dependents();
+    griddep_wait();
     __shared__ int part[1024];
     const int per = (U + 1023) / 1024;
     const int b0 = threadIdx.x * per;
@@ -842,6 +846,8 @@ __global__ void combine_kernel(const __grid_constant__ DecodeParams p, int nctas
     __shared__ float weights[kMaxPartsD];
     __shared__ int nslots;
     __shared__ float lse_sh;
+    griddep_launch_dependents();
+    griddep_wait();
     const int row = blockIdx.x;
     const int u = row / p.G;
     const int q = row % p.G;
@@ -1020,8 +1026,8 @@ int run_decode(const AttnArgs& a, bool split, void* ws, cudaStream_t st)
     p.limit = wait_limit();
 
     if (p.prefix) {
-        tile_prefix_kernel<<<1, 1024, 0, st>>>(a.seqlens, a.Hkv, U, const_cast<int32_t*>(p.prefix));
-        FMHA_CHECK_LAUNCH("tile_prefix_kernel");
+        FMHA_CHECK_CUDA(launch_pdl(tile_prefix_kernel, dim3(1), dim3(1024), 0, st, a.seqlens, a.Hkv, U,
+                                   const_cast<int32_t*>(p.prefix)));
         count_launch();
     }
     // The epilogue warpgroup takes each item's epilogue off the softmax warps when a unit has several
@@ -1051,17 +1057,17 @@ int run_decode(const AttnArgs& a, bool split, void* ws, cudaStream_t st)
     }
     if (grid > 0) {
         timing_mark_begin(st);
-        if (epi)
-            decode_kernel<D, CAUSAL, true><<<grid, decode_threads<true>(), C::kSmemBytes, st>>>(qmap, kmap, vmap, p);
-        else
-            decode_kernel<D, CAUSAL, false><<<grid, decode_threads<false>(), C::kSmemBytes, st>>>(qmap, kmap, vmap, p);
+        const cudaError_t e = epi ? launch_pdl(decode_kernel<D, CAUSAL, true>, dim3(static_cast<unsigned>(grid)),
+                                               dim3(decode_threads<true>()), C::kSmemBytes, st, qmap, kmap, vmap, p)
+                                  : launch_pdl(decode_kernel<D, CAUSAL, false>, dim3(static_cast<unsigned>(grid)),
+                                               dim3(decode_threads<false>()), C::kSmemBytes, st, qmap, kmap, vmap, p);
         timing_mark_end(st);
-        FMHA_CHECK_LAUNCH("decode_kernel");
+        FMHA_CHECK_CUDA(e);
         count_launch();
     }
     if (split && !p.fixup && U * G > 0) {
-        combine_kernel<<<U * G, D, 0, st>>>(p, grid);
-        FMHA_CHECK_LAUNCH("combine_kernel");
+        FMHA_CHECK_CUDA(launch_pdl(combine_kernel, dim3(static_cast<unsigned>(U * G)), dim3(static_cast<unsigned>(D)), 0,
+                                   st, p, grid));
         count_launch();
     }
     return FMHA_OK;

@@ -21,6 +21,8 @@ namespace {
 
 __global__ void amax_kernel(const float* __restrict__ x, int64_t n, unsigned* amax_bits)
 {
+    griddep_launch_dependents();
+    griddep_wait();
     float m = 0.f;
     const int64_t n4 = n / 4;
     const float4* x4 = reinterpret_cast<const float4*>(x);
@@ -38,6 +40,8 @@ __global__ void quant_kernel(const float* __restrict__ x, int64_t nblocks, uint8
                              uint8_t* __restrict__ scales, float* tensor_scale, const unsigned* amax_bits,
                              const float* sg_in)
 {
+    griddep_launch_dependents();
+    griddep_wait();
     // s_g: given by the caller, or fp32(amax / 2688) (one correctly rounded division)
     const float sg = sg_in ? *sg_in : __fdiv_rn(__uint_as_float(*amax_bits), 2688.0f);
     if (blockIdx.x == 0 && threadIdx.x == 0 && tensor_scale) *tensor_scale = sg;
@@ -70,8 +74,7 @@ int launch_nvfp4(const float* x, uint8_t* codes, uint8_t* scales, float* tensor_
         if (n > 0) {
             const int64_t want = (n / 4 + 255) / 256;
             const int grid = static_cast<int>(want < 4 * nsm ? (want > 0 ? want : 1) : 4 * nsm);
-            amax_kernel<<<grid, 256, 0, st>>>(x, n, amax_bits);
-            FMHA_CHECK_LAUNCH("amax_kernel");
+            FMHA_CHECK_CUDA(launch_pdl(amax_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0, st, x, n, amax_bits));
             count_launch();
         }
     }
@@ -79,9 +82,10 @@ int launch_nvfp4(const float* x, uint8_t* codes, uint8_t* scales, float* tensor_
     const int64_t want = (nblocks + 255) / 256;
     const int grid = static_cast<int>(want < 8 * nsm ? (want > 0 ? want : 1) : 8 * nsm);
     if (!amax_ready) timing_mark_begin(st);
-    quant_kernel<<<grid, 256, 0, st>>>(x, nblocks, codes, scales, tensor_scale, amax_bits, sg_in);
+    const cudaError_t e = launch_pdl(quant_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0, st, x, nblocks, codes,
+                                     scales, tensor_scale, const_cast<const unsigned*>(amax_bits), sg_in);
     if (!amax_ready) timing_mark_end(st);
-    FMHA_CHECK_LAUNCH("quant_kernel");
+    FMHA_CHECK_CUDA(e);
     count_launch();
     return FMHA_OK;
 }

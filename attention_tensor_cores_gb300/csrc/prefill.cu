@@ -201,8 +201,8 @@ __global__ void __launch_bounds__(prefill_threads<RING>(), 1)
     __shared__ int abort_flag;
 
     const int warp = threadIdx.x / 32;
+    griddep_launch_dependents();
     const WaitCtl wc{&abort_flag, p.status, p.limit};
-    if (RING && blockIdx.x == 0 && threadIdx.x == 0 && p.nv_ts) *p.nv_ts = *p.nv_sg;   // single-pass NVFP4: report s_g
     if (threadIdx.x == 0) {
         abort_flag = 0;
         for (int i = 0; i < QS; ++i) {
@@ -236,6 +236,8 @@ __global__ void __launch_bounds__(prefill_threads<RING>(), 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
+    griddep_wait();   // the previous kernel of the stream has completed: global memory from here on
+    if (RING && blockIdx.x == 0 && threadIdx.x == 0 && p.nv_ts) *p.nv_ts = *p.nv_sg;   // single-pass NVFP4: report s_g
     const int n_items = p.U * p.pairs;
 
     // Each setmaxnreg dominates only its own role's code (the register budget of code after a join
@@ -728,9 +730,10 @@ int run_prefill(const AttnArgs& a, bool dynamic, void* ws, cudaStream_t st)
     if (grid > 0) {
         if (dynamic) FMHA_CHECK_CUDA(cudaMemsetAsync(p.sched, 0, sizeof(int), st));
         timing_mark_begin(st);
-        prefill_kernel<D, CAUSAL, RING><<<grid, prefill_threads<RING>(), C::kSmemBytes, st>>>(qmap, kmap, vmap, p);
+        const cudaError_t e = launch_pdl(prefill_kernel<D, CAUSAL, RING>, dim3(static_cast<unsigned>(grid)),
+                                         dim3(prefill_threads<RING>()), C::kSmemBytes, st, qmap, kmap, vmap, p);
         timing_mark_end(st);
-        FMHA_CHECK_LAUNCH("prefill_kernel");
+        FMHA_CHECK_CUDA(e);
         count_launch();
     }
     return FMHA_OK;

@@ -47,6 +47,15 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count)
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
 }
 
+// Programmatic dependent launch.  A kernel launched with the programmatic-serialization attribute
+// may be placed on SMs while the previous kernel of its stream is still running.  griddep_wait blocks
+// until that kernel has completed and its memory operations are visible, so a kernel runs only code
+// that touches shared memory, Tensor Memory and its parameters before it.  griddep_launch_dependents
+// lets the next such kernel be launched once every CTA of this one has executed it.  Both do nothing
+// for a kernel launched without the attribute.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Makes initialised barriers visible to the async proxy (TMA, tensor core).
 __device__ __forceinline__ void fence_barrier_init()
 {

@@ -243,7 +243,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
     __shared__ int abort_flag;
 
     const int warp = threadIdx.x / 32;
-    if (blockIdx.x == 0 && threadIdx.x == 0 && p.nv_ts) *p.nv_ts = *p.nv_sg;   // single-pass NVFP4: report s_g
+    griddep_launch_dependents();
     // this CTA's half of the value columns (PAIR: its rank in the cluster); the even CTA leads a pair
     const int half = PAIR ? static_cast<int>(cluster_ctarank()) : static_cast<int>(blockIdx.x & 1);
     const bool leader = !PAIR || half == 0;
@@ -279,6 +279,8 @@ __global__ void __launch_bounds__(kWThreads, 1)
     if constexpr (PAIR) cluster_sync();   // both CTAs' barriers exist before either signals the other
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
+    griddep_wait();   // the previous kernel of the stream has completed: global memory from here on
+    if (blockIdx.x == 0 && threadIdx.x == 0 && p.nv_ts) *p.nv_ts = *p.nv_sg;   // single-pass NVFP4: report s_g
     // waits on the barriers the other CTA's softmax threads arrive on (cluster-scope acquire); copy and
     // MMA completions aimed at a barrier are waited for with the ordinary wait
     auto wait_x = [&](uint64_t* b, uint32_t parity) -> bool {
@@ -683,6 +685,8 @@ __global__ void __launch_bounds__(kWThreads, 1)
 __global__ void __launch_bounds__(1024) wide_prefix_kernel(const int32_t* seqlens, int Hkv, int row_tiles, int U,
                                                           int32_t* prefix)
 {
+    griddep_launch_dependents();
+    griddep_wait();
     __shared__ int part[1024];
     const int per = (U + 1023) / 1024;
     const int b0 = threadIdx.x * per;
@@ -717,6 +721,8 @@ __global__ void __launch_bounds__(kWRows) wide_combine_kernel(const __grid_const
 {
     __shared__ int slots[kMaxParts];
     __shared__ int nslots;
+    griddep_launch_dependents();
+    griddep_wait();
     const int u = blockIdx.x / (kWD / kCombCols);
     const int col0 = (blockIdx.x % (kWD / kCombCols)) * kCombCols;
     const int r = static_cast<int>(threadIdx.x);
@@ -1000,8 +1006,8 @@ int launch_wide(const AttnArgs& a, int num_splits, void* ws, size_t ws_bytes, cu
     p.status = device_status_ptr();
     p.limit = wait_limit();
     if (p.prefix) {
-        wide_prefix_kernel<<<1, 1024, 0, st>>>(a.seqlens, a.Hkv, row_tiles, p.U, const_cast<int32_t*>(p.prefix));
-        FMHA_CHECK_LAUNCH("wide_prefix_kernel");
+        FMHA_CHECK_CUDA(launch_pdl(wide_prefix_kernel, dim3(1), dim3(1024), 0, st, a.seqlens, a.Hkv, row_tiles, p.U,
+                                   const_cast<int32_t*>(p.prefix)));
         count_launch();
     }
     if (pair) {
@@ -1010,13 +1016,13 @@ int launch_wide(const AttnArgs& a, int num_splits, void* ws, size_t ws_bytes, cu
         cfg.blockDim = dim3(kWThreads, 1, 1);
         cfg.dynamicSmemBytes = WCfg<true>::kSmem;
         cfg.stream = st;
-        cudaLaunchAttribute attr[1];
+        cudaLaunchAttribute attr[2];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = 2;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        cfg.numAttrs = 1 + pdl_attribute(st, &attr[1]);
         timing_mark_begin(st);
         const cudaError_t e = cudaLaunchKernelEx(&cfg, wide_kernel<true>, qmap, kmap, vmap, p);
         timing_mark_end(st);
@@ -1024,14 +1030,15 @@ int launch_wide(const AttnArgs& a, int num_splits, void* ws, size_t ws_bytes, cu
     } else {
         FMHA_CHECK_CUDA(set_smem_limit_once(reinterpret_cast<const void*>(wide_kernel<false>), WCfg<false>::kSmem));
         timing_mark_begin(st);
-        wide_kernel<false><<<2 * npairs, kWThreads, WCfg<false>::kSmem, st>>>(qmap, kmap, vmap, p);
+        const cudaError_t e = launch_pdl(wide_kernel<false>, dim3(static_cast<unsigned>(2 * npairs)), dim3(kWThreads),
+                                         WCfg<false>::kSmem, st, qmap, kmap, vmap, p);
         timing_mark_end(st);
+        if (e != cudaSuccess) return cuda_error(e, "wide_kernel");
     }
-    FMHA_CHECK_LAUNCH("wide_kernel");
     count_launch();
     if (whole) return FMHA_OK;   // every unit was written by its pair
-    wide_combine_kernel<<<p.U * (kWD / kCombCols), kWRows, 0, st>>>(p, npairs);
-    FMHA_CHECK_LAUNCH("wide_combine_kernel");
+    FMHA_CHECK_CUDA(launch_pdl(wide_combine_kernel, dim3(static_cast<unsigned>(p.U * (kWD / kCombCols))), dim3(kWRows),
+                               0, st, p, npairs));
     count_launch();
     return FMHA_OK;
 }

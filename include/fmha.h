@@ -14,6 +14,10 @@
  *   - All tensor pointers are DEVICE pointers owned by the caller; the library never allocates
  *     or frees device memory, never synchronises (except fmha_check_status) and launches only
  *     on `stream`.  Inputs are read-only; outputs must not alias inputs.
+ *   - Kernels are launched with programmatic dependent launch (except while `stream` is being
+ *     captured into a graph): a call's kernel may be placed on the SMs while the previous kernel of
+ *     `stream` finishes, but touches no global memory until that kernel has completed, so calls keep
+ *     plain stream order (a call may read what the previous kernel wrote, or overwrite what it read).
  *   - Layouts are contiguous, row-major: Q/O [B][Hq][Sq][D], K/V [B][Hkv][Skv][D], LSE [B][Hq][Sq].
  *   - Grouped-query attention: query head hq reads key/value head hq / (Hq / Hkv).
  *   - LSE is the natural logarithm of sum_j exp(scale * q.k_j) (scale included), FP32.
