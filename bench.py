@@ -35,20 +35,20 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # reported only while those sources are unchanged.
 TRAFFIC = {
     # decode B8 H32 Sq1 Skv4096 D128 (decode_kernel<128, 0, 0>, 128 CTAs of two whole units): read
-    # 537,037,824 + written 2,838,784 bytes (profiles/decode_kernel_decode-B8-H32-Skv4096-D128.md)
-    "decode_kernel<128>": {"bytes": 539876608, "source_sha": "2eefc8e21129a4a0"},
+    # 537,047,296 + written 2,819,328 bytes (profiles/decode_kernel_decode-B8-H32-Skv4096-D128.md)
+    "decode_kernel<128>": {"bytes": 539866624, "source_sha": "cc61cfcc3a305433"},
     # ragged GQA decode B64 Hq32 Hkv8 Skv<=32768 D128 (decode_kernel<128, 0, 1>): the quarter-size workload
-    # (B16) read 1,005,862,144 + wrote 374,016 bytes for 1,001,226,240 algorithmic K/V bytes (1.005x); scaled
+    # (B16) read 1,005,935,104 + wrote 674,048 bytes for 1,001,226,240 algorithmic K/V bytes (1.005x); scaled
     # by the K/V bytes to the full workload's 4,106,002,432 (profiles/side-kernels_ragged-decode-wide-combine-nvfp4.md)
-    "decode_kernel<128>/ragged": {"bytes": 4126547982, "source_sha": "2eefc8e21129a4a0"},
-    # speculative decode B8 Hq32 Hkv8 Sq4 Skv8192 D128, causal (decode_kernel<128, 1, 1>): read 268,839,680 +
-    # written 2,982,144 bytes (profiles/decode_kernel_decode-B8-H32-Skv4096-D128.md)
-    "decode_kernel<128>/speculative": {"bytes": 271821824, "source_sha": "2eefc8e21129a4a0"},
-    # wide-head B32 Hq128 Hkv1 Skv16384 D512, independent CTAs: read 1,081,725,184 + written 10,468,096
+    "decode_kernel<128>/ragged": {"bytes": 4128077612, "source_sha": "cc61cfcc3a305433"},
+    # speculative decode B8 Hq32 Hkv8 Sq4 Skv8192 D128, causal (decode_kernel<128, 1, 1>): read 268,840,192 +
+    # written 2,885,376 bytes (profiles/decode_kernel_decode-B8-H32-Skv4096-D128.md)
+    "decode_kernel<128>/speculative": {"bytes": 271725568, "source_sha": "cc61cfcc3a305433"},
+    # wide-head B32 Hq128 Hkv1 Skv16384 D512, independent CTAs: read 1,081,723,648 + written 10,473,728
     # bytes (profiles/wide_kernel_wide-head-B32-Hq128-Hkv1-Skv16384-D512.md)
-    "wide_kernel<independent>": {"bytes": 1092193280, "source_sha": "921408e1310a6fac"},
-    # same workload, CTA-pair MMA: read 1,081,819,648 + written 10,509,312 bytes (same file)
-    "wide_kernel<pair>": {"bytes": 1092328960, "source_sha": "921408e1310a6fac"},
+    "wide_kernel<independent>": {"bytes": 1092197376, "source_sha": "eec238122760f699"},
+    # same workload, CTA-pair MMA: read 1,081,827,072 + written 10,319,872 bytes (same file)
+    "wide_kernel<pair>": {"bytes": 1092146944, "source_sha": "eec238122760f699"},
 }
 
 
