@@ -710,19 +710,25 @@ __global__ void __launch_bounds__(1024) wide_prefix_kernel(const int32_t* seqlen
 }
 
 // Merges split units (lse = log sum exp lse_i, O = sum exp(lse_i - lse) O_i) and writes units
-// without keys (O = 0, LSE = -inf).  A block serves 32 of the 512 columns of one unit's 128 query
-// rows: warp 0 finds the pairs that hold partials of the unit once (64-bit divisions), then thread
-// r merges row r, its LSE in registers and its 32 columns over the partials.  A warp's load of one
-// 8-column group covers 32 consecutive rows, 1 KB of contiguous memory in the partial layout.
+// without keys (O = 0, LSE = -inf).  A block serves kCombCols of the 512 columns of one unit's 128
+// query rows: warp 0 finds the pairs that hold partials of the unit once (64-bit divisions), then
+// thread r merges row r, its LSE in registers and its kCombCols columns over the partials.  A warp's
+// load of one 8-column group covers 32 consecutive rows, 1 KB of contiguous memory in the partial
+// layout.  16 columns a block rather than 32 halve the registers that hold four partials' columns in
+// flight, so twice the blocks are resident (B32 Hq128 Skv16384: step 199.6 -> 196.8 us).
 constexpr int kMaxParts = 512;
-constexpr int kCombCols = 32;
+constexpr int kCombCols = 16;
+static_assert(kCombCols % 16 == 0, "the single-pass NVFP4 encoder takes whole 16-value blocks of a row");
 
 __global__ void __launch_bounds__(kWRows) wide_combine_kernel(const __grid_constant__ WideParams p, int npairs)
 {
     __shared__ int slots[kMaxParts];
     __shared__ int nslots;
     griddep_launch_dependents();
-    griddep_wait();
+    // with uniform lengths the unit's partial slots follow from the parameters alone, so a block that
+    // starts while the wide kernel still runs computes them before the wait; else after it (prefix)
+    const bool params_only = !p.prefix && !p.seqlens;
+    if (!params_only) griddep_wait();
     const int u = blockIdx.x / (kWD / kCombCols);
     const int col0 = (blockIdx.x % (kWD / kCombCols)) * kCombCols;
     const int r = static_cast<int>(threadIdx.x);
@@ -757,6 +763,7 @@ __global__ void __launch_bounds__(kWRows) wide_combine_kernel(const __grid_const
         if (lane == 0) nslots = cnt;
     }
     __syncthreads();
+    if (params_only) griddep_wait();
     const int ns = nslots;
     if (ns < 0) return;   // the same for the whole block
     // rows beyond R (a partial row tile) compute on in-bounds workspace rows and store nothing,
@@ -845,7 +852,7 @@ __global__ void __launch_bounds__(kWRows) wide_combine_kernel(const __grid_const
     }
     if (live && col0 == 0 && p.lse) p.lse[orow] = lse_v;
     if (live && p.nv_codes) {
-        // single-pass NVFP4: the thread's 32 columns are two 16-value blocks of its row
+        // single-pass NVFP4: the thread's columns are whole 16-value blocks of its row
         const float sg = *p.nv_sg;
 #pragma unroll
         for (int b = 0; b < kCombCols / 16; ++b) {
