@@ -44,11 +44,11 @@ TRAFFIC = {
     # speculative decode B8 Hq32 Hkv8 Sq4 Skv8192 D128, causal (decode_kernel<128, 1, 1>): read 268,840,192 +
     # written 2,885,376 bytes (profiles/decode_kernel_decode-B8-H32-Skv4096-D128.md)
     "decode_kernel<128>/speculative": {"bytes": 271725568, "source_sha": "cc61cfcc3a305433"},
-    # wide-head B32 Hq128 Hkv1 Skv16384 D512, independent CTAs: read 1,081,723,648 + written 10,473,728
+    # wide-head B32 Hq128 Hkv1 Skv16384 D512, independent CTAs: read 1,081,725,440 + written 10,528,256
     # bytes (profiles/wide_kernel_wide-head-B32-Hq128-Hkv1-Skv16384-D512.md)
-    "wide_kernel<independent>": {"bytes": 1092197376, "source_sha": "eec238122760f699"},
-    # same workload, CTA-pair MMA: read 1,081,827,072 + written 10,319,872 bytes (same file)
-    "wide_kernel<pair>": {"bytes": 1092146944, "source_sha": "eec238122760f699"},
+    "wide_kernel<independent>": {"bytes": 1092253696, "source_sha": "fadaeaf162c32fa2"},
+    # same workload, CTA-pair MMA: read 1,081,820,672 + written 10,290,688 bytes (same file)
+    "wide_kernel<pair>": {"bytes": 1092111360, "source_sha": "fadaeaf162c32fa2"},
 }
 
 
