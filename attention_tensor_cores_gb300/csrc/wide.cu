@@ -20,7 +20,8 @@
 //    P(j).  The tensor pipe then alternates QK(j+1), PV(j) without waiting on the softmax.
 //  * Stream-K over keys: the tiles of all units (b, kv-head, 128-row block) are laid end to end and
 //    pair p of P takes [p*T/P, (p+1)*T/P); a run that covers a whole unit writes O and LSE,
-//    otherwise a normalised partial goes to slot unit + p and the combine kernel merges them.
+//    otherwise a normalised partial goes to slot unit + p and the combine kernel merges them.  With
+//    uniform lengths the CTA-pair variant leaves empty positions after each unit on that line.
 //    Without a workspace (no split), pair p takes whole units p, p + P, ... and writes them itself:
 //    no partials, no combine launch.
 //  * Roles: warps 0-3 softmax (one query row per thread, lazy rescale as in the row-tile kernel),
@@ -72,6 +73,12 @@ struct WCfg {
 // TMEM columns: S 0..127, P 128..191 (BF16 pairs of 128 keys; the pair variant uses 128..255, see the
 // kernel), O half 256..511.
 constexpr uint32_t kWColS = 0, kWColP = 128, kWColO = 256;
+// A pair that ends one unit and starts the next pays one more epilogue (a partial) and one more Q load
+// than a pair inside a unit.  With uniform lengths each unit can be followed by empty positions on the
+// stream-K split line, so that such pairs get fewer tiles.  Measured on B32 Hq128 Skv16384 (one GB300,
+// gaps 0-4): the CTA-pair kernel's step 232.3-233.0 -> 229.4-230.0 us with 2; the independent kernel
+// flat from 0 to 2 and slower beyond, so it keeps none.
+constexpr int kWSplitGapPair = 2;
 
 // Position of chunk c of V(j) in an item's chunk sequence K(0); K(1), V(0); ...; K(T-1), V(T-2); V(T-1).
 template <bool PAIR>
@@ -93,6 +100,7 @@ struct WideParams {
     const int32_t* seqlens;
     const int32_t* prefix;   // [U+1] tile prefix (ragged), else NULL
     int tiles_uniform;
+    int gap;            // split with uniform lengths: empty positions after each unit on the split line
     int whole_units;    // 1: no split, pair p handles units p, p + P, ... whole (no workspace)
     void* out;
     int out_f32;
@@ -134,9 +142,14 @@ __device__ __forceinline__ int wunit_tiles(const WideParams& p, int u)
     if (p.prefix) return p.prefix[u + 1] - p.prefix[u];
     return (wunit_keys(p, u) + kWKeys - 1) / kWKeys;
 }
+// Start of unit u on the stream-K split line: its tiles, then (uniform lengths) p.gap empty positions.
 __device__ __forceinline__ long long wunit_start(const WideParams& p, int u)
 {
-    return p.prefix ? static_cast<long long>(p.prefix[u]) : static_cast<long long>(u) * p.tiles_uniform;
+    return p.prefix ? static_cast<long long>(p.prefix[u]) : static_cast<long long>(u) * (p.tiles_uniform + p.gap);
+}
+__device__ __forceinline__ long long wsplit_total(const WideParams& p)
+{
+    return p.prefix ? static_cast<long long>(p.prefix[p.U]) : static_cast<long long>(p.U) * (p.tiles_uniform + p.gap);
 }
 
 struct WSched {
@@ -153,7 +166,7 @@ struct WSched {
             g1 = p->U;
             return;
         }
-        const long long T = p->prefix ? p->prefix[p->U] : static_cast<long long>(p->U) * p->tiles_uniform;
+        const long long T = wsplit_total(*p);
         g = (static_cast<long long>(pr) * T) / npairs;
         g1 = (static_cast<long long>(pr + 1) * T) / npairs;
     }
@@ -180,7 +193,13 @@ struct WSched {
             }
             uu = lo;
         } else {
-            uu = static_cast<int>(g / p->tiles_uniform);
+            const long long len = p->tiles_uniform + p->gap;
+            uu = static_cast<int>(g / len);
+            if (g - uu * len >= p->tiles_uniform) {   // in the empty positions after unit uu
+                g = (uu + 1) * len;
+                if (g >= g1) return false;
+                ++uu;
+            }
         }
         const long long s = wunit_start(*p, uu);
         const int nt = wunit_tiles(*p, uu);
@@ -739,7 +758,7 @@ __global__ void __launch_bounds__(kWRows) wide_combine_kernel(const __grid_const
         int cnt = 0;
         if (tiles > 0) {
             const long long Tu = wunit_start(p, u);
-            const long long T = p.prefix ? p.prefix[p.U] : static_cast<long long>(p.U) * p.tiles_uniform;
+            const long long T = wsplit_total(p);
             const long long P = npairs;
             const int c0 = static_cast<int>(min((((Tu + 1) * P) - 1) / T, P - 1));
             const int c1 = static_cast<int>(min((((Tu + tiles) * P) - 1) / T, P - 1));
@@ -997,6 +1016,7 @@ int launch_wide(const AttnArgs& a, int num_splits, void* ws, size_t ws_bytes, cu
     p.seqlens = a.seqlens;
     p.prefix = (a.seqlens && !whole) ? reinterpret_cast<const int32_t*>(base + w.prefix_off) : nullptr;
     p.tiles_uniform = (a.Skv + kWKeys - 1) / kWKeys;
+    p.gap = (!whole && !a.seqlens && pair) ? kWSplitGapPair : 0;
     p.whole_units = whole ? 1 : 0;
     const bool nvfp4 = a.out_kind == FMHA_OUT_NVFP4;
     p.out = nvfp4 ? nullptr : a.out;
