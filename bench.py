@@ -44,11 +44,11 @@ TRAFFIC = {
     # speculative decode B8 Hq32 Hkv8 Sq4 Skv8192 D128, causal (decode_kernel<128, 1, 1>): read 268,840,192 +
     # written 2,885,376 bytes (profiles/decode_kernel_decode-B8-H32-Skv4096-D128.md)
     "decode_kernel<128>/speculative": {"bytes": 271725568, "source_sha": "cc61cfcc3a305433"},
-    # wide-head B32 Hq128 Hkv1 Skv16384 D512, independent CTAs: read 1,081,725,440 + written 10,528,256
+    # wide-head B32 Hq128 Hkv1 Skv16384 D512, independent CTAs: read 1,081,728,512 + written 10,642,432
     # bytes (profiles/wide_kernel_wide-head-B32-Hq128-Hkv1-Skv16384-D512.md)
-    "wide_kernel<independent>": {"bytes": 1092253696, "source_sha": "fadaeaf162c32fa2"},
-    # same workload, CTA-pair MMA: read 1,081,820,672 + written 10,290,688 bytes (same file)
-    "wide_kernel<pair>": {"bytes": 1092111360, "source_sha": "fadaeaf162c32fa2"},
+    "wide_kernel<independent>": {"bytes": 1092370944, "source_sha": "b1d8fac676288ac8"},
+    # same workload, CTA-pair MMA: read 1,081,851,648 + written 10,881,280 bytes (same file)
+    "wide_kernel<pair>": {"bytes": 1092732928, "source_sha": "b1d8fac676288ac8"},
 }
 
 
