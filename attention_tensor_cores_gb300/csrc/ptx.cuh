@@ -26,19 +26,6 @@ __device__ __forceinline__ uint32_t lane_id()
     return r;
 }
 
-__device__ __forceinline__ bool elect_one()
-{
-    uint32_t pred = 0;
-    asm volatile(
-        "{\n"
-        ".reg .pred P;\n"
-        "elect.sync _|P, 0xffffffff;\n"
-        "selp.u32 %0, 1, 0, P;\n"
-        "}\n"
-        : "=r"(pred));
-    return pred != 0;
-}
-
 // ------------------------------------------------------------------------------------------
 // mbarrier
 // ------------------------------------------------------------------------------------------
@@ -600,11 +587,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
-}
-
-__device__ __forceinline__ float bf16_bits_to_float(uint16_t h)
-{
-    return __uint_as_float(static_cast<uint32_t>(h) << 16);
 }
 
 __device__ __forceinline__ uint16_t float_to_bf16_bits(float f)
