@@ -35,20 +35,20 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # reported only while those sources are unchanged.
 TRAFFIC = {
     # decode B8 H32 Sq1 Skv4096 D128 (decode_kernel<128, 0, 0>, 128 CTAs of two whole units): read
-    # 537,047,296 + written 2,819,328 bytes (profiles/decode_kernel_decode-B8-H32-Skv4096-D128.md)
-    "decode_kernel<128>": {"bytes": 539866624, "source_sha": "cc61cfcc3a305433"},
+    # 537,033,984 + written 3,251,200 bytes (profiles/decode_kernel_decode-B8-H32-Skv4096-D128.md)
+    "decode_kernel<128>": {"bytes": 540285184, "source_sha": "621d25212fa5f05b"},
     # ragged GQA decode B64 Hq32 Hkv8 Skv<=32768 D128 (decode_kernel<128, 0, 1>): the quarter-size workload
-    # (B16) read 1,005,935,104 + wrote 674,048 bytes for 1,001,226,240 algorithmic K/V bytes (1.005x); scaled
+    # (B16) read 1,005,863,936 + wrote 341,504 bytes for 1,001,226,240 algorithmic K/V bytes (1.005x); scaled
     # by the K/V bytes to the full workload's 4,106,002,432 (profiles/side-kernels_ragged-decode-wide-combine-nvfp4.md)
-    "decode_kernel<128>/ragged": {"bytes": 4128077612, "source_sha": "cc61cfcc3a305433"},
-    # speculative decode B8 Hq32 Hkv8 Sq4 Skv8192 D128, causal (decode_kernel<128, 1, 1>): read 268,840,192 +
-    # written 2,885,376 bytes (profiles/decode_kernel_decode-B8-H32-Skv4096-D128.md)
-    "decode_kernel<128>/speculative": {"bytes": 271725568, "source_sha": "cc61cfcc3a305433"},
-    # wide-head B32 Hq128 Hkv1 Skv16384 D512, independent CTAs: read 1,081,728,512 + written 10,642,432
+    "decode_kernel<128>/ragged": {"bytes": 4126422000, "source_sha": "621d25212fa5f05b"},
+    # speculative decode B8 Hq32 Hkv8 Sq4 Skv8192 D128, causal (decode_kernel<128, 1, 1>): read 268,839,168 +
+    # written 2,798,592 bytes (profiles/decode_kernel_decode-B8-H32-Skv4096-D128.md)
+    "decode_kernel<128>/speculative": {"bytes": 271637760, "source_sha": "621d25212fa5f05b"},
+    # wide-head B32 Hq128 Hkv1 Skv16384 D512, independent CTAs: read 1,081,726,464 + written 10,248,960
     # bytes (profiles/wide_kernel_wide-head-B32-Hq128-Hkv1-Skv16384-D512.md)
-    "wide_kernel<independent>": {"bytes": 1092370944, "source_sha": "b1d8fac676288ac8"},
-    # same workload, CTA-pair MMA: read 1,081,851,648 + written 10,881,280 bytes (same file)
-    "wide_kernel<pair>": {"bytes": 1092732928, "source_sha": "b1d8fac676288ac8"},
+    "wide_kernel<independent>": {"bytes": 1091975424, "source_sha": "78a9a91c90649bc2"},
+    # same workload, CTA-pair MMA: read 1,081,783,808 + written 10,341,632 bytes (same file)
+    "wide_kernel<pair>": {"bytes": 1092125440, "source_sha": "78a9a91c90649bc2"},
 }
 
 
