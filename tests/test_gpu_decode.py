@@ -184,6 +184,24 @@ def test_split_merge_in_kernel(F, B, Hq, Hkv, Skv, D):
     check_o_lse(res["o"], res["lse"], o_ref, l_ref, "in-kernel merge")
 
 
+@pytest.mark.parametrize("B,Hq,Hkv,Skv,D", [
+    (10, 15, 15, 300, 128),    # 150 units: one whole unit per CTA on 150 CTAs
+    (20, 15, 15, 200, 64),     # 300 units: two whole units per CTA on 150 CTAs
+    (2, 127, 127, 130, 128),   # 254 units: two per CTA on 127 CTAs (5/6 of 152), a one-key tail tile
+    (16, 32, 8, 500, 128),     # 128 units of four query columns: the epilogue-warpgroup kernel
+    (1, 157, 157, 400, 128),   # 157 units (prime, no divisor in range): the stream-K split stays
+])
+def test_whole_units_when_units_divide_evenly(F, B, Hq, Hkv, Skv, D):
+    """With uniform lengths the split decode launches as many CTAs as divide the units evenly when that
+    number lies between 5/6 of the SMs and all of them, and each CTA streams whole units (no partials,
+    no merge).  The shapes are chosen for 152 SMs; on any device the result must match the oracle."""
+    w = inputs.Workload("t", B, Hq, Hkv, 1, Skv, D, 1.0, "bf16", 38)
+    q, k, v, _ = w.make("cuda")
+    res = run_attention(F, q, k, v, w.scale, num_splits=0)
+    o_ref, l_ref = oracle.attention(q.cpu(), k.cpu(), v.cpu(), w.scale)
+    check_o_lse(res["o"], res["lse"], o_ref, l_ref, "whole units")
+
+
 def test_merge_counters_across_calls(F):
     """Arrival counters are tagged per call, not reset: repeated calls on one workspace (and a
     workspace first filled with arbitrary bytes) give identical results."""
