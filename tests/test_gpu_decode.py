@@ -87,7 +87,8 @@ def test_split_and_whole_agree(F):
 
 def test_decode_full_size_every_row(F):
     """B8 H32 Sq1 Skv4096 D128 (split-KV, BF16 O + LSE): every one of the 256 query rows, one per
-    (b, kv-head) unit, so every unit and every stream-K split boundary is checked."""
+    (b, kv-head) unit, so every unit is checked: on 152 SMs 128 CTAs take two whole units each; on a
+    device whose SM count gives no such divisor the units are split and every split boundary is."""
     w = inputs.workloads()[1]
     q, k, v, _ = w.make("cuda")
     res = run_attention(F, q, k, v, w.scale, num_splits=0)
