@@ -330,8 +330,10 @@ __global__ void __launch_bounds__(decode_threads<EPI>(), 1)
     // unit has several query columns, else the softmax warps themselves (barrier 1), for which the
     // epilogue is short and an extra warpgroup's handoff measured slower.  tid: O^T row (Tensor
     // Memory lane) and output column, ew: warp within the group.
+    // slots_ready: fx_n / fx_slot already hold this item's partial slots (the epilogue warpgroup finds
+    // them while it waits for the item)
     auto run_epilogue = [&](const Item& it, bool empty, const float (&m)[kN], const float (&l)[kN],
-                            const float (&acc)[kN], int tid, int ew, int bar) {
+                            const float (&acc)[kN], int tid, int ew, int bar, bool slots_ready) {
         const int lane = static_cast<int>(lane_id());
         const int G = p.G;
         const float nv_sg = p.nv_sg ? *p.nv_sg : 0.f;
@@ -419,7 +421,7 @@ __global__ void __launch_bounds__(decode_threads<EPI>(), 1)
             // fence waits for the stores instead of 128.
             named_bar_sync(bar, 128);
             if (tid == 0) {
-                const int n = unit_partial_slots(p, it.u, static_cast<int>(gridDim.x), fx_slot, kMaxFixSlots);
+                const int n = slots_ready ? fx_n : unit_partial_slots(p, it.u, static_cast<int>(gridDim.x), fx_slot, kMaxFixSlots);
                 fx_n = n;
                 __threadfence();
                 const int arrived = n > 0 ? arrive_unit(p.unit_ctr + it.u, p.gen, n) : 0;
@@ -499,6 +501,7 @@ __global__ void __launch_bounds__(decode_threads<EPI>(), 1)
                     const float wm = warp_max(amax_m);
                     if (lane == 0 && wm > 0.f) atomicMax(p.amax_bits, __float_as_uint(wm));
                 }
+                named_bar_sync(bar, 128);   // every read of fx_slot is done before thread 0 refills it
             }
         }
     };
@@ -742,7 +745,7 @@ __global__ void __launch_bounds__(decode_threads<EPI>(), 1)
             if (it.t1 > it.t0) consume(alpha_prev);
 
             if constexpr (!EPI) {
-                run_epilogue(it, it.t1 <= it.t0, m, l, acc, tid, warp, 1);
+                run_epilogue(it, it.t1 <= it.t0, m, l, acc, tid, warp, 1, false);
                 continue;
             }
             // ---- hand the item to the epilogue warpgroup: acc and the partial column sums l through
@@ -779,6 +782,10 @@ __global__ void __launch_bounds__(decode_threads<EPI>(), 1)
         const uint32_t lane_base = static_cast<uint32_t>(ew * 32) << 16;
         Ring hr(2);
         while (sched.next(it)) {   // the softmax warpgroup's sequence of items
+            // a partial's slots (64-bit divisions) while the softmax warps still stream the item, off
+            // the path from its last tile to its arrival count
+            const bool pre = p.fixup && !(it.whole && !(p.split && p.nv_codes)) && it.t1 > it.t0;
+            if (pre && tid == 0) fx_n = unit_partial_slots(p, it.u, static_cast<int>(gridDim.x), fx_slot, kMaxFixSlots);
             mbar_wait(&ep_full[hr.idx], hr.phase, wc);
             tc_fence_after();
             __syncwarp();   // tcgen05.ld is warp-collective
@@ -799,7 +806,7 @@ __global__ void __launch_bounds__(decode_threads<EPI>(), 1)
             mbar_arrive(&ep_empty[hr.idx]);
             hr.advance();
 
-            run_epilogue(it, empty, m, l, acc, tid, ew, 2);
+            run_epilogue(it, empty, m, l, acc, tid, ew, 2, pre);
         }
       }
     }
