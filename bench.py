@@ -35,15 +35,15 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # reported only while those sources are unchanged.
 TRAFFIC = {
     # decode B8 H32 Sq1 Skv4096 D128 (decode_kernel<128, 0, 0>, 128 CTAs of two whole units): read
-    # 537,033,984 + written 3,251,200 bytes (profiles/decode_kernel_decode-B8-H32-Skv4096-D128.md)
-    "decode_kernel<128>": {"bytes": 540285184, "source_sha": "621d25212fa5f05b"},
+    # 537,030,656 + written 2,818,304 bytes (profiles/decode_kernel_decode-B8-H32-Skv4096-D128.md)
+    "decode_kernel<128>": {"bytes": 539848960, "source_sha": "352c1ba17c15bf38"},
     # ragged GQA decode B64 Hq32 Hkv8 Skv<=32768 D128 (decode_kernel<128, 0, 1>): the quarter-size workload
-    # (B16) read 1,005,863,936 + wrote 341,504 bytes for 1,001,226,240 algorithmic K/V bytes (1.005x); scaled
+    # (B16) read 1,005,865,216 + wrote 683,008 bytes for 1,001,226,240 algorithmic K/V bytes (1.005x); scaled
     # by the K/V bytes to the full workload's 4,106,002,432 (profiles/side-kernels_ragged-decode-wide-combine-nvfp4.md)
-    "decode_kernel<128>/ragged": {"bytes": 4126422000, "source_sha": "621d25212fa5f05b"},
-    # speculative decode B8 Hq32 Hkv8 Sq4 Skv8192 D128, causal (decode_kernel<128, 1, 1>): read 268,839,168 +
-    # written 2,798,592 bytes (profiles/decode_kernel_decode-B8-H32-Skv4096-D128.md)
-    "decode_kernel<128>/speculative": {"bytes": 271637760, "source_sha": "621d25212fa5f05b"},
+    "decode_kernel<128>/ragged": {"bytes": 4127827748, "source_sha": "352c1ba17c15bf38"},
+    # speculative decode B8 Hq32 Hkv8 Sq4 Skv8192 D128, causal (decode_kernel<128, 1, 1>): read 268,839,424 +
+    # written 2,847,232 bytes (profiles/decode_kernel_decode-B8-H32-Skv4096-D128.md)
+    "decode_kernel<128>/speculative": {"bytes": 271686656, "source_sha": "352c1ba17c15bf38"},
     # wide-head B32 Hq128 Hkv1 Skv16384 D512, independent CTAs: read 1,081,726,464 + written 10,248,960
     # bytes (profiles/wide_kernel_wide-head-B32-Hq128-Hkv1-Skv16384-D512.md)
     "wide_kernel<independent>": {"bytes": 1091975424, "source_sha": "78a9a91c90649bc2"},
