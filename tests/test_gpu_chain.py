@@ -8,7 +8,8 @@ kernel has completed.  Each chain is
     3. attn(q3) -> bufA    overwrites call 2's input (write after read)
 
 and afterwards call 2's output is compared with the FP64 oracle on call 1's output, and bufA with a
-separate call on q3 (the kernels are deterministic, so the bits must agree)."""
+separate call on q3 (the kernels are deterministic, so the bits must agree).  Each chain runs on the
+legacy default stream and on a stream the caller created."""
 import numpy as np
 import pytest
 import torch
@@ -67,8 +68,9 @@ class Call:
         self.F.fmha_fwd_ex(q, k, v, self.codes if self.kind == "nvfp4" else out, self.lse, scale, self.opts)
 
 
+@pytest.mark.parametrize("stream", ["default", "created"])
 @pytest.mark.parametrize("name", list(CASES))
-def test_dependent_calls_back_to_back(F, name):
+def test_dependent_calls_back_to_back(F, name, stream):
     B, Hq, Hkv, Sq, Skv, D, causal, ragged, kind2 = CASES[name]
     w = inputs.Workload("chain", B, Hq, Hkv, Sq, Skv, D, 1.0, "bf16", 91, ragged=ragged)
     q0, k, v, sl = w.make("cuda")
@@ -79,9 +81,12 @@ def test_dependent_calls_back_to_back(F, name):
     bufA = torch.full((B, Hq, Sq, D), float("nan"), dtype=torch.bfloat16, device="cuda")
     bufB = torch.full((B, Hq, Sq, D), float("nan"), dtype=torch.bfloat16, device="cuda")
     torch.cuda.synchronize()
-    c1(q0, k, v, bufA, w.scale)
-    c2(bufA, k, v, bufB, w.scale)
-    c3(q3, k, v, bufA, w.scale)
+    side = torch.cuda.Stream() if stream == "created" else torch.cuda.current_stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):   # the library launches on the current stream
+        c1(q0, k, v, bufA, w.scale)
+        c2(bufA, k, v, bufB, w.scale)
+        c3(q3, k, v, bufA, w.scale)
     torch.cuda.synchronize()
     assert F.fmha_check_status() == 0
     got_b = (c2.f32.cpu().numpy() if kind2 == "nvfp4" else bufB.float().cpu().numpy()).reshape(-1, D)
