@@ -146,9 +146,23 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
     return fn;
 }
 
+// The driver-API encoder needs a context current on the calling thread.  The runtime makes its
+// primary context current lazily, at a thread's first call that needs one, so a host thread whose first
+// CUDA call is this library's would have none: bind the current device's primary context first (once
+// per thread; a later cudaSetDevice by the caller binds that device's).
+static void bind_primary_context()
+{
+    thread_local bool bound = false;
+    if (bound) return;
+    int dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess && cudaSetDevice(dev) == cudaSuccess) bound = true;
+    (void)cudaGetLastError();
+}
+
 int make_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
                    const uint32_t* box)
 {
+    bind_primary_context();
     auto fn = encode_fn();
     if (!fn) return set_error(FMHA_ERR_CUDA, "cuTensorMapEncodeTiled entry point not available");
     cuuint64_t gdim[5];
