@@ -1,7 +1,8 @@
 """GPU edge and degenerate cases through the C ABI: empty problems; a zero query, where every
 visible key has the same score, so O is the plain mean of the visible value rows and LSE = ln n
 (a closed form that does not depend on the keys), on every kernel path including the causal mask;
-and shapes at the edges of the dispatch and the mask against the oracle."""
+shapes at the edges of the dispatch and the mask against the oracle; and an output of more than
+2^31 elements."""
 import math
 
 import numpy as np
@@ -92,3 +93,39 @@ def test_boundary_shapes_against_oracle(F, B, Hq, Hkv, Sq, Skv, D, causal, split
     check_o_lse(res["o"], res["lse"], o_ref, l_ref, "boundary shape")
     if causal and Sq > Skv:
         assert np.isneginf(l_ref).any() and np.all(res["o"][np.isneginf(l_ref)] == 0.0)
+
+
+def test_output_beyond_2_to_31_elements(F):
+    """A prefill whose output holds more than 2^31 elements (Hq = Hkv = 72, Sq = 262144, one 128-key
+    tile, D = 128: 2.4e9 elements), so every output offset past 2^31 must be formed in 64 bits.  Rows on
+    both sides of the 2^31-element boundary and at the very end, against the oracle head by head."""
+    H, Sq, Skv, D = 72, 262144, 128, 128
+    g = torch.Generator(device="cuda").manual_seed(96)
+    q = torch.randn(1, H, Sq, D, generator=g, device="cuda").to(torch.bfloat16)
+    k = torch.randn(1, H, Skv, D, generator=g, device="cuda").to(torch.bfloat16)
+    v = torch.randn(1, H, Skv, D, generator=g, device="cuda").to(torch.bfloat16)
+    out = torch.empty(1, H, Sq, D, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(1, H, Sq, dtype=torch.float32, device="cuda")
+    scale = 1.0 / math.sqrt(D)
+    F.fmha_fwd(q, k, v, out, lse, scale)
+    torch.cuda.synchronize()
+    assert F.fmha_check_status() == 0
+    n_rows = H * Sq
+    boundary = (1 << 31) // D            # the first row whose elements start at offset 2^31
+    rng = np.random.default_rng(7)
+    rows = np.unique(np.concatenate([[0, boundary - 2, boundary - 1, boundary, boundary + 1, n_rows - 1],
+                                     rng.integers(boundary, n_rows, 24)]))
+    rows_t = torch.from_numpy(rows).cuda()
+    o = out.view(-1, D)[rows_t].float().cpu().numpy()
+    l = lse.view(-1)[rows_t].cpu().numpy()
+    qs = q.view(-1, D)[rows_t].cpu()
+    o_ref = np.zeros((len(rows), D))
+    l_ref = np.zeros(len(rows))
+    kc, vc = k.cpu(), v.cpu()
+    for h in np.unique(rows // Sq):
+        sel = np.where(rows // Sq == h)[0]
+        oh, lh = oracle.attention(qs[torch.from_numpy(sel)].view(1, 1, len(sel), D), kc[:, h:h + 1], vc[:, h:h + 1], scale)
+        o_ref[sel], l_ref[sel] = oh, lh
+    check_o_lse(o, l, o_ref, l_ref, "output beyond 2^31 elements")
+    del q, k, v, out, lse
+    torch.cuda.empty_cache()
