@@ -1,0 +1,74 @@
+"""A seeded sweep of random shapes across the dispatch: head dimension (64, 128, 512), grouping,
+query rows per head, key length, bottom-right causal mask, ragged key lengths (including empty
+sequences), output kind (BF16, FP32, NVFP4), split mode (no options, automatic split, whole units)
+and the D = 512 kernel variant.  Each case against the FP64 oracle; for NVFP4 the FP32 output against
+the oracle and the codes and scales bit-exact against the oracle's quantiser on that output.  The
+shapes are drawn once from a fixed seed, so the sweep is the same on every run."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from attention_tensor_cores_gb300 import inputs
+from attn_util import check_o_lse, run_attention
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def F():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import attention_tensor_cores_gb300 as F
+    F.load()
+    return F
+
+
+def _cases(n=200, seed=2024):
+    rng = np.random.default_rng(seed)
+    cases = []
+    while len(cases) < n:
+        D = int(rng.choice([64, 128, 512], p=[0.4, 0.4, 0.2]))
+        Hkv = int(rng.choice([1, 2, 4]))
+        Hq = Hkv * int(rng.choice([1, 2, 4, 8, 16]))
+        Sq = int(rng.choice([1, 1, 2, 4, 16, 33, 130, 300]))
+        Skv = int(rng.integers(1, 2500))
+        B = int(rng.integers(1, 4))
+        causal = bool(rng.random() < 0.4)
+        ragged = bool(rng.random() < 0.4)
+        kind = str(rng.choice(["bf16", "f32", "nvfp4"], p=[0.45, 0.35, 0.2]))
+        splits = [None, 0, 1][int(rng.integers(0, 3))]
+        variant = int(rng.integers(0, 3))           # D = 512: automatic, independent, CTA pair
+        case_seed = int(rng.integers(1, 1 << 30))
+        if B * Hq * Sq * Skv * D > 3e8:             # keep the oracle within seconds
+            continue
+        if splits is None and (kind != "bf16" or ragged or causal):
+            splits = 0                              # fmha_fwd takes no options
+        cases.append((B, Hq, Hkv, Sq, Skv, D, causal, ragged, kind, splits, variant, case_seed))
+    return cases
+
+
+CASES = _cases()
+
+
+@pytest.mark.parametrize("case", CASES, ids=[f"c{i}" for i in range(len(CASES))])
+def test_random_shape_against_oracle(F, case):
+    B, Hq, Hkv, Sq, Skv, D, causal, ragged, kind, splits, variant, seed = case
+    w = inputs.Workload("sweep", B, Hq, Hkv, Sq, Skv, D, 1.0, "bf16", seed)
+    q, k, v, _ = w.make("cuda")
+    lens = None
+    sl_t = None
+    if ragged:
+        lens = np.random.default_rng(seed).integers(0, Skv + 1, B).astype(np.int32)
+        sl_t = torch.from_numpy(lens).cuda()
+    kw = {}
+    if D == 512:
+        kw["wide_variant"] = [None, F.FMHA_WIDE_INDEPENDENT, F.FMHA_WIDE_PAIR][variant]
+    res = run_attention(F, q, k, v, w.scale, out_kind=kind, seqlens=sl_t, num_splits=splits,
+                        want_f32=(kind == "nvfp4"), causal=causal, **kw)
+    o_ref, l_ref = oracle.attention(q.cpu(), k.cpu(), v.cpu(), w.scale, seqlens_k=lens, causal=causal)
+    check_o_lse(res["o"], res["lse"], o_ref, l_ref, f"sweep {case}")
+    if kind == "nvfp4":
+        codes, scales, _ = oracle.nvfp4_quantize(res["o"].reshape(-1))
+        np.testing.assert_array_equal(res["codes"], codes)
+        np.testing.assert_array_equal(res["scales"][: scales.size], scales)
