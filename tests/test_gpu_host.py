@@ -81,3 +81,43 @@ def test_host_matches_device_call(F):
     check_o_lse(out.float().cpu().numpy().reshape(-1, w.D), lse.cpu().numpy().reshape(-1), o_ref, l_ref, "device")
     check_o_lse(o_host.float().numpy().reshape(-1, w.D), lse_host.numpy().reshape(-1), o_ref, l_ref, "host")
     np.testing.assert_allclose(o_host.float().numpy(), out.float().cpu().numpy(), atol=2e-2)
+
+
+def _host_cases(n=24, seed=515):
+    rng = np.random.default_rng(seed)
+    cases = []
+    while len(cases) < n:
+        D = int(rng.choice([64, 128, 512], p=[0.4, 0.4, 0.2]))
+        Hkv = int(rng.choice([1, 2, 4]))
+        Hq = Hkv * int(rng.choice([1, 2, 4, 8, 16]))
+        Sq = int(rng.choice([1, 1, 2, 4, 33, 130]))
+        Skv = int(rng.integers(1, 2000))
+        B = int(rng.integers(1, 9))
+        if B * Hq * Sq * Skv * D > 2e8:
+            continue
+        cases.append((B, Hq, Hkv, Sq, Skv, D, bool(rng.random() < 0.4), str(rng.choice(["bf16", "f32"])),
+                      int(rng.integers(0, 2)), int(rng.integers(1, 1 << 30))))
+    return cases
+
+
+HOST_CASES = _host_cases()
+
+
+@pytest.mark.parametrize("case", HOST_CASES, ids=[f"h{i}" for i in range(len(HOST_CASES))])
+def test_host_random_shapes(F, case):
+    """A seeded sweep of shapes through fmha_fwd_host (1 to 8 batch entries, so one to four chunks),
+    against the oracle."""
+    B, Hq, Hkv, Sq, Skv, D, causal, out, splits, seed = case
+    w = inputs.Workload("t", B, Hq, Hkv, Sq, Skv, D, 1.0, "bf16", seed)
+    q, k, v, _ = w.make("cpu")
+    q, k, v = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    kind = F.FMHA_OUT_F32 if out == "f32" else F.FMHA_OUT_BF16
+    o = torch.full((B, Hq, Sq, D), float("nan"), dtype=torch.float32 if out == "f32" else torch.bfloat16).pin_memory()
+    lse = torch.full((B, Hq, Sq), float("nan"), dtype=torch.float32).pin_memory()
+    opts = F.make_opts(kind, num_splits=splits, causal=causal)
+    buf = torch.empty(F.fmha_host_buffer_size(B, Hq, Hkv, Sq, Skv, D, opts), dtype=torch.uint8, device="cuda")
+    F.fmha_fwd_host(q, k, v, o, lse, w.scale, buf, opts)
+    torch.cuda.synchronize()
+    assert F.fmha_check_status() == 0
+    o_ref, l_ref = oracle.attention(q, k, v, w.scale, causal=causal)
+    check_o_lse(o.float().numpy().reshape(-1, D), lse.numpy().reshape(-1), o_ref, l_ref, f"host {case}")
