@@ -77,3 +77,35 @@ def test_too_large_is_refused(F):
     assert rc == F.FMHA_ERR_WORKSPACE
     assert b"static area holds" in lib.fmha_last_error()
     assert F.fmha_check_status() == 0
+
+
+def _noalloc_cases(n=16, seed=616):
+    rng = np.random.default_rng(seed)
+    cases = []
+    while len(cases) < n:
+        D = int(rng.choice([64, 128]))
+        Hkv = int(rng.choice([1, 2, 4, 8]))
+        g = int(rng.choice([1, 2, 4, 8, 16]))
+        Sq = int(rng.choice([1, 2, 4]))
+        if g * Sq > 16:
+            continue
+        cases.append((int(rng.integers(1, 9)), Hkv * g, Hkv, Sq, int(rng.integers(1, 5000)), D,
+                      bool(rng.random() < 0.5), int(rng.integers(1, 1 << 30))))
+    return cases
+
+
+NOALLOC_CASES = _noalloc_cases()
+
+
+@pytest.mark.parametrize("case", NOALLOC_CASES, ids=[f"n{i}" for i in range(len(NOALLOC_CASES))])
+def test_noalloc_random_shapes(F, case):
+    """A seeded sweep of decode shapes (up to 16 query rows per key/value head, ragged lengths with
+    empty sequences) through the allocation-free entry point, against the oracle."""
+    B, Hq, Hkv, Sq, Skv, D, ragged, seed = case
+    w = inputs.Workload("t", B, Hq, Hkv, Sq, Skv, D, 1.0, "bf16", seed)
+    q, k, v, _ = w.make("cuda")
+    lens = np.random.default_rng(seed).integers(0, Skv + 1, B).astype(np.int32) if ragged else None
+    sl = None if lens is None else torch.from_numpy(lens).cuda()
+    o, l = _noalloc(F, q, k, v, w.scale, sl)
+    o_ref, l_ref = oracle.attention(q.cpu(), k.cpu(), v.cpu(), w.scale, seqlens_k=lens)
+    check_o_lse(o, l, o_ref, l_ref, f"noalloc {case}")
