@@ -72,3 +72,35 @@ def test_random_shape_against_oracle(F, case):
         codes, scales, _ = oracle.nvfp4_quantize(res["o"].reshape(-1))
         np.testing.assert_array_equal(res["codes"], codes)
         np.testing.assert_array_equal(res["scales"][: scales.size], scales)
+
+
+SP_CASES = _cases(n=40, seed=9090)
+
+
+@pytest.mark.parametrize("case", SP_CASES, ids=[f"s{i}" for i in range(len(SP_CASES))])
+def test_random_shape_single_pass_nvfp4(F, case):
+    """Single-pass NVFP4 (a given per-tensor scale s_g, encoded in the epilogues or the combine) on
+    random shapes: s_g between 0.1 and 2 times the two-pass scale, so some blocks saturate and
+    others do not.  Codes and scales bit-exact against the oracle's encoding with that s_g of the
+    kernel's own FP32 O, and that O against the oracle."""
+    B, Hq, Hkv, Sq, Skv, D, causal, ragged, _, splits, variant, seed = case
+    w = inputs.Workload("sweep", B, Hq, Hkv, Sq, Skv, D, 1.0, "bf16", seed)
+    q, k, v, _ = w.make("cuda")
+    lens = np.random.default_rng(seed).integers(0, Skv + 1, B).astype(np.int32) if ragged else None
+    sl_t = None if lens is None else torch.from_numpy(lens).cuda()
+    ns = 0 if splits is None else splits
+    kw = {}
+    if D == 512:
+        kw["wide_variant"] = [None, F.FMHA_WIDE_INDEPENDENT, F.FMHA_WIDE_PAIR][variant]
+    two = run_attention(F, q, k, v, w.scale, out_kind="nvfp4", seqlens=sl_t, num_splits=ns, causal=causal, **kw)
+    factor = float(np.random.default_rng(seed + 1).uniform(0.1, 2.0))
+    sg = float(np.float32(two["tensor_scale"] * factor))
+    if not sg > 0.0:
+        sg = 1.0 / 2688.0   # an all-zero output (every row empty): any usable scale
+    a = run_attention(F, q, k, v, w.scale, out_kind="nvfp4", seqlens=sl_t, num_splits=ns, want_f32=True,
+                      causal=causal, nvfp4_scale=sg, **kw)
+    o_ref, l_ref = oracle.attention(q.cpu(), k.cpu(), v.cpu(), w.scale, seqlens_k=lens, causal=causal)
+    check_o_lse(a["o"], a["lse"], o_ref, l_ref, f"single-pass sweep {case}")
+    codes, scales = oracle.nvfp4_quantize_scaled(a["o"].reshape(-1), sg)
+    np.testing.assert_array_equal(a["scales"], scales)
+    np.testing.assert_array_equal(a["codes"], codes)
