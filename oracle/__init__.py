@@ -43,8 +43,12 @@ def _load():
     global _lib
     with _lock:
         if _lib is None:
-            build()
-            lib = ctypes.CDLL(_LIB_PATH)
+            # ORACLE_LIB names a prebuilt library to load instead: the mutation tests point it at
+            # copies of this oracle built with one planted mistake, which the pins must reject.
+            path = os.environ.get("ORACLE_LIB")
+            if not path:
+                path = build()
+            lib = ctypes.CDLL(path)
             P = ctypes.c_void_p
             I = ctypes.c_int
             I64 = ctypes.c_int64

@@ -181,6 +181,32 @@ def test_brute_force_arbitrary_precision():
         assert abs(float(mpmath.log(den)) - lse[0]) <= 1e-14
 
 
+def test_brute_force_batched_grouped_layout():
+    """The same 50-digit brute force over every row of a batched grouped-query problem, with no
+    library routine involved: output row (b, hq, i) uses query head hq of batch b and key/value
+    head hq // (Hq / Hkv) of the same batch, in contiguous (batch, head, sequence, dim) order."""
+    mpmath = pytest.importorskip("mpmath")
+    mpmath.mp.dps = 50
+    B, Hq, Hkv, Sq, Skv, D = 2, 4, 2, 2, 3, 2
+    q, k, v = _bf16((B, Hq, Sq, D), 110, 2.0), _bf16((B, Hkv, Skv, D), 210, 2.0), _bf16((B, Hkv, Skv, D), 310)
+    scale = 0.61
+    o, lse = oracle.attention(q, k, v, scale)
+    mp = lambda x: mpmath.mpf(float(x))
+    row = 0
+    for b in range(B):
+        for hq in range(Hq):
+            h = hq // (Hq // Hkv)
+            for i in range(Sq):
+                es = [mpmath.exp(mpmath.mpf(scale) * mpmath.fsum(mp(q[b, hq, i, d]) * mp(k[b, h, j, d]) for d in range(D)))
+                      for j in range(Skv)]
+                den = mpmath.fsum(es)
+                for d in range(D):
+                    num = mpmath.fsum(es[j] * mp(v[b, h, j, d]) for j in range(Skv))
+                    assert abs(float(num / den) - o[row, d]) <= 1e-14, (b, hq, i, d)
+                assert abs(float(mpmath.log(den)) - lse[row]) <= 1e-14, (b, hq, i)
+                row += 1
+
+
 def test_qk_raw_product():
     g = torch.Generator().manual_seed(5)
     q = torch.randint(-4, 5, (1, 16), generator=g).to(torch.bfloat16)
