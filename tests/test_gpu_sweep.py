@@ -1,4 +1,4 @@
-"""A seeded sweep of random shapes across the dispatch: head dimension (64, 128, 512), grouping,
+"""A seeded sweep of 600 random shapes across the dispatch: head dimension (64, 128, 512), grouping,
 query rows per head, key length, bottom-right causal mask, ragged key lengths (including empty
 sequences), output kind (BF16, FP32, NVFP4), split mode (no options, automatic split, whole units)
 and the D = 512 kernel variant.  Each case against the FP64 oracle; for NVFP4 the FP32 output against
@@ -24,7 +24,7 @@ def F():
     return F
 
 
-def _cases(n=200, seed=2024):
+def _cases(n=600, seed=2024):
     rng = np.random.default_rng(seed)
     cases = []
     while len(cases) < n:
@@ -74,7 +74,7 @@ def test_random_shape_against_oracle(F, case):
         np.testing.assert_array_equal(res["scales"][: scales.size], scales)
 
 
-SP_CASES = _cases(n=40, seed=9090)
+SP_CASES = _cases(n=80, seed=9090)
 
 
 @pytest.mark.parametrize("case", SP_CASES, ids=[f"s{i}" for i in range(len(SP_CASES))])
