@@ -1,9 +1,10 @@
 """A seeded sweep of 600 random shapes across the dispatch: head dimension (64, 128, 512), grouping,
 query rows per head, key length, bottom-right causal mask, ragged key lengths (including empty
 sequences), output kind (BF16, FP32, NVFP4), split mode (no options, automatic split, whole units)
-and the D = 512 kernel variant.  Each case against the FP64 oracle; for NVFP4 the FP32 output against
-the oracle and the codes and scales bit-exact against the oracle's quantiser on that output.  The
-shapes are drawn once from a fixed seed, so the sweep is the same on every run."""
+and the D = 512 kernel variant, plus 120 (and 20 single-pass) with up to 40,000 keys.  Each case
+against the FP64 oracle; for NVFP4 the FP32 output against the oracle and the codes and scales
+bit-exact against the oracle's quantiser on that output.  The shapes are drawn once from a fixed
+seed, so the sweep is the same on every run."""
 import numpy as np
 import pytest
 import torch
@@ -24,7 +25,7 @@ def F():
     return F
 
 
-def _cases(n=600, seed=2024):
+def _cases(n=600, seed=2024, skv_max=2500, cap=3e8):
     rng = np.random.default_rng(seed)
     cases = []
     while len(cases) < n:
@@ -32,7 +33,7 @@ def _cases(n=600, seed=2024):
         Hkv = int(rng.choice([1, 2, 4]))
         Hq = Hkv * int(rng.choice([1, 2, 4, 8, 16]))
         Sq = int(rng.choice([1, 1, 2, 4, 16, 33, 130, 300]))
-        Skv = int(rng.integers(1, 2500))
+        Skv = int(rng.integers(1, skv_max))
         B = int(rng.integers(1, 4))
         causal = bool(rng.random() < 0.4)
         ragged = bool(rng.random() < 0.4)
@@ -40,7 +41,7 @@ def _cases(n=600, seed=2024):
         splits = [None, 0, 1][int(rng.integers(0, 3))]
         variant = int(rng.integers(0, 3))           # D = 512: automatic, independent, CTA pair
         case_seed = int(rng.integers(1, 1 << 30))
-        if B * Hq * Sq * Skv * D > 3e8:             # keep the oracle within seconds
+        if B * Hq * Sq * Skv * D > cap:             # keep the oracle within seconds
             continue
         if splits is None and (kind != "bf16" or ragged or causal):
             splits = 0                              # fmha_fwd takes no options
@@ -74,6 +75,16 @@ def test_random_shape_against_oracle(F, case):
         np.testing.assert_array_equal(res["scales"][: scales.size], scales)
 
 
+# longer key sets (up to 40,000 keys, ten times the work per shape): long split units, deep merges
+BIG_CASES = _cases(n=120, seed=880001, skv_max=40000, cap=3e9)
+BIG_SP_CASES = _cases(n=20, seed=880002, skv_max=40000, cap=3e9)
+
+
+@pytest.mark.parametrize("case", BIG_CASES, ids=[f"b{i}" for i in range(len(BIG_CASES))])
+def test_random_long_shape_against_oracle(F, case):
+    test_random_shape_against_oracle(F, case)
+
+
 SP_CASES = _cases(n=80, seed=9090)
 
 
@@ -104,3 +115,8 @@ def test_random_shape_single_pass_nvfp4(F, case):
     codes, scales = oracle.nvfp4_quantize_scaled(a["o"].reshape(-1), sg)
     np.testing.assert_array_equal(a["scales"], scales)
     np.testing.assert_array_equal(a["codes"], codes)
+
+
+@pytest.mark.parametrize("case", BIG_SP_CASES, ids=[f"bs{i}" for i in range(len(BIG_SP_CASES))])
+def test_random_long_shape_single_pass_nvfp4(F, case):
+    test_random_shape_single_pass_nvfp4(F, case)
